@@ -1,0 +1,227 @@
+"""Pins for the fp64 oracle: checks against things other than the oracle itself.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError when the
+oracle disagrees with
+  * a library routine computing the same special case (torch's fp64
+    scaled_dot_product_attention and logsumexp on tiny shapes, block-diagonal
+    SDPA for packed sequences), or
+  * a closed form or invariant of exact attention (rows of P summing to 1,
+    a single key, all-equal scores, causal row 0, two keys, score shift,
+    permutation equivariance), or
+  * the split-K decoding identity (phase 1 + phase 2 equal full attention).
+tests/test_oracle_mutants.py plants mistakes in copies of the C source and
+checks that every one of them trips at least one pin here.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+TOL = 1e-12
+
+
+def _rand(shape, seed):
+    g = torch.Generator("cpu").manual_seed(seed)
+    return torch.randn(*shape, generator=g, dtype=torch.float64)
+
+
+def _masked_scores(q, k, scale, causal):
+    s = scale * (q @ k.transpose(-1, -2))
+    if causal:
+        Sq, Sk = s.shape[-2:]
+        keep = torch.ones(Sq, Sk, dtype=torch.bool).tril()
+        s = s.masked_fill(~keep, float("-inf"))
+    return s
+
+
+def _close(a, b, tol=TOL, what=""):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    assert a.shape == b.shape, (what, a.shape, b.shape)
+    assert np.all(np.isfinite(a)), f"{what}: non-finite values"
+    err = float(np.max(np.abs(a - b))) if a.size else 0.0
+    assert err <= tol, f"{what}: max abs err {err:.3e} > {tol:.1e}"
+
+
+def pin_sdpa(orc):
+    """torch SDPA (fp64, is_causal = top-left tril mask) and logsumexp on tiny shapes."""
+    seed = 0
+    for D in (1, 4, 64):
+        for Sq in (1, 2, 3, 17):
+            for Sk in (1, 2, 3, 17):
+                for causal in (False, True):
+                    seed += 1
+                    q, k, v = _rand((2, Sq, D), seed), _rand((2, Sk, D), seed + 500), _rand((2, Sk, D), seed + 900)
+                    scale = 0.3 + 0.1 * (seed % 7)
+                    o, lse = orc.attention(q, k, v, causal, scale)
+                    ref = F.scaled_dot_product_attention(q, k, v, is_causal=causal, scale=scale)
+                    ref_lse = torch.logsumexp(_masked_scores(q, k, scale, causal), dim=-1)
+                    _close(o, ref.numpy(), what=f"O D={D} Sq={Sq} Sk={Sk} causal={causal}")
+                    _close(lse, ref_lse.numpy(), what=f"LSE D={D} Sq={Sq} Sk={Sk} causal={causal}")
+
+
+def pin_rows_sum_to_one(orc):
+    """With V = 1 every output equals the row sum of P, which must be 1."""
+    for causal in (False, True):
+        q, k = _rand((3, 19, 8), 11), _rand((3, 23, 8), 12)
+        v = torch.ones(3, 23, 8, dtype=torch.float64)
+        o, _ = orc.attention(q, k, v, causal, 0.7)
+        _close(o, np.ones_like(o), what=f"row sums causal={causal}")
+
+
+def pin_single_key(orc):
+    """Sk = 1: O = V[0] and LSE = scale * q . k0 for every query."""
+    q, k, v = _rand((2, 5, 16), 21), _rand((2, 1, 16), 22), _rand((2, 1, 16), 23)
+    scale = 0.25
+    o, lse = orc.attention(q, k, v, False, scale)
+    _close(o, v.expand(2, 5, 16).numpy(), what="single key O")
+    _close(lse, (scale * (q @ k.transpose(-1, -2)))[..., 0].numpy(), what="single key LSE")
+
+
+def pin_equal_scores(orc):
+    """K = 0 makes every score 0: O = mean of the visible V rows, LSE = ln(#visible)."""
+    Sk, D = 9, 6
+    q, v = _rand((2, Sk, D), 31), _rand((2, Sk, D), 32)
+    k = torch.zeros(2, Sk, D, dtype=torch.float64)
+    o, lse = orc.attention(q, k, v, False, 1.3)
+    _close(o, v.mean(dim=1, keepdim=True).expand(2, Sk, D).numpy(), what="equal scores O")
+    _close(lse, np.full((2, Sk), math.log(Sk)), what="equal scores LSE")
+    o, lse = orc.attention(q, k, v, True, 1.3)
+    counts = torch.arange(1, Sk + 1, dtype=torch.float64)
+    prefix_mean = torch.cumsum(v, dim=1) / counts[None, :, None]
+    _close(o, prefix_mean.numpy(), what="equal scores causal O")
+    _close(lse, np.log(counts.numpy())[None, :].repeat(2, 0), what="equal scores causal LSE")
+
+
+def pin_causal_row0(orc):
+    """Causal row 0 sees only key 0: O[0] = V[0], LSE[0] = scale * q0 . k0."""
+    q, k, v = _rand((4, 12, 32), 41), _rand((4, 12, 32), 42), _rand((4, 12, 32), 43)
+    scale = 1 / math.sqrt(32)
+    o, lse = orc.attention(q, k, v, True, scale)
+    _close(o[:, 0], v[:, 0].numpy(), what="causal row 0 O")
+    _close(lse[:, 0], (scale * (q[:, 0] * k[:, 0]).sum(-1)).numpy(), what="causal row 0 LSE")
+
+
+def pin_two_keys(orc):
+    """Two keys: O = sigmoid(s0 - s1) V0 + sigmoid(s1 - s0) V1, LSE = log(e^s0 + e^s1)."""
+    q, k, v = _rand((1, 7, 5), 51), _rand((1, 2, 5), 52), _rand((1, 2, 5), 53)
+    scale = 0.9
+    o, lse = orc.attention(q, k, v, False, scale)
+    for i in range(7):
+        s0 = scale * float((q[0, i] * k[0, 0]).sum())
+        s1 = scale * float((q[0, i] * k[0, 1]).sum())
+        w0 = 1.0 / (1.0 + math.exp(s1 - s0))
+        w1 = 1.0 / (1.0 + math.exp(s0 - s1))
+        _close(o[0, i], (w0 * v[0, 0] + w1 * v[0, 1]).numpy(), what="two keys O")
+        mx = max(s0, s1)
+        _close(lse[0, i], mx + math.log(math.exp(s0 - mx) + math.exp(s1 - mx)), what="two keys LSE")
+
+
+def pin_shift(orc):
+    """Adding the same c to every score of a row leaves O alone and shifts LSE by c.
+    The shift is built by appending one dimension: q' = [q, 1], k' = [k, c/scale]
+    (and a zero column to V, so O keeps its first D columns)."""
+    q, k, v = _rand((2, 6, 7), 61), _rand((2, 10, 7), 62), _rand((2, 10, 7), 63)
+    scale, c = 0.5, 3.75
+    o, lse = orc.attention(q, k, v, False, scale)
+    q2 = torch.cat([q, torch.ones(2, 6, 1, dtype=torch.float64)], -1)
+    k2 = torch.cat([k, torch.full((2, 10, 1), c / scale, dtype=torch.float64)], -1)
+    v2 = torch.cat([v, torch.zeros(2, 10, 1, dtype=torch.float64)], -1)
+    o2, lse2 = orc.attention(q2, k2, v2, False, scale)
+    _close(o2[..., :7], o, what="shift O")
+    _close(lse2, lse + c, what="shift LSE")
+
+
+def pin_permutation(orc):
+    """Non-causal attention is invariant to permuting the (key, value) pairs and
+    equivariant to permuting the queries."""
+    q, k, v = _rand((3, 11, 9), 71), _rand((3, 13, 9), 72), _rand((3, 13, 9), 73)
+    o, lse = orc.attention(q, k, v, False, 0.6)
+    pk = torch.randperm(13, generator=torch.Generator().manual_seed(5))
+    pq = torch.randperm(11, generator=torch.Generator().manual_seed(6))
+    o2, lse2 = orc.attention(q, k[:, pk], v[:, pk], False, 0.6)
+    _close(o2, o, what="key permutation O")
+    _close(lse2, lse, what="key permutation LSE")
+    o3, lse3 = orc.attention(q[:, pq], k, v, False, 0.6)
+    _close(o3, o[:, pq.numpy()], what="query permutation O")
+    _close(lse3, lse[:, pq.numpy()], what="query permutation LSE")
+
+
+def pin_rows_subset(orc):
+    """Evaluating a subset of rows gives exactly those rows of the full result."""
+    q, k, v = _rand((2, 40, 8), 81), _rand((2, 40, 8), 82), _rand((2, 40, 8), 83)
+    rows = [0, 7, 39, 13, 13]
+    for causal in (False, True):
+        o, lse = orc.attention(q, k, v, causal, 0.4)
+        os_, ls_ = orc.attention(q, k, v, causal, 0.4, rows=rows)
+        _close(os_, o[:, rows], tol=0.0, what="row subset O")
+        _close(ls_, lse[:, rows], tol=0.0, what="row subset LSE")
+
+
+def pin_partials_definition(orc):
+    """Phase-1 partials: m_s is the largest scaled score in partition s,
+    O_s / l_s is exact attention over that partition's keys and
+    m_s + ln l_s its LSE (checked with torch SDPA / logsumexp); an empty
+    partition has m = -inf, l = 0, O = 0."""
+    D = 8
+    for Sk, S in ((100, 32), (17, 5), (64, 4), (7, 7)):
+        q, k, v = _rand((3, 1, D), 91 + Sk), _rand((3, Sk, D), 92 + Sk), _rand((3, Sk, D), 93 + Sk)
+        scale = 1 / math.sqrt(D)
+        op, mp, lp = orc.splitkv_partials(q, k, v, S, scale)
+        P = -(-Sk // S)
+        for s in range(S):
+            lo, hi = s * P, min(s * P + P, Sk)
+            if lo >= hi:
+                assert np.all(mp[:, s] == -np.inf) and np.all(lp[:, s] == 0) and np.all(op[:, s] == 0)
+                continue
+            ks, vs = k[:, lo:hi], v[:, lo:hi]
+            scores = scale * (q @ ks.transpose(-1, -2))[:, 0]
+            _close(mp[:, s], scores.max(-1).values.numpy(), what="partial max")
+            ref = F.scaled_dot_product_attention(q, ks, vs, scale=scale)[:, 0]
+            _close(op[:, s] / lp[:, s, None], ref.numpy(), what="partial O/l")
+            _close(mp[:, s] + np.log(lp[:, s]), torch.logsumexp(scores, -1).numpy(), what="partial LSE")
+
+
+def pin_merge_identity(orc):
+    """Phase 2 applied to phase 1 equals full attention (uneven, single and empty partitions)."""
+    D = 16
+    for Sk, S in ((100, 32), (17, 5), (256, 1), (7, 7), (300, 8)):
+        q, k, v = _rand((4, 1, D), 101 + Sk), _rand((4, Sk, D), 102 + Sk), _rand((4, Sk, D), 103 + Sk)
+        scale = 1 / math.sqrt(D)
+        op, mp, lp = orc.splitkv_partials(q, k, v, S, scale)
+        o, lse = orc.splitkv_merge(op, mp, lp)
+        ref = F.scaled_dot_product_attention(q, k, v, scale=scale)[:, 0]
+        ref_lse = torch.logsumexp(scale * (q @ k.transpose(-1, -2))[:, 0], -1)
+        _close(o, ref.numpy(), what=f"merge O Sk={Sk} S={S}")
+        _close(lse, ref_lse.numpy(), what=f"merge LSE Sk={Sk} S={S}")
+
+
+def pin_varlen_block_diag(orc):
+    """Packed sequences equal SDPA over the whole packed stream with a
+    block-diagonal mask (causal inside each block); LSE is laid out [H, T]."""
+    lengths = [5, 1, 17, 9]
+    H, D = 3, 8
+    T = sum(lengths)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    q, k, v = _rand((T, H, D), 111), _rand((T, H, D), 112), _rand((T, H, D), 113)
+    scale = 0.45
+    for causal in (False, True):
+        o, lse = orc.attention_varlen(q, k, v, cu, cu, causal, scale)
+        seg = torch.repeat_interleave(torch.arange(len(lengths)), torch.tensor(lengths))
+        pos = torch.cat([torch.arange(n) for n in lengths])
+        keep = seg[:, None] == seg[None, :]
+        if causal:
+            keep &= pos[None, :] <= pos[:, None]
+        qh, kh, vh = (x.transpose(0, 1) for x in (q, k, v))  # [H, T, D]
+        ref = F.scaled_dot_product_attention(qh, kh, vh, attn_mask=keep, scale=scale).transpose(0, 1)
+        s = (scale * qh @ kh.transpose(-1, -2)).masked_fill(~keep, float("-inf"))
+        _close(o, ref.numpy(), what=f"varlen O causal={causal}")
+        _close(lse, torch.logsumexp(s, -1).numpy(), what=f"varlen LSE causal={causal}")
+
+
+PINS = [pin_sdpa, pin_rows_sum_to_one, pin_single_key, pin_equal_scores, pin_causal_row0,
+        pin_two_keys, pin_shift, pin_permutation, pin_rows_subset, pin_partials_definition,
+        pin_merge_identity, pin_varlen_block_diag]

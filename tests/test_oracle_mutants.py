@@ -1,0 +1,55 @@
+"""Mutation check of the oracle's pins.
+
+Each case copies the committed C oracle, plants one plausible mistake in the
+copy (a dropped term, a wrong sign or index, a transposed operand, a wrong
+mask), compiles it on the CPU and requires that at least one pin rejects it.
+The committed oracle itself is never modified.
+"""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import PINS
+
+MUTANTS = [
+    ("dropped scale", "S[(size_t)r * Sk + j] = scale * dot;", "S[(size_t)r * Sk + j] = dot;"),
+    ("mask hides the past", "for (int j = i + 1; j < Sk; ++j) S[(size_t)r * Sk + j] = -INFINITY;",
+     "for (int j = 0; j < i && j < Sk; ++j) S[(size_t)r * Sk + j] = -INFINITY;"),
+    ("mask hides the diagonal", "for (int j = i + 1; j < Sk; ++j) S[(size_t)r * Sk + j] = -INFINITY;",
+     "for (int j = i; j < Sk; ++j) S[(size_t)r * Sk + j] = -INFINITY;"),
+    ("K used as V", "acc += P[(size_t)r * Sk + j] * v[(size_t)j * D + d];",
+     "acc += P[(size_t)r * Sk + j] * k[(size_t)j * D + d];"),
+    ("transposed scores", "dot += q[(size_t)i * D + d] * k[(size_t)j * D + d];",
+     "dot += q[(size_t)(j % Sq) * D + d] * k[(size_t)(i % Sk) * D + d];"),
+    ("dropped last dimension", "for (int d = 0; d < D; ++d) dot += q[(size_t)i * D + d]",
+     "for (int d = 0; d < D - 1; ++d) dot += q[(size_t)i * D + d]"),
+    ("no normalisation", "P[(size_t)r * Sk + j] /= l;", "P[(size_t)r * Sk + j] /= 1.0;"),
+    ("LSE without the max", "lse[r] = m + log(l);", "lse[r] = log(l);"),
+    ("softmax without max subtraction", "P[(size_t)r * Sk + j] = exp(S[(size_t)r * Sk + j] - m);",
+     "P[(size_t)r * Sk + j] = exp(S[(size_t)r * Sk + j]);"),
+    ("partition size rounded down", "const int P = (Sk + num_splits - 1) / num_splits;",
+     "const int P = Sk / num_splits;"),
+    ("partial max unscaled", "if (scale * dot > m) m = scale * dot;", "if (dot > m) m = dot;"),
+    ("merge weight without max", "acc += exp(m_part[s] - mg) / lg * o_part[(size_t)s * D + d];",
+     "acc += 1.0 / lg * o_part[(size_t)s * D + d];"),
+    ("merge LSE sign", "*lse = mg + log(lg);", "*lse = mg - log(lg);"),
+    ("merge sum unweighted", "lg += exp(m_part[s] - mg) * l_part[s];", "lg += l_part[s];"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_reject_mutant(name, old, new, tmp_path):
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, f"mutation site not found exactly once: {old!r}"
+    path = os.path.join(tmp_path, "mutant.c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    mutant = oracle.Oracle(oracle.compile_source(path, os.path.join(tmp_path, "libmutant.so")))
+    caught = []
+    for pin in PINS:
+        try:
+            pin(mutant)
+        except (AssertionError, ValueError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin rejects the mutant '{name}'"

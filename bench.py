@@ -1,0 +1,508 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic inputs:
+  * prefill: FlashAttention-2 forward, B=1 H=32 Sq=Sk=4096 D=128 bf16, causal
+    (the LLaMA-7B prefill shape of the pages' benchmark table), and
+  * decode: split-KV decoding, B=16 H=8 Sk=8192 D=128 bf16, 32 partitions,
+    phase 1 + log-sum-exp merge.
+The headline `value` is prefill attention TFLOPS (causal FLOPs counted at half
+of 4*B*H*S^2*D); the decode throughput in GB/s (K and V read once, plus q and
+O) sits in the `decode` object. Inputs are resident in HBM, and L2 is flushed
+(a 256 MiB write) before every step, outside the timed kernels. Each kernel is
+timed with CUDA events on the stream it is launched on.
+
+`--impl reference` times the fp64 CPU oracle instead (a bounded sample of the
+same workload per step) with the same metric and unit.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 launch under torchrun: every rank runs its own replica of the
+workload (no data-path communication; weak scaling) and rank 0 reports the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd TFLOPS & % bf16 tensor peak; split-KV decode HBM GB/s & % peak"
+PREFILL = "llama_prefill"
+DECODE = "decode"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["exact_attention_54_gb300/csrc/fa_fwd_kernel.cuh", "exact_attention_54_gb300/csrc/sm103_ptx.cuh",
+                  "exact_attention_54_gb300/csrc/fa_decode.cu"]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=50, help="steps of the end-to-end (host buffer) loop")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------- environment --
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS if k in p}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return {}
+    with open(path) as f:
+        t = json.load(f)
+    if t.get("kernel_source_hash") != kernel_source_hash():
+        return {}
+    return t.get("per_launch_bytes", {})
+
+
+def aggregate_max(values, world):
+    """Element-wise max over ranks (timings: the slowest rank decides)."""
+    if world == 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64)
+    if dist.get_backend() == "nccl":
+        t = t.cuda()
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.cpu().tolist()
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed loop runs."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu), "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def _snapshot(self):
+        try:
+            out = subprocess.run(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                  "-i", str(self.gpu)], capture_output=True, text=True, timeout=20).stdout
+            return [ln for ln in out.splitlines() if ln.strip()]
+        except (OSError, subprocess.SubprocessError):
+            return []
+
+    def stop(self, t_begin: float, t_end: float):
+        """Summarise the samples stamped inside [t_begin, t_end] (time.time())."""
+        import datetime
+        lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=10)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            with open(self.path) as f:
+                lines = [ln for ln in f.read().splitlines() if ln.strip()]
+        if self.path:
+            os.unlink(self.path)
+        source = "during"
+        if not lines:
+            lines, source = self._snapshot(), "after"
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        inside = []
+        for ln in lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            inside.append((ts is not None and t_begin <= ts <= t_end, f))
+        if source == "during" and any(ok for ok, _ in inside):
+            rows = [f for ok, f in inside if ok]
+        else:  # no sample fell inside the loop: keep what there is, and say so
+            rows = [f for _, f in inside]
+            if source == "during":
+                source = "around"
+        for f in rows:
+            try:
+                sm.append(float(f[2]))
+                mx.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[6:10]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "when": source}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "when": source}
+
+
+# ------------------------------------------------------------------ oracle --
+
+_INPUT_CACHE = {}
+
+
+def _cached_inputs(w):
+    from exact_attention_54_gb300 import inputs
+    if w.name not in _INPUT_CACHE:
+        _INPUT_CACHE[w.name] = inputs.make_workload(w)
+    return _INPUT_CACHE[w.name]
+
+
+def oracle_rate(w, target_s: float):
+    """Time the fp64 oracle, as it stands, on a bounded sample of workload w:
+    one head per host thread, a strided subset of query rows in each. Returns
+    (TFLOPS of useful attention work, threads, description, seconds)."""
+    import oracle
+    from exact_attention_54_gb300 import inputs
+    from exact_attention_54_gb300.metrics import attention_flops
+
+    threads = oracle.default_threads()
+    heads = min(threads, w.B * w.H)
+    q, k, v = _cached_inputs(w)
+    q = q.reshape(-1, w.Sq, w.D)[:heads]
+    k = k.reshape(-1, w.Sk, w.D)[:heads]
+    v = v.reshape(-1, w.Sk, w.D)[:heads]
+
+    def useful(rows):
+        keys = [min(r + 1, w.Sk) if w.causal else w.Sk for r in rows]
+        return sum(4.0 * n * w.D for n in keys) * heads
+
+    probe = list(range(0, w.Sq, max(1, w.Sq // 8)))[:8]
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.causal, w.scale, rows=probe, nthreads=threads)
+    per_row = (time.perf_counter() - t0) / len(probe)
+    n = int(max(1, min(w.Sq, target_s / max(per_row, 1e-9))))
+    stride = max(1, w.Sq // n)
+    rows = list(range(0, w.Sq, stride))[:n]
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.causal, w.scale, rows=rows, nthreads=threads)
+    dt = time.perf_counter() - t0
+    assert attention_flops(1, 1, w.Sq, w.Sk, w.D, w.causal) > 0
+    desc = (f"{heads} of {w.B * w.H} heads x {len(rows)} of {w.Sq} query rows (stride {stride}) of {w.name}; "
+            f"fp64, S and P materialised per row; untuned C oracle")
+    return useful(rows) / dt / 1e12, threads, desc, dt
+
+
+def oracle_decode_rate(w, target_s: float):
+    """fp64 oracle on a bounded sample of the decode workload (heads x all keys),
+    as GB/s of the K/V bytes the sample covers."""
+    import oracle
+    from exact_attention_54_gb300 import inputs
+
+    threads = oracle.default_threads()
+    q, k, v = _cached_inputs(w)
+    q = q.reshape(-1, 1, w.D)
+    k = k.reshape(-1, w.Sk, w.D)
+    v = v.reshape(-1, w.Sk, w.D)
+    t0 = time.perf_counter()
+    oracle.attention(q[:threads], k[:threads], v[:threads], False, w.scale, nthreads=threads)
+    per_head = (time.perf_counter() - t0) / min(threads, q.shape[0])
+    heads = int(max(1, min(q.shape[0], target_s / max(per_head, 1e-9))))
+    t0 = time.perf_counter()
+    oracle.attention(q[:heads], k[:heads], v[:heads], False, w.scale, nthreads=threads)
+    dt = time.perf_counter() - t0
+    nbytes = heads * (2 * w.Sk * w.D + 2 * w.D) * 2
+    return nbytes / dt / 1e9, threads, f"{heads} of {q.shape[0]} heads of {w.name} (all keys), fp64 oracle", dt
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 oracle on the host cores, same metric/unit."""
+    if rank != 0:
+        return None
+    from exact_attention_54_gb300 import inputs
+    w = inputs.WORKLOADS[PREFILL]
+    budget = min(10.0, 120.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_rate(w, budget)
+    rates, secs = [], []
+    desc, threads = "", 1
+    for _ in range(args.steps):
+        r, threads, desc, dt = oracle_rate(w, budget)
+        rates.append(r)
+        secs.append(dt)
+    value = statistics.median(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_block(),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                         "sample": f"per step: {desc}"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def config_block():
+    return {"workload": "llama7b_prefill_b1h32s4096d128_bf16_causal + decode_b16h8sk8192d128_bf16_split32",
+            "prefill": {"B": 1, "H": 32, "Sq": 4096, "Sk": 4096, "D": 128, "dtype": "bf16", "causal": True,
+                        "scale": "1/sqrt(128)"},
+            "decode": {"B": 16, "H": 8, "Sq": 1, "Sk": 8192, "D": 128, "dtype": "bf16", "num_splits": 32},
+            "l2": "flushed before every step (256 MiB write, outside the timed kernels)",
+            "inputs": "seeded i.i.d. N(0,1), resident in HBM"}
+
+
+# --------------------------------------------------------------------- GPU --
+
+def run_gpu(args, rank, world, local):
+    import torch
+
+    import exact_attention_54_gb300 as fa
+    from exact_attention_54_gb300 import inputs
+    from exact_attention_54_gb300.metrics import attention_flops, decode_bytes
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    fa.load_library()
+
+    wp = inputs.WORKLOADS[PREFILL]
+    wd = inputs.WORKLOADS[DECODE]
+    q, k, v = (t.to(dev) for t in inputs.make_workload(wp))
+    o = torch.empty_like(q)
+    lse = torch.empty(wp.B, wp.H, wp.Sq, dtype=torch.float32, device=dev)
+    dq, dk, dv = (t.to(dev) for t in inputs.make_workload(wd))
+    S = wd.num_splits
+    ws = (torch.empty(wd.B, wd.H, S, wd.D, dtype=torch.float32, device=dev),
+          torch.empty(wd.B, wd.H, S, dtype=torch.float32, device=dev),
+          torch.empty(wd.B, wd.H, S, dtype=torch.float32, device=dev))
+    do = torch.empty(wd.B, wd.H, 1, wd.D, dtype=wd.dtype, device=dev)
+    dlse = torch.empty(wd.B, wd.H, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    pf_flops = attention_flops(wp.B, wp.H, wp.Sq, wp.Sk, wp.D, wp.causal)
+    dc_bytes = decode_bytes(wd.B, wd.H, wd.Sk, wd.D)
+
+    def step(evs=None):
+        flush.fill_(float(1.0))
+        if evs:
+            evs[0].record(stream)
+        fa.fa_fwd(q, k, v, o, lse, wp.causal, wp.scale, stream)
+        if evs:
+            evs[1].record(stream)
+        fa.fa_decode_splitkv(dq, dk, dv, *ws, S, wd.scale, stream)
+        if evs:
+            evs[2].record(stream)
+        fa.fa_splitkv_merge(*ws, do, dlse, stream)
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # nvidia-smi start-up; samples before t_begin are discarded
+    t_begin = time.time()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(events[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    t_end = time.time()
+    if world > 1:
+        dist.barrier()
+    clock = clocks.stop(t_begin, t_end)
+    fa.fa_check_device_error()
+
+    pf = [e[0].elapsed_time(e[1]) for e in events]  # ms
+    sp = [e[1].elapsed_time(e[2]) for e in events]
+    mg = [e[2].elapsed_time(e[3]) for e in events]
+    pf_sum, sp_sum, mg_sum = sum(pf), sum(sp), sum(mg)
+    pf_sum, dc_sum, wall = aggregate_max([pf_sum, sp_sum + mg_sum, wall], world)
+    K = args.steps
+    prefill_tflops = world * pf_flops * K / (pf_sum * 1e-3) / 1e12
+    decode_gbs = world * dc_bytes * K / (dc_sum * 1e-3) / 1e9
+
+    # end-to-end through host buffers (pinned), copies inside the timed region
+    e2e = run_e2e(args, fa, torch, stream, dev, wp, wd, (q, k, v), (dq, dk, dv), world)
+
+    peaks, peak_src = load_peaks()
+    traffic = committed_traffic()
+    pf_avg_ms = statistics.mean(pf)
+    sp_avg_ms = statistics.mean(sp)
+    achieved_tf = pf_flops / (pf_avg_ms * 1e-3) / 1e12
+    achieved_gbs = dc_bytes / ((sp_avg_ms + statistics.mean(mg)) * 1e-3) / 1e9
+    split_gbs = dc_bytes / (sp_avg_ms * 1e-3) / 1e9
+    tb = traffic.get("fa_fwd_kernel")
+    line = {
+        "metric": METRIC, "value": prefill_tflops, "unit": "TFLOPS", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": (pf_sum + dc_sum) / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_block(),
+        "roofline": {"bound": "tensor", "kernel": "fa_fwd_kernel<128,bf16,causal>", "achieved": achieved_tf,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved_tf / peaks["bf16_tflops"],
+                     "traffic": tb, "peak_source": f"{peak_src} bf16 dense (burst)",
+                     "frac_of_sustained": achieved_tf / peaks["bf16_tflops_sustained"],
+                     "per_launch_flops": pf_flops, "avg_launch_ms": pf_avg_ms},
+        "decode": {
+            "metric": "split-KV decode HBM GB/s", "value": decode_gbs, "unit": "GB/s",
+            "ms_per_step": dc_sum / K, "split_ms": sp_avg_ms, "merge_ms": statistics.mean(mg),
+            "roofline": {"bound": "hbm", "kernel": "fa_decode_split_kernel<128,bf16> + fa_splitkv_merge_kernel",
+                         "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved_gbs / peaks["hbm_gbs"], "frac_of_8000_nominal": achieved_gbs / 8000.0,
+                         "split_only_gbs": split_gbs, "split_only_frac": split_gbs / peaks["hbm_gbs"],
+                         "traffic": traffic.get("fa_decode_split_kernel"), "peak_source": f"{peak_src} copy",
+                         "per_step_bytes": dc_bytes},
+            "e2e": e2e["decode"],
+        },
+        "e2e": e2e["prefill"],
+        "gpu_launches": 3 * K,
+        "clocks": clock,
+        "wall_ms_per_step": 1e3 * wall / K,
+    }
+    return line
+
+
+def run_e2e(args, fa, torch, stream, dev, wp, wd, pre, dec, world):
+    """Same metrics through the public API from pinned host buffers: every step
+    copies its inputs host->device, runs the kernels and reads the outputs back."""
+    from exact_attention_54_gb300.metrics import attention_flops, decode_bytes
+    n = max(1, min(args.e2e_steps, args.steps))
+    hq, hk, hv = (t.cpu().pin_memory() for t in pre)
+    ho = torch.empty(wp.B, wp.H, wp.Sq, wp.D, dtype=wp.dtype).pin_memory()
+    hl = torch.empty(wp.B, wp.H, wp.Sq, dtype=torch.float32).pin_memory()
+    q, k, v = (torch.empty_like(t, device=dev) for t in pre)
+    o = torch.empty_like(q)
+    lse = torch.empty(wp.B, wp.H, wp.Sq, dtype=torch.float32, device=dev)
+    S = wd.num_splits
+    gq, gk, gv = (t.cpu().pin_memory() for t in dec)
+    dq, dk, dv = (torch.empty_like(t, device=dev) for t in dec)
+    ws = (torch.empty(wd.B, wd.H, S, wd.D, dtype=torch.float32, device=dev),
+          torch.empty(wd.B, wd.H, S, dtype=torch.float32, device=dev),
+          torch.empty(wd.B, wd.H, S, dtype=torch.float32, device=dev))
+    do = torch.empty(wd.B, wd.H, 1, wd.D, dtype=wd.dtype, device=dev)
+    dlse = torch.empty(wd.B, wd.H, dtype=torch.float32, device=dev)
+    hdo = torch.empty(wd.B, wd.H, 1, wd.D, dtype=wd.dtype).pin_memory()
+    hdl = torch.empty(wd.B, wd.H, dtype=torch.float32).pin_memory()
+
+    def pre_step():
+        for d, h in ((q, hq), (k, hk), (v, hv)):
+            d.copy_(h, non_blocking=True)
+        fa.fa_fwd(q, k, v, o, lse, wp.causal, wp.scale, stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    def dec_step():
+        for d, h in ((dq, gq), (dk, gk), (dv, gv)):
+            d.copy_(h, non_blocking=True)
+        fa.fa_decode_splitkv(dq, dk, dv, *ws, S, wd.scale, stream)
+        fa.fa_splitkv_merge(*ws, do, dlse, stream)
+        hdo.copy_(do, non_blocking=True)
+        hdl.copy_(dlse, non_blocking=True)
+
+    out = {}
+    for name, fn in (("prefill", pre_step), ("decode", dec_step)):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            fn()
+        torch.cuda.synchronize()
+        dt = aggregate_max([time.perf_counter() - t0], world)[0]
+        if name == "prefill":
+            val = world * attention_flops(wp.B, wp.H, wp.Sq, wp.Sk, wp.D, wp.causal) * n / dt / 1e12
+            h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+            d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+            out[name] = {"value": val, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                         "steps": n, "ms_per_step": 1e3 * dt / n}
+        else:
+            val = world * decode_bytes(wd.B, wd.H, wd.Sk, wd.D) * n / dt / 1e9
+            h2d = sum(t.numel() * t.element_size() for t in (gq, gk, gv))
+            d2h = hdo.numel() * hdo.element_size() + hdl.numel() * hdl.element_size()
+            out[name] = {"value": val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                         "steps": n, "ms_per_step": 1e3 * dt / n}
+    return out
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            line = run_reference(args, rank, world)
+        else:
+            line = run_gpu(args, rank, world, local)
+            if rank == 0 and line is not None and not args.no_cpu_baseline:
+                from exact_attention_54_gb300 import inputs
+                r, threads, desc, dt = oracle_rate(inputs.WORKLOADS[PREFILL], args.cpu_seconds)
+                line["cpu_baseline"] = {"value": r, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                                        "sample": desc, "seconds": dt}
+                r2, t2, desc2, dt2 = oracle_decode_rate(inputs.WORKLOADS[DECODE], args.cpu_seconds / 3)
+                line["decode"]["cpu_baseline"] = {"value": r2, "unit": "GB/s", "cores": t2, "kind": "oracle",
+                                                  "sample": desc2, "seconds": dt2}
+        if rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

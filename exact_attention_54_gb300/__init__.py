@@ -1,1 +1,200 @@
-"""GB300-native exact attention (FlashAttention-2 forward, varlen, split-KV decode)."""
+"""GB300-native exact attention: FlashAttention-2 forward (dense and packed
+varlen, causal or not, with per-row LSE) and split-KV decoding with a
+log-sum-exp merge, as hand-written sm_103a kernels behind the C ABI declared in
+include/fa.h.
+
+This module is the thin Python binding over libfa.so: the functions named like
+the C entry points (``fa_fwd``, ``fa_fwd_varlen``, ``fa_decode_splitkv``,
+``fa_splitkv_merge``) only marshal torch CUDA tensors into pointers and sizes
+and check the returned status. ``flash_attention``, ``flash_attention_varlen``
+and ``flash_decode`` additionally allocate the outputs (and the decode
+workspace) with torch. Every step of the computation runs in the library's
+kernels; there is no fallback. If libfa.so is missing, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+__all__ = ["FAError", "fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_splitkv_merge",
+           "fa_check_device_error", "fa_status_string", "flash_attention", "flash_attention_varlen",
+           "flash_decode", "library_path", "load_library", "EXPORTED_SYMBOLS"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libfa.so")
+_lock = threading.Lock()
+_lib = None
+
+FA_FP16, FA_BF16 = 0, 1
+FA_MAX_SPLITS = 1024
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_splitkv_merge",
+                    "fa_check_device_error", "fa_status_string", "fa_version")
+
+
+class FAError(RuntimeError):
+    """A libfa entry point returned a non-zero status."""
+
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: status {status} ({msg})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libfa.so (declares the argument types of every entry point)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is not built: run exact_attention_54_gb300.build.build() "
+                               "(or __graft_entry__.build()) first")
+        lib = ctypes.CDLL(p)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
+        lib.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        lib.fa_splitkv_merge.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp]
+        lib.fa_check_device_error.argtypes = [vp]
+        lib.fa_status_string.argtypes = [i]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_version.argtypes = []
+        for name in ("fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_splitkv_merge",
+                     "fa_check_device_error", "fa_version"):
+            getattr(lib, name).restype = ctypes.c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def fa_status_string(status: int) -> str:
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise FAError(fn, status, fa_status_string(status))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return FA_FP16
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: expected float16 or bfloat16")
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need_contig(*ts):
+    for t in ts:
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+# ------------------------------------------------------------- entry points --
+
+def fa_fwd(q, k, v, o, lse, causal: bool, scale: float | None = None, stream=None):
+    """Dense forward: q, o [B,H,Sq,D]; k, v [B,H,Sk,D]; lse [B,H,Sq] fp32."""
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    _need_contig(q, k, v, o, lse)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    st = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sq, Sk, D, int(bool(causal)),
+                               float(scale), _dtype_code(q), _stream(stream))
+    _check("fa_fwd", st)
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal: bool,
+                  scale: float | None = None, stream=None):
+    """Packed forward: q, o [total_q,H,D]; k, v [total_k,H,D]; lse [H,total_q];
+    cu_seqlens_* int32 CUDA tensors of length num_seqs+1."""
+    Tq, H, D = q.shape
+    Tk = k.shape[0]
+    _need_contig(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k)
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    st = load_library().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q),
+                                      _ptr(cu_seqlens_k), cu_seqlens_q.numel() - 1, Tq, Tk, int(max_seqlen_q), H,
+                                      D, int(bool(causal)), float(scale), _dtype_code(q), _stream(stream))
+    _check("fa_fwd_varlen", st)
+
+
+def fa_decode_splitkv(q, k, v, o_part, m_part, l_part, num_splits: int, scale: float | None = None, stream=None):
+    """Phase 1: q [B,H,1,D] (or [B,H,D]); k, v [B,H,Sk,D]; o_part [B,H,S,D],
+    m_part and l_part [B,H,S] fp32."""
+    B, H, Sk, D = k.shape
+    _need_contig(q, k, v, o_part, m_part, l_part)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    st = load_library().fa_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o_part), _ptr(m_part), _ptr(l_part),
+                                          B, H, Sk, D, int(num_splits), float(scale), _dtype_code(k),
+                                          _stream(stream))
+    _check("fa_decode_splitkv", st)
+
+
+def fa_splitkv_merge(o_part, m_part, l_part, o, lse, stream=None):
+    """Phase 2: partials from phase 1 -> o [B,H,1,D] (16-bit), lse [B,H] fp32."""
+    B, H, S, D = o_part.shape
+    _need_contig(o_part, m_part, l_part, o, lse)
+    st = load_library().fa_splitkv_merge(_ptr(o_part), _ptr(m_part), _ptr(l_part), _ptr(o), _ptr(lse), B, H, D,
+                                         S, _dtype_code(o), _stream(stream))
+    _check("fa_splitkv_merge", st)
+
+
+def fa_check_device_error(stream=None):
+    """Synchronise the stream and raise if a kernel abandoned a barrier wait."""
+    _check("fa_check_device_error", load_library().fa_check_device_error(_stream(stream)))
+
+
+# ------------------------------------------------------ allocating helpers --
+
+def flash_attention(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Returns (o, lse) for dense [B,H,S,D] CUDA tensors."""
+    B, H, Sq, D = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def flash_attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal: bool = False,
+                           scale: float | None = None, stream=None):
+    """Returns (o [total_q,H,D], lse [H,total_q]) for packed sequences."""
+    Tq, H, D = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty(H, Tq, dtype=torch.float32, device=q.device)
+    fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, causal, scale, stream)
+    return o, lse
+
+
+def flash_decode(q, k, v, num_splits: int, scale: float | None = None, stream=None, workspace=None):
+    """Split-KV decoding (phase 1 + phase 2). Returns (o [B,H,1,D], lse [B,H]).
+    ``workspace`` may pass preallocated (o_part, m_part, l_part)."""
+    B, H, Sk, D = k.shape
+    if workspace is None:
+        workspace = (torch.empty(B, H, num_splits, D, dtype=torch.float32, device=k.device),
+                     torch.empty(B, H, num_splits, dtype=torch.float32, device=k.device),
+                     torch.empty(B, H, num_splits, dtype=torch.float32, device=k.device))
+    o_part, m_part, l_part = workspace
+    o = torch.empty(B, H, 1, D, dtype=k.dtype, device=k.device)
+    lse = torch.empty(B, H, dtype=torch.float32, device=k.device)
+    fa_decode_splitkv(q, k, v, o_part, m_part, l_part, num_splits, scale, stream)
+    fa_splitkv_merge(o_part, m_part, l_part, o, lse, stream)
+    return o, lse

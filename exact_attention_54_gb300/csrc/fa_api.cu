@@ -1,0 +1,255 @@
+// C ABI of libfa.so (declared in include/fa.h): argument validation, TMA tensor
+// map encoding and kernel launches. Allocates no memory; the only state is one
+// device-resident error word per GPU.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_launch.h"
+
+namespace {
+
+__device__ int g_device_error_word = 0;
+
+constexpr int kMaxDevices = 64;
+
+// Address of the error word on the current device (looked up once per device).
+int *device_error_word() {
+    static std::mutex mu;
+    static int *cache[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<int *>(p);
+    }
+    return cache[dev];
+}
+
+int num_sms() {
+    static std::mutex mu;
+    static int cache[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 3-D map over a 16-bit tensor whose innermost dimension is D, with 64 x 1 x
+// 128 or 64 x 128 x 1 boxes and 128-byte swizzle (rows of 128 bytes land in
+// shared memory in the layout the MMA descriptors describe). Out-of-range
+// rows read as zero.
+bool encode_map(CUtensorMap *m, bool bf16, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box1, uint32_t box2) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    const cuuint32_t box[3] = {64, box1, box2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                          const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxLen = 1 << 30;
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char *fa_status_string(fa_status_t s) {
+    switch (s) {
+        case FA_OK: return "ok";
+        case FA_ERR_NULL: return "a required pointer is NULL";
+        case FA_ERR_SHAPE: return "invalid or too large tensor shape";
+        case FA_ERR_HEADDIM: return "head dimension must be 64 or 128";
+        case FA_ERR_DTYPE: return "dtype must be FA_FP16 or FA_BF16";
+        case FA_ERR_ALIGN: return "tensor pointer is not 16-byte aligned";
+        case FA_ERR_SPLITS: return "num_splits must be in [1, min(Sk, FA_MAX_SPLITS)]";
+        case FA_ERR_SCALE: return "scale must be finite and positive";
+        case FA_ERR_CUDA: return "CUDA runtime error";
+        case FA_ERR_DEVICE_TIMEOUT: return "a kernel abandoned a barrier wait (device timeout)";
+    }
+    return "unknown status";
+}
+
+fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Sq, int Sk,
+                   int D, int causal, float scale, fa_dtype_t dtype, void *stream) {
+    if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+    if (D != 64 && D != 128) return FA_ERR_HEADDIM;
+    if (B < 1 || H < 1 || Sq < 1 || Sk < 1 || Sq > kMaxLen || Sk > kMaxLen) return FA_ERR_SHAPE;
+    const long long BH = static_cast<long long>(B) * H;
+    const long long n_pairs = ((Sq + 127) / 128 + 1) / 2;
+    if (BH > INT_MAX || BH * n_pairs > INT_MAX) return FA_ERR_SHAPE;
+    if (!scale_ok(scale)) return FA_ERR_SCALE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse)) return FA_ERR_ALIGN;
+
+    const bool bf16 = dtype == FA_BF16;
+    CUtensorMap maps[3];
+    const uint64_t row = static_cast<uint64_t>(D) * 2;
+    if (!encode_map(&maps[0], bf16, q, D, Sq, BH, row, row * Sq, 128, 1) ||
+        !encode_map(&maps[1], bf16, k, D, Sk, BH, row, row * Sk, 128, 1) ||
+        !encode_map(&maps[2], bf16, v, D, Sk, BH, row, row * Sk, 128, 1))
+        return FA_ERR_CUDA;
+    int *err = device_error_word();
+    const int sms = num_sms();
+    if (err == nullptr || sms <= 0) return FA_ERR_CUDA;
+
+    fa::FwdParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.B = B;
+    p.H = H;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.total_q = 0;
+    p.n_pairs = static_cast<int>(n_pairs);
+    p.num_work = static_cast<int>(BH * n_pairs);
+    p.scale_log2 = scale * kLog2e;
+    p.err = err;
+    p.timeout_ns = fa::kWaitTimeoutNs;
+    const int grid = p.num_work < sms ? p.num_work : sms;
+    const cudaError_t e =
+        fa::launch_fwd_dense(D, bf16, causal != 0, maps, p, grid, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status_t fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int num_seqs, int total_q,
+                          int total_k, int max_seqlen_q, int H, int D, int causal, float scale, fa_dtype_t dtype,
+                          void *stream) {
+    if (!q || !k || !v || !o || !lse || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_NULL;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+    if (D != 64 && D != 128) return FA_ERR_HEADDIM;
+    if (num_seqs < 1 || total_q < 1 || total_k < 1 || max_seqlen_q < 1 || H < 1 || max_seqlen_q > kMaxLen ||
+        total_q > kMaxLen || total_k > kMaxLen)
+        return FA_ERR_SHAPE;
+    const long long SH = static_cast<long long>(num_seqs) * H;
+    const long long n_pairs = ((max_seqlen_q + 127) / 128 + 1) / 2;
+    if (SH > INT_MAX || SH * n_pairs > INT_MAX) return FA_ERR_SHAPE;
+    if (!scale_ok(scale)) return FA_ERR_SCALE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse)) return FA_ERR_ALIGN;
+
+    const bool bf16 = dtype == FA_BF16;
+    CUtensorMap maps[3];
+    const uint64_t row = static_cast<uint64_t>(D) * 2;
+    const uint64_t tok = row * H;
+    if (!encode_map(&maps[0], bf16, q, D, H, total_q, row, tok, 1, 128) ||
+        !encode_map(&maps[1], bf16, k, D, H, total_k, row, tok, 1, 128) ||
+        !encode_map(&maps[2], bf16, v, D, H, total_k, row, tok, 1, 128))
+        return FA_ERR_CUDA;
+    int *err = device_error_word();
+    const int sms = num_sms();
+    if (err == nullptr || sms <= 0) return FA_ERR_CUDA;
+
+    fa::FwdParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.B = num_seqs;
+    p.H = H;
+    p.Sq = max_seqlen_q;
+    p.Sk = 0;
+    p.total_q = total_q;
+    p.n_pairs = static_cast<int>(n_pairs);
+    p.num_work = static_cast<int>(SH * n_pairs);
+    p.scale_log2 = scale * kLog2e;
+    p.err = err;
+    p.timeout_ns = fa::kWaitTimeoutNs;
+    const int grid = p.num_work < sms ? p.num_work : sms;
+    const cudaError_t e =
+        fa::launch_fwd_varlen(D, bf16, causal != 0, maps, p, grid, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status_t fa_decode_splitkv(const void *q, const void *k, const void *v, float *o_part, float *m_part,
+                              float *l_part, int B, int H, int Sk, int D, int num_splits, float scale,
+                              fa_dtype_t dtype, void *stream) {
+    if (!q || !k || !v || !o_part || !m_part || !l_part) return FA_ERR_NULL;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+    if (D != 64 && D != 128) return FA_ERR_HEADDIM;
+    if (B < 1 || H < 1 || Sk < 1 || Sk > kMaxLen) return FA_ERR_SHAPE;
+    if (num_splits < 1 || num_splits > Sk || num_splits > FA_MAX_SPLITS) return FA_ERR_SPLITS;
+    const long long BH = static_cast<long long>(B) * H;
+    if (BH * num_splits > INT_MAX) return FA_ERR_SHAPE;
+    if (!scale_ok(scale)) return FA_ERR_SCALE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned4(o_part) || !aligned4(m_part) ||
+        !aligned4(l_part))
+        return FA_ERR_ALIGN;
+    const int P = (Sk + num_splits - 1) / num_splits;
+    const cudaError_t e = fa::launch_decode_split(D, dtype == FA_BF16, q, k, v, o_part, m_part, l_part,
+                                                  static_cast<int>(BH), Sk, num_splits, P, scale * kLog2e,
+                                                  static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status_t fa_splitkv_merge(const float *o_part, const float *m_part, const float *l_part, void *o, float *lse,
+                             int B, int H, int D, int num_splits, fa_dtype_t dtype, void *stream) {
+    if (!o_part || !m_part || !l_part || !o || !lse) return FA_ERR_NULL;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+    if (D != 64 && D != 128) return FA_ERR_HEADDIM;
+    if (B < 1 || H < 1) return FA_ERR_SHAPE;
+    if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_SPLITS;
+    const long long BH = static_cast<long long>(B) * H;
+    if (BH > INT_MAX) return FA_ERR_SHAPE;
+    if (!aligned4(o_part) || !aligned4(m_part) || !aligned4(l_part) || !aligned16(o) || !aligned4(lse))
+        return FA_ERR_ALIGN;
+    const cudaError_t e = fa::launch_splitkv_merge(D, dtype == FA_BF16, o_part, m_part, l_part, o, lse,
+                                                   static_cast<int>(BH), num_splits,
+                                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status_t fa_check_device_error(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    int *err = device_error_word();
+    if (err == nullptr) return FA_ERR_CUDA;
+    int host = 0;
+    if (cudaMemcpy(&host, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+    if (host == 0) return FA_OK;
+    const int zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_DEVICE_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,238 @@
+// Split-KV decoding for one query per head (S_q = 1).
+//
+// Phase 1 ("Adaptive High-Performance Attention Kernels in CUDA", Advanced
+// Production Features 1; "FlashAttention-2 MMA", Split-KV strategy): the Sk
+// keys of a head are cut into num_splits partitions of P = ceil(Sk/num_splits)
+// keys and one CTA computes the partial result of each partition:
+//   m_s = max_j scale q.k_j,  l_s = sum_j e^{scale q.k_j - m_s},
+//   O_s = sum_j e^{scale q.k_j - m_s} v_j   (not normalised).
+// The work is a stream over K and V that are read exactly once, so the kernel
+// is bound by HBM bandwidth: every lane moves 16-byte vectors, a warp reads
+// whole 256-byte key rows back to back (512 contiguous bytes per instruction at
+// D = 128), and each thread keeps 8 K rows and 8 V rows in flight.
+//
+// Phase 2 (same passage): O = sum_s e^{m_s - m_g} / l_g * O_s with
+// m_g = max_s m_s, l_g = sum_s e^{m_s - m_g} l_s, and LSE = m_g + ln l_g.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include <cstdint>
+
+#include "fa_launch.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+constexpr int kDecodeThreads = 128;
+constexpr int kDecodeUnroll = 8;  // keys in flight per lane group
+
+template <bool BF16>
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (BF16) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        } else {
+            const __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
+            const float2 x = __half22float2(h);
+            f[2 * i] = x.x;
+            f[2 * i + 1] = x.y;
+        }
+    }
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// grid: one CTA per (head, partition), x = bh * num_splits + s.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kDecodeThreads)
+    fa_decode_split_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
+                           const uint16_t *__restrict__ v, float *__restrict__ o_part,
+                           float *__restrict__ m_part, float *__restrict__ l_part, int Sk, int num_splits,
+                           int keys_per_split, float scale_log2) {
+    constexpr int kLanesPerKey = D / 8;                  // 16-byte pieces per key row
+    constexpr int kKeysPerWarp = 32 / kLanesPerKey;      // key rows one warp load covers
+    constexpr int kWarps = kDecodeThreads / 32;
+    constexpr int kGroups = kWarps * kKeysPerWarp;       // lane groups per CTA, one key each per step
+    constexpr int U = kDecodeUnroll;
+
+    __shared__ float sm_m[kGroups];
+    __shared__ float sm_l[kGroups];
+    __shared__ __align__(16) float sm_acc[kGroups][D];
+
+    const int bh = blockIdx.x / num_splits;
+    const int s = blockIdx.x % num_splits;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int sub = lane % kLanesPerKey;                  // which 8 elements of the row
+    const int g = warp * kKeysPerWarp + lane / kLanesPerKey;
+    const int k_lo = s * keys_per_split;
+    const int k_hi = min(k_lo + keys_per_split, Sk);
+
+    float qf[8];
+    unpack8<BF16>(*reinterpret_cast<const uint4 *>(q + static_cast<size_t>(bh) * D + sub * 8), qf);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) qf[e] *= scale_log2;  // scores in base-2 units
+
+    const uint16_t *kb = k + static_cast<size_t>(bh) * Sk * D + sub * 8;
+    const uint16_t *vb = v + static_cast<size_t>(bh) * Sk * D + sub * 8;
+    float m = -CUDART_INF_F, l = 0.f;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+
+    for (int key0 = k_lo + g; key0 < k_hi; key0 += kGroups * U) {
+        uint4 kr[U], vr[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int key = key0 + u * kGroups;
+            if (key < k_hi) {
+                kr[u] = ldg_stream(kb + static_cast<size_t>(key) * D);
+                vr[u] = ldg_stream(vb + static_cast<size_t>(key) * D);
+            } else {
+                kr[u] = make_uint4(0, 0, 0, 0);
+                vr[u] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        float sc[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float kf[8];
+            unpack8<BF16>(kr[u], kf);
+            float d = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) d = fmaf(qf[e], kf[e], d);
+            // butterfly over the lanes of one key row: every lane ends with the same bits
+#pragma unroll
+            for (int off = kLanesPerKey / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+            sc[u] = (key0 + u * kGroups < k_hi) ? d : -CUDART_INF_F;
+        }
+        float mx = sc[0];
+#pragma unroll
+        for (int u = 1; u < U; ++u) mx = fmaxf(mx, sc[u]);
+        const float m_new = fmaxf(m, mx);
+        const float m_sub = (m_new == -CUDART_INF_F) ? 0.f : m_new;
+        const float alpha = ptx::ex2(m - m_sub);
+        l *= alpha;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] *= alpha;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const float pu = ptx::ex2(sc[u] - m_sub);
+            l += pu;
+            float vf[8];
+            unpack8<BF16>(vr[u], vf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(pu, vf[e], acc[e]);
+        }
+        m = m_new;
+    }
+
+    // merge the lane groups of this CTA (same log-sum-exp rule as phase 2)
+    if (sub == 0) {
+        sm_m[g] = m;
+        sm_l[g] = l;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sm_acc[g][sub * 8 + e] = acc[e];
+    __syncthreads();
+    for (int d = threadIdx.x; d < D; d += kDecodeThreads) {
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int i = 0; i < kGroups; ++i) M = fmaxf(M, sm_m[i]);
+        float L = 0.f, O = 0.f;
+        if (M != -CUDART_INF_F) {
+#pragma unroll
+            for (int i = 0; i < kGroups; ++i) {
+                const float w = ptx::ex2(sm_m[i] - M);
+                L = fmaf(w, sm_l[i], L);
+                O = fmaf(w, sm_acc[i][d], O);
+            }
+        }
+        const size_t ps = static_cast<size_t>(bh) * num_splits + s;
+        o_part[ps * D + d] = O;
+        if (d == 0) {
+            m_part[ps] = (M == -CUDART_INF_F) ? -CUDART_INF_F : M * 0.69314718055994531f;
+            l_part[ps] = L;
+        }
+    }
+}
+
+// grid: one CTA per head, D threads (one output element each).
+template <int D, bool BF16>
+__global__ void __launch_bounds__(D)
+    fa_splitkv_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ m_part,
+                            const float *__restrict__ l_part, uint16_t *__restrict__ o, float *__restrict__ lse,
+                            int num_splits) {
+    const int bh = blockIdx.x;
+    const int d = threadIdx.x;
+    const float *mp = m_part + static_cast<size_t>(bh) * num_splits;
+    const float *lp = l_part + static_cast<size_t>(bh) * num_splits;
+    const float *op = o_part + static_cast<size_t>(bh) * num_splits * D + d;
+    float mg = -CUDART_INF_F;
+    for (int s = 0; s < num_splits; ++s) mg = fmaxf(mg, mp[s]);
+    float lg = 0.f, acc = 0.f;
+    if (mg != -CUDART_INF_F) {
+        for (int s = 0; s < num_splits; ++s) {
+            const float w = expf(mp[s] - mg);
+            lg = fmaf(w, lp[s], lg);
+            acc = fmaf(w, op[static_cast<size_t>(s) * D], acc);
+        }
+    }
+    const float out = lg > 0.f ? acc / lg : 0.f;
+    if constexpr (BF16) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(out);
+        o[static_cast<size_t>(bh) * D + d] = *reinterpret_cast<const uint16_t *>(&h);
+    } else {
+        const __half h = __float2half_rn(out);
+        o[static_cast<size_t>(bh) * D + d] = *reinterpret_cast<const uint16_t *>(&h);
+    }
+    if (d == 0) lse[bh] = lg > 0.f ? mg + logf(lg) : -CUDART_INF_F;
+}
+
+template <int D, bool BF16>
+static cudaError_t launch_split_t(const void *q, const void *k, const void *v, float *op, float *mp, float *lp,
+                                  int BH, int Sk, int S, int P, float scale_log2, cudaStream_t st) {
+    const long long grid = static_cast<long long>(BH) * S;
+    fa_decode_split_kernel<D, BF16><<<static_cast<unsigned>(grid), kDecodeThreads, 0, st>>>(
+        static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(v), op,
+        mp, lp, Sk, S, P, scale_log2);
+    return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+static cudaError_t launch_merge_t(const float *op, const float *mp, const float *lp, void *o, float *lse, int BH,
+                                  int S, cudaStream_t st) {
+    fa_splitkv_merge_kernel<D, BF16><<<BH, D, 0, st>>>(op, mp, lp, static_cast<uint16_t *>(o), lse, S);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_split(int D, bool bf16, const void *q, const void *k, const void *v, float *o_part,
+                                float *m_part, float *l_part, int BH, int Sk, int num_splits, int keys_per_split,
+                                float scale_log2, cudaStream_t stream) {
+    if (D == 64 && !bf16) return launch_split_t<64, false>(q, k, v, o_part, m_part, l_part, BH, Sk, num_splits, keys_per_split, scale_log2, stream);
+    if (D == 64 && bf16) return launch_split_t<64, true>(q, k, v, o_part, m_part, l_part, BH, Sk, num_splits, keys_per_split, scale_log2, stream);
+    if (D == 128 && !bf16) return launch_split_t<128, false>(q, k, v, o_part, m_part, l_part, BH, Sk, num_splits, keys_per_split, scale_log2, stream);
+    if (D == 128 && bf16) return launch_split_t<128, true>(q, k, v, o_part, m_part, l_part, BH, Sk, num_splits, keys_per_split, scale_log2, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_splitkv_merge(int D, bool bf16, const float *o_part, const float *m_part, const float *l_part,
+                                 void *o, float *lse, int BH, int num_splits, cudaStream_t stream) {
+    if (D == 64 && !bf16) return launch_merge_t<64, false>(o_part, m_part, l_part, o, lse, BH, num_splits, stream);
+    if (D == 64 && bf16) return launch_merge_t<64, true>(o_part, m_part, l_part, o, lse, BH, num_splits, stream);
+    if (D == 128 && !bf16) return launch_merge_t<128, false>(o_part, m_part, l_part, o, lse, BH, num_splits, stream);
+    if (D == 128 && bf16) return launch_merge_t<128, true>(o_part, m_part, l_part, o, lse, BH, num_splits, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

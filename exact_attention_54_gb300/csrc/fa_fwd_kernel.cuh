@@ -1,0 +1,507 @@
+// FlashAttention-2 forward on sm_103a: TMA-staged tiles, tcgen05 MMAs with
+// TMEM accumulators, online softmax in registers.
+//
+// Method ("FlashAttention-2 MMA", Technical Details; "Adaptive
+// High-Performance Attention Kernels in CUDA", Architectural Progression
+// stages 2-4): the outer loop runs over 128-row query tiles, the inner loop
+// over 128-key K/V tiles; each step forms S = Q K^T, updates the running row
+// maximum m and running sum l, rescales the output accumulator by
+// alpha = exp(m_old - m_new) and adds P V. The output stays on chip for the
+// whole inner loop and one log-sum-exp per row is written at the end. Causal
+// tiles that lie entirely above the diagonal are never visited; only tiles
+// that straddle it are masked (k_idx <= q_idx, top-left aligned).
+//
+// GB300 mapping (one CTA per SM, persistent):
+//   warp 0        TMA producer: Q tile pair once per work item, then a ring of
+//                 K/V stages (128-byte swizzle, 128 rows x 64 columns per box)
+//   warp 1        MMA issuer (one thread): S_t = Q_t K^T into TMEM, then
+//                 O_t += P_t V with P_t read from TMEM (A operand) and V
+//                 MN-major from shared memory. Also owns the TMEM allocation.
+//   warps 4..7    softmax warpgroup for query tile 0 (one row per thread)
+//   warps 8..11   softmax warpgroup for query tile 1
+// The two query tiles of a work item share every K/V stage and alternate on
+// the tensor core: while one warpgroup exponentiates its S tile, the MMAs of
+// the other tile run. TMEM columns: S0 [0,128) S1 [128,256) O0 and O1 after;
+// P_t (16-bit) overwrites the first 64 columns of S_t.
+//
+// The running maximum is only moved when it grows by more than 2^8 (in the
+// exponent's base-2 units); until then P may exceed 1 by up to 256x. O and l
+// carry the same stale maximum, so O / l is unchanged; this only saves
+// rescaling work.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "fa_launch.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+constexpr int kBlockM = 128;      // query rows per tile
+constexpr int kBlockN = 128;      // keys per K/V tile
+constexpr int kFwdThreads = 384;  // 12 warps
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct FwdShape {
+    static_assert(D == 64 || D == 128, "head dim");
+    static constexpr int kColBlocks = D / 64;            // 128-byte column blocks per row
+    static constexpr int kBlockBytes = kBlockM * 128;    // one 128-row x 64-column box
+    static constexpr int kTileBytes = kBlockM * D * 2;   // one 128-row tile of Q, K or V
+    static constexpr int kStages = (D == 128) ? 2 : 4;   // K/V ring depth
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+    static constexpr int kOffV = kOffK + kStages * kTileBytes;
+    static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+    // barrier indices
+    static constexpr int kQFull = 0, kQEmpty = 1, kTeardown = 2;
+    static constexpr int kKFull = 3;
+    static constexpr int kVFull = kKFull + kStages;
+    static constexpr int kKVEmpty = kVFull + kStages;
+    static constexpr int kSFull = kKVEmpty + kStages;    // +t
+    static constexpr int kPFull = kSFull + 2;            // +t
+    static constexpr int kODone = kPFull + 2;            // +t
+    static constexpr int kNumBars = kODone + 2;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
+    static constexpr uint32_t kTmemS = 0;                     // + t * 128
+    static constexpr uint32_t kTmemO = 256;                   // + t * D
+    static constexpr uint32_t kTmemCols = 512;
+};
+
+// One unit of work: a pair of consecutive 128-row query tiles of one
+// (sequence, head). Tiles past the end of the sequence are inactive.
+struct Work {
+    int b, h;
+    int seq_q0, seq_k0;  // token offsets of the sequence (varlen), else 0
+    int Lq, Lk;          // query and key lengths of the sequence
+    int q_start[2];      // first query row of each tile (relative to the sequence)
+    int rows[2];         // valid rows of each tile (0 = inactive)
+    int n_kv[2];         // K/V tiles each query tile visits
+    int n_kv_max;
+};
+
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ Work get_work(const FwdParams &p, int w) {
+    Work k;
+    const int BH = p.B * p.H;
+    const int pair = p.n_pairs - 1 - w / BH;  // longest causal work first
+    const int bh = w % BH;
+    k.b = bh / p.H;
+    k.h = bh % p.H;
+    if constexpr (VARLEN) {
+        k.seq_q0 = p.cu_q[k.b];
+        k.Lq = p.cu_q[k.b + 1] - k.seq_q0;
+        k.seq_k0 = p.cu_k[k.b];
+        k.Lk = p.cu_k[k.b + 1] - k.seq_k0;
+    } else {
+        k.seq_q0 = 0;
+        k.seq_k0 = 0;
+        k.Lq = p.Sq;
+        k.Lk = p.Sk;
+    }
+    const int nk_all = (k.Lk + kBlockN - 1) / kBlockN;
+    k.n_kv_max = 0;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int qs = (2 * pair + t) * kBlockM;
+        k.q_start[t] = qs;
+        const int rows = k.Lq - qs;
+        k.rows[t] = rows <= 0 ? 0 : (rows < kBlockM ? rows : kBlockM);
+        int nkv = 0;
+        if (k.rows[t] > 0) {
+            nkv = nk_all;
+            if (CAUSAL) {
+                const int last = (qs + k.rows[t] - 1) / kBlockN + 1;
+                nkv = last < nk_all ? last : nk_all;
+            }
+        }
+        k.n_kv[t] = nkv;
+        k.n_kv_max = nkv > k.n_kv_max ? nkv : k.n_kv_max;
+    }
+    return k;
+}
+
+// Static persistent schedule: round r hands out work items [r*G, (r+1)*G),
+// alternating direction each round so that the heavy early items and the light
+// late items balance across CTAs.
+__device__ __forceinline__ int work_index(int r) {
+    const int G = static_cast<int>(gridDim.x);
+    const int pos = (r & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+    return r * G + pos;
+}
+
+// ------------------------------------------------------------------ roles --
+
+template <int D, bool CAUSAL, bool VARLEN>
+__device__ void fwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
+                             const FwdParams &p, uint32_t sbase, volatile int *abort_flag) {
+    using S = FwdShape<D>;
+    const uint32_t bars = sbase + S::kOffBar;
+    auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+    uint32_t it = 0;  // K/V tiles issued
+    uint32_t wi = 0;  // work items loaded
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+        const int w = work_index(r);
+        if (w >= p.num_work) break;
+        const Work wk = get_work<CAUSAL, VARLEN>(p, w);
+        if (wk.n_kv_max == 0) continue;
+        if (wi > 0 && !(ok = ptx::bar_wait(bar(S::kQEmpty), (wi - 1) & 1, abort_flag, p.timeout_ns)))
+            break;
+        uint32_t qbytes = 0;
+        for (int t = 0; t < 2; ++t) qbytes += wk.n_kv[t] > 0 ? S::kTileBytes : 0;
+        ptx::bar_arrive_expect_tx(bar(S::kQFull), qbytes);
+        for (int t = 0; t < 2; ++t) {
+            if (wk.n_kv[t] == 0) continue;
+            for (int c = 0; c < S::kColBlocks; ++c) {
+                const uint32_t dst = sbase + S::kOffQ + t * S::kTileBytes + c * S::kBlockBytes;
+                if constexpr (VARLEN)
+                    ptx::tma_load_3d(dst, tq, bar(S::kQFull), c * 64, wk.h, wk.seq_q0 + wk.q_start[t]);
+                else
+                    ptx::tma_load_3d(dst, tq, bar(S::kQFull), c * 64, wk.q_start[t], wk.b * p.H + wk.h);
+            }
+        }
+        for (int j = 0; j < wk.n_kv_max; ++j, ++it) {
+            const uint32_t stage = it % S::kStages;
+            if (it >= S::kStages &&
+                !(ok = ptx::bar_wait(bar(S::kKVEmpty + stage), ((it / S::kStages) - 1) & 1, abort_flag,
+                                     p.timeout_ns)))
+                break;
+            ptx::bar_arrive_expect_tx(bar(S::kKFull + stage), S::kTileBytes);
+            for (int c = 0; c < S::kColBlocks; ++c) {
+                const uint32_t dst = sbase + S::kOffK + stage * S::kTileBytes + c * S::kBlockBytes;
+                if constexpr (VARLEN)
+                    ptx::tma_load_3d(dst, tk, bar(S::kKFull + stage), c * 64, wk.h, wk.seq_k0 + j * kBlockN);
+                else
+                    ptx::tma_load_3d(dst, tk, bar(S::kKFull + stage), c * 64, j * kBlockN, wk.b * p.H + wk.h);
+            }
+            ptx::bar_arrive_expect_tx(bar(S::kVFull + stage), S::kTileBytes);
+            for (int c = 0; c < S::kColBlocks; ++c) {
+                const uint32_t dst = sbase + S::kOffV + stage * S::kTileBytes + c * S::kBlockBytes;
+                if constexpr (VARLEN)
+                    ptx::tma_load_3d(dst, tv, bar(S::kVFull + stage), c * 64, wk.h, wk.seq_k0 + j * kBlockN);
+                else
+                    ptx::tma_load_3d(dst, tv, bar(S::kVFull + stage), c * 64, j * kBlockN, wk.b * p.H + wk.h);
+            }
+        }
+        ++wi;
+    }
+    // Never leave with copies in flight: wait (bounded, even after an abort)
+    // for the newest load into every stage and for the newest Q load.
+    for (uint32_t s = 0; s < S::kStages && s < it; ++s) {
+        const uint32_t last = (it - 1) - ((it - 1 - s) % S::kStages);
+        ptx::bar_wait(bar(S::kKFull + s), (last / S::kStages) & 1, nullptr, p.timeout_ns);
+        ptx::bar_wait(bar(S::kVFull + s), (last / S::kStages) & 1, nullptr, p.timeout_ns);
+    }
+    if (wi > 0) ptx::bar_wait(bar(S::kQFull), (wi - 1) & 1, nullptr, p.timeout_ns);
+}
+
+template <int D, bool BF16, bool CAUSAL, bool VARLEN>
+__device__ void fwd_mma(const FwdParams &p, uint32_t sbase, uint32_t tmem, volatile int *abort_flag) {
+    using S = FwdShape<D>;
+    constexpr uint32_t kIdescQK = ptx::idesc_f16(BF16, kBlockM, kBlockN, false);
+    constexpr uint32_t kIdescPV = ptx::idesc_f16(BF16, kBlockM, D, true);
+    const uint32_t bars = sbase + S::kOffBar;
+    auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+
+    // S_t = Q_t K^T: D/16 MMAs of K=16, both operands K-major, 128-byte swizzled.
+    auto issue_qk = [&](int t, uint32_t stage) {
+        const uint32_t q0 = sbase + S::kOffQ + t * S::kTileBytes;
+        const uint32_t k0 = sbase + S::kOffK + stage * S::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * S::kBlockBytes + (kk % 4) * 32;
+            ptx::mma_ss(tmem + S::kTmemS + t * 128, ptx::smem_desc_sw128(q0 + off, 16, 1024),
+                        ptx::smem_desc_sw128(k0 + off, 16, 1024), kIdescQK, kk > 0);
+        }
+    };
+    // O_t (+)= P_t V: 128/16 MMAs of K=16; P_t from TMEM (two 16-bit values per
+    // column), V MN-major: 64-column boxes 16 KB apart, 8-key atoms 1 KB apart.
+    auto issue_pv = [&](int t, uint32_t stage, bool accumulate) {
+        const uint32_t v0 = sbase + S::kOffV + stage * S::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+            ptx::mma_ts(tmem + S::kTmemO + t * D, tmem + S::kTmemS + t * 128 + kk * 8,
+                        ptx::smem_desc_sw128(v0 + kk * 2048, S::kBlockBytes, 1024), kIdescPV,
+                        (accumulate || kk > 0) ? 1u : 0u);
+        }
+    };
+
+    uint32_t it = 0, wi = 0;
+    uint32_t cnt[2] = {0, 0};  // PV steps issued per query tile (= P_FULL phases consumed)
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+        const int w = work_index(r);
+        if (w >= p.num_work) break;
+        const Work wk = get_work<CAUSAL, VARLEN>(p, w);
+        if (wk.n_kv_max == 0) continue;
+        if (!(ok = ptx::bar_wait(bar(S::kQFull), wi & 1, abort_flag, p.timeout_ns))) break;
+        {
+            const uint32_t st0 = it % S::kStages;
+            if (!(ok = ptx::bar_wait(bar(S::kKFull + st0), (it / S::kStages) & 1, abort_flag, p.timeout_ns)))
+                break;
+            ptx::tc_fence_after();
+            for (int t = 0; t < 2; ++t) {
+                if (wk.n_kv[t] == 0) continue;
+                issue_qk(t, st0);
+                ptx::mma_commit(bar(S::kSFull + t));
+            }
+        }
+        for (int j = 0; j < wk.n_kv_max && ok; ++j) {
+            const uint32_t itj = it + j;
+            const uint32_t stage = itj % S::kStages;
+            bool v_ready = false;
+            for (int t = 0; t < 2; ++t) {
+                if (j >= wk.n_kv[t]) continue;
+                if (!(ok = ptx::bar_wait(bar(S::kPFull + t), cnt[t] & 1, abort_flag, p.timeout_ns))) break;
+                if (!v_ready) {
+                    if (!(ok = ptx::bar_wait(bar(S::kVFull + stage), (itj / S::kStages) & 1, abort_flag,
+                                             p.timeout_ns)))
+                        break;
+                    v_ready = true;
+                }
+                ptx::tc_fence_after();
+                issue_pv(t, stage, j > 0);
+                ptx::mma_commit(bar(S::kODone + t));
+                ++cnt[t];
+                if (j + 1 < wk.n_kv[t]) {
+                    const uint32_t itn = itj + 1;
+                    const uint32_t sn = itn % S::kStages;
+                    if (!(ok = ptx::bar_wait(bar(S::kKFull + sn), (itn / S::kStages) & 1, abort_flag,
+                                             p.timeout_ns)))
+                        break;
+                    ptx::tc_fence_after();
+                    issue_qk(t, sn);
+                    ptx::mma_commit(bar(S::kSFull + t));
+                }
+            }
+            if (ok) ptx::mma_commit(bar(S::kKVEmpty + stage));
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar(S::kQEmpty));
+        it += wk.n_kv_max;
+        ++wi;
+    }
+    // Every MMA issued above must finish before TMEM is released.
+    ptx::mma_commit(bar(S::kTeardown));
+    ptx::bar_wait(bar(S::kTeardown), 0, nullptr, p.timeout_ns);
+}
+
+template <int D, bool BF16, bool CAUSAL, bool VARLEN>
+__device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, int t, int wq, int lane,
+                            volatile int *abort_flag) {
+    using S = FwdShape<D>;
+    using Elem = uint16_t;
+    const uint32_t bars = sbase + S::kOffBar;
+    auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+    const int row = wq * 32 + lane;                             // row within the query tile
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;  // this warp's TMEM lanes
+    const uint32_t tS = tmem + lane_base + S::kTmemS + t * 128;
+    const uint32_t tO = tmem + lane_base + S::kTmemO + t * D;
+    const float scale_log2 = p.scale_log2;
+    constexpr unsigned kFull = 0xffffffffu;
+    uint32_t cnt = 0;  // S tiles consumed by this warpgroup
+    bool ok = true;
+
+    for (int r = 0; ok; ++r) {
+        const int w = work_index(r);
+        if (w >= p.num_work) break;
+        const Work wk = get_work<CAUSAL, VARLEN>(p, w);
+        if (wk.rows[t] == 0) continue;
+        const int q_row = wk.q_start[t] + row;
+        const bool row_valid = row < wk.rows[t];
+        const int nkv = wk.n_kv[t];
+        float m_used = -CUDART_INF_F;  // running max in base-2 units of the scaled score
+        float l = 0.f;
+
+        for (int j = 0; j < nkv; ++j) {
+            ok = ptx::bar_wait(bar(S::kSFull + t), cnt & 1, abort_flag, p.timeout_ns);
+            if (!__all_sync(kFull, ok)) { ok = false; break; }
+            ptx::tc_fence_after();
+            uint32_t s[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, s[c]);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ptx::reg_fence(s[c]);
+
+            const int k0 = j * kBlockN;
+            const bool need_mask = (k0 + kBlockN > wk.Lk) || (CAUSAL && k0 + kBlockN - 1 > wk.q_start[t]);
+            if (need_mask) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const int key = k0 + c;
+                    const bool vis = key < wk.Lk && (!CAUSAL || key <= q_row);
+                    if (!vis) s[c / 32][c % 32] = 0xff800000u;  // -inf
+                }
+            }
+            // row maximum of the raw scores (8 independent chains)
+            float mx8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(s[0][i]);
+#pragma unroll
+            for (int c = 8; c < 128; ++c) mx8[c % 8] = fmaxf(mx8[c % 8], __uint_as_float(s[c / 32][c % 32]));
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            const float m_cand = mx * scale_log2;
+            const bool need = m_cand > m_used + kRescaleThreshold;
+            float alpha = 1.f;
+            if (need) {
+                alpha = ptx::ex2(m_used - m_cand);  // 0 on the first tile (m_used = -inf)
+                m_used = m_cand;
+            }
+            l *= alpha;
+            const float m_sub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
+
+            // P = 2^(s * scale_log2 - m), packed two per 32-bit TMEM column
+            uint32_t pk[2][32];
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c2 = 0; c2 < 64; ++c2) {
+                const int c = 2 * c2;
+                const float a = ptx::ex2(fmaf(__uint_as_float(s[c / 32][c % 32]), scale_log2, -m_sub));
+                const float b = ptx::ex2(fmaf(__uint_as_float(s[(c + 1) / 32][(c + 1) % 32]), scale_log2, -m_sub));
+                ls[c2 % 4] += a + b;
+                pk[c2 / 32][c2 % 32] = ptx::pack2<BF16>(a, b);
+            }
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            ptx::tmem_st32(tS, pk[0]);
+            ptx::tmem_st32(tS + 32, pk[1]);
+
+            // O *= alpha, once the previous P V has landed (only when a row of
+            // this warp moved its maximum)
+            if (j > 0 && __any_sync(kFull, need)) {
+                ok = ptx::bar_wait(bar(S::kODone + t), (cnt - 1) & 1, abort_flag, p.timeout_ns);
+                if (!__all_sync(kFull, ok)) { ok = false; break; }
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32(tO + c * 32, o);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence(o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    ptx::tmem_st32(tO + c * 32, o);
+                }
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::bar_arrive(bar(S::kPFull + t));
+            ++cnt;
+        }
+        if (!ok) break;
+
+        // epilogue: O / l in the input dtype, LSE = (m + log2 l) * ln 2
+        if (nkv > 0) {
+            ok = ptx::bar_wait(bar(S::kODone + t), (cnt - 1) & 1, abort_flag, p.timeout_ns);
+            if (!__all_sync(kFull, ok)) { ok = false; break; }
+            ptx::tc_fence_after();
+        }
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const float lse = l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+        Elem *orow;
+        if constexpr (VARLEN)
+            orow = static_cast<Elem *>(p.o) + (static_cast<size_t>(wk.seq_q0 + q_row) * p.H + wk.h) * D;
+        else
+            orow = static_cast<Elem *>(p.o) + (static_cast<size_t>(wk.b * p.H + wk.h) * p.Sq + q_row) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            if (nkv > 0) {
+                ptx::tmem_ld32(tO + c * 32, o);
+                ptx::tmem_ld_wait();
+                ptx::reg_fence(o);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = 0u;
+            }
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                pk[i] = ptx::pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+            if (row_valid) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+        }
+        if (row_valid) {
+            if constexpr (VARLEN)
+                p.lse[static_cast<size_t>(wk.h) * p.total_q + wk.seq_q0 + q_row] = lse;
+            else
+                p.lse[static_cast<size_t>(wk.b * p.H + wk.h) * p.Sq + q_row] = lse;
+        }
+    }
+}
+
+// ----------------------------------------------------------------- kernel --
+
+template <int D, bool BF16, bool CAUSAL, bool VARLEN>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    using S = FwdShape<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = ptx::smem_addr(smem);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kOffMisc + 4);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        const uint32_t bars = sbase + S::kOffBar;
+        for (int i = 0; i < S::kNumBars; ++i) {
+            const bool p_full = (i == S::kPFull || i == S::kPFull + 1);
+            ptx::bar_init(bars + 8u * i, p_full ? kBlockM : 1u);
+        }
+        *abort_flag = 0;
+        ptx::bar_init_fence();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tm_q);
+        ptx::prefetch_tmap(&tm_k);
+        ptx::prefetch_tmap(&tm_v);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), S::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) fwd_producer<D, CAUSAL, VARLEN>(&tm_q, &tm_k, &tm_v, p, sbase, abort_flag);
+    } else if (warp == 1) {
+        if (lane == 0) fwd_mma<D, BF16, CAUSAL, VARLEN>(p, sbase, tmem, abort_flag);
+    } else if (warp >= 4) {
+        fwd_softmax<D, BF16, CAUSAL, VARLEN>(p, sbase, tmem, (warp - 4) / 4, warp % 4, lane, abort_flag);
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, S::kTmemCols);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicExch(p.err, kDeviceErrTimeout);
+}
+
+template <int D, bool BF16, bool CAUSAL, bool VARLEN>
+cudaError_t launch_fwd_t(const CUtensorMap *maps, const FwdParams &p, int grid, cudaStream_t stream) {
+    auto kern = fa_fwd_kernel<D, BF16, CAUSAL, VARLEN>;
+    constexpr int kSmem = FwdShape<D>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kFwdThreads, kSmem, stream>>>(maps[0], maps[1], maps[2], p);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,166 @@
+/*
+ * fa.h - C ABI of the GB300 (sm_103a) exact-attention library (libfa.so).
+ *
+ * Operations
+ *   fa_fwd             FlashAttention-2 forward over dense [B,H,S,D] tensors.
+ *   fa_fwd_varlen      the same forward over packed variable-length sequences.
+ *   fa_decode_splitkv  split-KV decoding, phase 1: per-partition partials.
+ *   fa_splitkv_merge   split-KV decoding, phase 2: log-sum-exp merge.
+ *
+ * Common rules
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller. The library
+ *     allocates no memory and keeps no state between calls, apart from one
+ *     device-resident error word per GPU (see fa_check_device_error).
+ *   - Calls are asynchronous: work is enqueued on `stream` (a cudaStream_t
+ *     passed as void*, NULL = the legacy default stream) and the call returns
+ *     after the launch. Inputs must stay valid until the work completes.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     failed check returns a negative status and enqueues nothing. Contents of
+ *     device arrays (cu_seqlens) are not read on the host.
+ *   - 16-bit tensors are contiguous, row-major, 16-byte aligned; fp32 arrays
+ *     are contiguous and 4-byte aligned. D is 64 or 128.
+ *   - `scale` multiplies Q K^T before the softmax and must be finite and > 0
+ *     (1/sqrt(D) is the usual value).
+ *   - LSE outputs are natural-log sums over the scaled, masked scores:
+ *     LSE_i = ln sum_j exp(scale * q_i . k_j).
+ *   - No C++ exception crosses this boundary.
+ *
+ * The kernels are compiled for sm_103a only; on another GPU every launch fails
+ * with FA_ERR_CUDA.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_NULL = -1,           /* a required pointer is NULL */
+    FA_ERR_SHAPE = -2,          /* a size is <= 0, or too large for 32-bit indexing */
+    FA_ERR_HEADDIM = -3,        /* D is not 64 or 128 */
+    FA_ERR_DTYPE = -4,          /* dtype is not FA_FP16 or FA_BF16 */
+    FA_ERR_ALIGN = -5,          /* a 16-bit tensor is not 16-byte aligned (fp32: 4-byte) */
+    FA_ERR_SPLITS = -6,         /* num_splits < 1 or > Sk (or > FA_MAX_SPLITS) */
+    FA_ERR_SCALE = -7,          /* scale is not finite and > 0 */
+    FA_ERR_CUDA = -8,           /* the CUDA runtime reported an error (launch, tensor map) */
+    FA_ERR_DEVICE_TIMEOUT = -9  /* a kernel gave up waiting on an on-chip barrier */
+} fa_status_t;
+
+typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype_t;
+
+/* Upper bound on the number of KV partitions of the split-KV decode. */
+#define FA_MAX_SPLITS 1024
+
+/*
+ * fa_fwd - exact attention forward pass, O = softmax(scale * Q K^T [+ mask]) V.
+ *
+ * Defined by "FlashAttention-2 MMA" (Usage Example: [B,H,S,D] tensors and a
+ * causal flag; Technical Details: online softmax with running max and sum,
+ * causal rule k_idx <= q_idx) and "Adaptive High-Performance Attention Kernels
+ * in CUDA" (Architectural Progression, stages 3-4: outer loop over query
+ * tiles, on-chip output accumulator, upper-triangular tiles skipped).
+ *
+ *   q    [B,H,Sq,D]  fp16/bf16          k, v [B,H,Sk,D]  same dtype
+ *   o    [B,H,Sq,D]  output, dtype of q
+ *   lse  [B,H,Sq]    fp32 output
+ *   causal  0 or 1. When 1, query i sees keys j <= i (top-left alignment,
+ *           also when Sq != Sk).
+ * Errors: FA_ERR_NULL, FA_ERR_SHAPE (B,H,Sq,Sk < 1), FA_ERR_HEADDIM,
+ * FA_ERR_DTYPE, FA_ERR_ALIGN, FA_ERR_SCALE, FA_ERR_CUDA.
+ */
+FA_API fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                   int B, int H, int Sq, int Sk, int D, int causal, float scale,
+                   fa_dtype_t dtype, void *stream);
+
+/*
+ * fa_fwd_varlen - the forward pass over packed sequences of different lengths.
+ *
+ * Defined by "Adaptive High-Performance Attention Kernels in CUDA" (Advanced
+ * Production Features 3: tokens flattened to [total_tokens, H, d], sequence
+ * boundaries from cumulative lengths, no padding computed).
+ *
+ *   q, o          [total_q,H,D]      k, v [total_k,H,D]
+ *   lse           [H,total_q] fp32   (per-head contiguous)
+ *   cu_seqlens_q  device int32[num_seqs+1], 0 = cu[0] <= cu[1] <= ... = total_q
+ *   cu_seqlens_k  device int32[num_seqs+1], same rules with total_k
+ *   max_seqlen_q  >= every query length (sizes the launch; rows of a longer
+ *                 sequence would be left unwritten)
+ * Sequence i attends its own keys only; causal positions are counted from the
+ * start of each sequence. Zero-length sequences are allowed.
+ * Errors: as fa_fwd, plus FA_ERR_SHAPE for num_seqs < 1 or total_* < 1.
+ */
+FA_API fa_status_t fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                          int num_seqs, int total_q, int total_k, int max_seqlen_q,
+                          int H, int D, int causal, float scale, fa_dtype_t dtype,
+                          void *stream);
+
+/*
+ * fa_decode_splitkv - split-KV decoding, phase 1 (one query per head).
+ *
+ * Defined by "Adaptive High-Performance Attention Kernels in CUDA" (Advanced
+ * Production Features 1: the KV cache is split into S partitions that run
+ * partial attention concurrently) and "FlashAttention-2 MMA" (Split-KV
+ * strategy for S_q = 1).
+ *
+ * Partition s covers keys [s*P, min((s+1)*P, Sk)) with P = ceil(Sk/S); the
+ * last partitions may be short or empty. For each (b,h,s):
+ *   m_part[b,h,s] = max_j scale * q . k_j                  (-inf if empty)
+ *   l_part[b,h,s] = sum_j exp(scale * q . k_j - m)         (0 if empty)
+ *   o_part[b,h,s,:] = sum_j exp(scale * q . k_j - m) v_j   (unnormalised)
+ *
+ *   q [B,H,1,D] (= [B,H,D])   k, v [B,H,Sk,D]   fp16/bf16
+ *   o_part [B,H,S,D] fp32, m_part and l_part [B,H,S] fp32: caller workspace.
+ * Errors: FA_ERR_NULL, FA_ERR_SHAPE, FA_ERR_HEADDIM, FA_ERR_DTYPE,
+ * FA_ERR_ALIGN, FA_ERR_SPLITS, FA_ERR_SCALE, FA_ERR_CUDA.
+ */
+FA_API fa_status_t fa_decode_splitkv(const void *q, const void *k, const void *v, float *o_part,
+                              float *m_part, float *l_part, int B, int H, int Sk, int D,
+                              int num_splits, float scale, fa_dtype_t dtype, void *stream);
+
+/*
+ * fa_splitkv_merge - split-KV decoding, phase 2 (log-sum-exp reduction).
+ *
+ * Defined by "Adaptive High-Performance Attention Kernels in CUDA" (Advanced
+ * Production Features 1: O = sum_s e^{m_s - m_global} / l_global * O_s), read
+ * with m_global = max_s m_s and l_global = sum_s e^{m_s - m_global} l_s.
+ *
+ *   inputs as written by fa_decode_splitkv with the same B, H, D, num_splits
+ *   o   [B,H,1,D] output (dtype)     lse [B,H] fp32 output = m_global + ln l_global
+ * Errors: FA_ERR_NULL, FA_ERR_SHAPE, FA_ERR_HEADDIM, FA_ERR_DTYPE,
+ * FA_ERR_ALIGN, FA_ERR_SPLITS, FA_ERR_CUDA.
+ */
+FA_API fa_status_t fa_splitkv_merge(const float *o_part, const float *m_part, const float *l_part,
+                             void *o, float *lse, int B, int H, int D, int num_splits,
+                             fa_dtype_t dtype, void *stream);
+
+/*
+ * fa_check_device_error - synchronise `stream`, then read and clear the
+ * current device's error word. Kernels bound every wait on an on-chip barrier;
+ * a wait that runs out sets the word, releases what the CTA holds and returns.
+ * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT, or FA_ERR_CUDA when the runtime
+ * itself reports an error.
+ */
+FA_API fa_status_t fa_check_device_error(void *stream);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+FA_API const char *fa_status_string(fa_status_t status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+FA_API int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */

@@ -1,0 +1,47 @@
+"""Shared helpers for the GPU parity tests."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+# Tolerances: max-abs error on the 16-bit output O and on the fp32 LSE
+# (fp32 accumulation inside the kernels; P is rounded to 16 bits before P V).
+O_TOL = 2e-2
+LSE_TOL = 1e-3
+
+
+def dev(*ts):
+    return [t.cuda().contiguous() for t in ts]
+
+
+def max_abs_err(actual, expected):
+    a = actual.detach().to("cpu", torch.float64).numpy() if hasattr(actual, "detach") else np.asarray(actual)
+    e = expected.detach().to("cpu", torch.float64).numpy() if hasattr(expected, "detach") else np.asarray(expected)
+    assert a.shape == e.shape, (a.shape, e.shape)
+    if a.size == 0:
+        return 0.0, None
+    if not np.all(np.isfinite(a)):
+        bad = np.argwhere(~np.isfinite(a))[0]
+        return float("inf"), tuple(int(x) for x in bad)
+    d = np.abs(a - e)
+    idx = np.unravel_index(int(np.argmax(d)), d.shape)
+    return float(d[idx]), tuple(int(x) for x in idx)
+
+
+def assert_close(actual, expected, tol, what=""):
+    err, where = max_abs_err(actual, expected)
+    assert err <= tol, f"{what}: max abs err {err:.3e} at {where} > {tol:.1e}"
+    return err
+
+
+def sample_rows(S: int, n_random: int = 24, seed: int = 0):
+    """Rows worth checking in a length-S sequence: the edges of every 128-row
+    tile near the start and end, the last rows, and a seeded random sample."""
+    rows = {0, 1, 2, S - 1, S - 2}
+    for t in (127, 128, 129, 255, 256, 257, S // 2, S - 128, S - 129):
+        if 0 <= t < S:
+            rows.add(t)
+    g = torch.Generator().manual_seed(seed)
+    if S > 0:
+        rows.update(torch.randint(0, S, (n_random,), generator=g).tolist())
+    return sorted(r for r in rows if 0 <= r < S)

@@ -1,0 +1,142 @@
+"""Dense forward (fa_fwd) against the fp64 oracle on the same seeded inputs.
+
+Small shapes are compared element by element over every row; the full-size
+LLaMA-7B prefill shape (1,32,4096,4096,128, causal, bf16) is checked on sampled
+rows in the launch configuration the benchmark times. The masking bookkeeping
+is checked exactly: results must not change by a single bit when keys that no
+query may see are poisoned."""
+import pytest
+import torch
+
+import exact_attention_54_gb300 as fa
+import oracle
+from exact_attention_54_gb300 import inputs
+from gpu_helpers import LSE_TOL, O_TOL, assert_close, dev, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def run(q, k, v, causal, scale):
+    qd, kd, vd = dev(q, k, v)
+    o, lse = fa.flash_attention(qd, kd, vd, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    return o.cpu(), lse.cpu()
+
+
+def check(q, k, v, causal, scale, rows=None, what=""):
+    o, lse = run(q, k, v, causal, scale)
+    ro, rl = oracle.attention(q, k, v, causal, scale, rows=rows)
+    if rows is not None:
+        o, lse = o[:, :, rows], lse[:, :, rows]
+    assert_close(o, ro, O_TOL, f"O {what}")
+    assert_close(lse, rl, LSE_TOL, f"LSE {what}")
+
+
+@pytest.mark.parametrize("key", ["tiny", "tiny_causal", "small"])
+def test_named_workloads(key):
+    w = inputs.WORKLOADS[key]
+    q, k, v = inputs.make_workload(w)
+    check(q, k, v, w.causal, w.scale, what=w.name)
+
+
+SHAPES = [
+    # B, H, Sq, Sk, D, dtype, causal
+    (1, 1, 1, 1, 64, torch.float16, False),
+    (1, 1, 1, 1, 128, torch.bfloat16, True),
+    (2, 3, 129, 129, 64, torch.bfloat16, True),
+    (1, 2, 200, 200, 128, torch.float16, True),
+    (1, 2, 300, 77, 128, torch.bfloat16, False),
+    (1, 2, 77, 300, 64, torch.float16, False),
+    (1, 2, 300, 77, 64, torch.bfloat16, True),     # Sq > Sk: late rows see every key
+    (1, 2, 77, 300, 128, torch.float16, True),     # Sq < Sk: top-left alignment
+    (2, 2, 640, 640, 128, torch.bfloat16, True),   # several tile pairs, odd tile count
+    (1, 1, 1000, 1000, 64, torch.float16, False),
+    (3, 2, 384, 512, 128, torch.bfloat16, False),
+]
+
+
+@pytest.mark.parametrize("B,H,Sq,Sk,D,dtype,causal", SHAPES)
+def test_shapes(B, H, Sq, Sk, D, dtype, causal):
+    q, k, v = inputs.make_dense(B, H, Sq, Sk, D, dtype, seed=Sq * 7 + Sk + D)
+    check(q, k, v, causal, 1.0 / D ** 0.5, what=f"{(B, H, Sq, Sk, D, dtype, causal)}")
+
+
+def test_non_default_scale():
+    q, k, v = inputs.make_dense(1, 2, 256, 256, 128, torch.bfloat16, seed=5)
+    check(q, k, v, True, 0.37, what="scale 0.37")
+    check(q, k, v, False, 0.02, what="scale 0.02")
+
+
+def test_llama_prefill_full_size_sampled_rows():
+    w = inputs.WORKLOADS["llama_prefill"]
+    q, k, v = inputs.make_workload(w)
+    rows = sample_rows(w.Sq, n_random=40, seed=w.seed)
+    check(q, k, v, True, w.scale, rows=rows, what=w.name)
+
+
+def test_causal_skipped_tiles_never_read():
+    """Causal, Sq = 256 < Sk = 512: keys 256.. are above every row's diagonal,
+    so their tiles are skipped. NaN there must not change a single bit."""
+    q, k, v = inputs.make_dense(2, 2, 256, 512, 128, torch.bfloat16, seed=11)
+    o1, l1 = run(q, k, v, True, 0.1)
+    k2, v2 = k.clone(), v.clone()
+    k2[:, :, 256:] = float("nan")
+    v2[:, :, 256:] = float("nan")
+    o2, l2 = run(q, k2, v2, True, 0.1)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+
+
+def test_causal_mask_inside_diagonal_tiles_is_exact():
+    """Rows [0, r) of a causal run depend on keys [0, r) only. With huge K/V
+    values planted in keys [r, S) (masked inside the straddling tile), rows
+    [0, r) must equal, bit for bit, a run on the first r rows and keys."""
+    S, r = 384, 200
+    q, k, v = inputs.make_dense(1, 2, S, S, 64, torch.float16, seed=12)
+    k2, v2 = k.clone(), v.clone()
+    k2[:, :, r:] = 3.0e4
+    v2[:, :, r:] = -3.0e4
+    o_full, l_full = run(q, k2, v2, True, 0.125)
+    o_cut, l_cut = run(q[:, :, :r].contiguous(), k[:, :, :r].contiguous(), v[:, :, :r].contiguous(), True, 0.125)
+    assert torch.equal(o_full[:, :, :r].view(torch.int16), o_cut.view(torch.int16))
+    assert torch.equal(l_full[:, :, :r].view(torch.int32), l_cut.view(torch.int32))
+
+
+def test_ragged_key_tail_is_masked():
+    """Non-causal, Sk = 200: the second key tile is zero-filled past key 199 by
+    TMA and must be masked, so the result equals the oracle over 200 keys."""
+    q, k, v = inputs.make_dense(1, 1, 128, 200, 64, torch.bfloat16, seed=13)
+    check(q, k, v, False, 0.125, what="ragged key tail")
+
+
+def test_outputs_do_not_spill_past_the_buffer():
+    B, H, Sq, D = 1, 2, 200, 128
+    q, k, v = dev(*inputs.make_dense(B, H, Sq, Sq, D, torch.bfloat16, seed=14))
+    o_buf = torch.full((B * H * Sq * D + 4096,), 1.5, dtype=torch.bfloat16, device="cuda")
+    l_buf = torch.full((B * H * Sq + 256,), 7.0, dtype=torch.float32, device="cuda")
+    o = o_buf[: B * H * Sq * D].view(B, H, Sq, D)
+    lse = l_buf[: B * H * Sq].view(B, H, Sq)
+    fa.fa_fwd(q, k, v, o, lse, True, 0.1)
+    torch.cuda.synchronize()
+    assert torch.all(o_buf[B * H * Sq * D:] == 1.5)
+    assert torch.all(l_buf[B * H * Sq:] == 7.0)
+
+
+def test_repeatable_bitwise():
+    q, k, v = inputs.make_dense(2, 4, 512, 512, 128, torch.bfloat16, seed=15)
+    o1, l1 = run(q, k, v, True, 0.09)
+    o2, l2 = run(q, k, v, True, 0.09)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+
+
+def test_non_default_stream():
+    q, k, v = dev(*inputs.make_dense(1, 2, 256, 256, 64, torch.float16, seed=16))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o, lse = fa.flash_attention(q, k, v, causal=True, scale=0.125, stream=s)
+    s.synchronize()
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), True, 0.125)
+    assert_close(o.cpu(), ro, O_TOL, "stream O")
+    assert_close(lse.cpu(), rl, LSE_TOL, "stream LSE")

@@ -1,0 +1,102 @@
+"""Packed variable-length forward (fa_fwd_varlen) against the fp64 oracle, plus
+exact checks of the sequence bookkeeping: every sequence must equal, bit for
+bit, a dense call on its own slice, and nothing may be written outside the
+output buffers."""
+import pytest
+import torch
+
+import exact_attention_54_gb300 as fa
+import oracle
+from exact_attention_54_gb300 import inputs
+from gpu_helpers import LSE_TOL, O_TOL, assert_close, dev, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def run_varlen(q, k, v, cu, causal, scale):
+    qd, kd, vd, cud = dev(q, k, v, cu)
+    mx = int((cu[1:] - cu[:-1]).max())
+    o, lse = fa.flash_attention_varlen(qd, kd, vd, cud, cud, max(mx, 1), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    return o.cpu(), lse.cpu()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D,dtype", [(64, torch.float16), (128, torch.bfloat16)])
+def test_small_varlen_all_rows(causal, D, dtype):
+    lengths = [1, 127, 128, 129, 0, 300, 5]
+    _, cu, q, k, v = inputs.make_varlen(len(lengths), 0, 0, 3, D, dtype, seed=21, lengths=lengths)
+    scale = 1.0 / D ** 0.5
+    o, lse = run_varlen(q, k, v, cu, causal, scale)
+    ro, rl = oracle.attention_varlen(q, k, v, cu, cu, causal, scale)
+    assert_close(o, ro, O_TOL, "varlen O")
+    assert_close(lse, rl, LSE_TOL, "varlen LSE")
+
+
+def test_varlen_equals_dense_per_sequence_bitwise():
+    lengths = [200, 1, 384, 129, 77]
+    H, D = 4, 128
+    _, cu, q, k, v = inputs.make_varlen(len(lengths), 0, 0, H, D, torch.bfloat16, seed=22, lengths=lengths)
+    o, lse = run_varlen(q, k, v, cu, True, 0.088)
+    for i, L in enumerate(lengths):
+        a, b = int(cu[i]), int(cu[i + 1])
+        qs, ks, vs = (x[a:b].transpose(0, 1).unsqueeze(0).contiguous() for x in (q, k, v))  # [1,H,L,D]
+        qd, kd, vd = dev(qs, ks, vs)
+        od, ld = fa.flash_attention(qd, kd, vd, causal=True, scale=0.088)
+        torch.cuda.synchronize()
+        assert torch.equal(o[a:b].view(torch.int16), od[0].transpose(0, 1).cpu().view(torch.int16)), f"seq {i} O"
+        assert torch.equal(lse[:, a:b].view(torch.int32), ld[0].cpu().view(torch.int32)), f"seq {i} LSE"
+
+
+def test_varlen_guards_untouched():
+    lengths = [130, 61, 257]
+    H, D = 2, 64
+    _, cu, q, k, v = inputs.make_varlen(len(lengths), 0, 0, H, D, torch.float16, seed=23, lengths=lengths)
+    T = int(cu[-1])
+    qd, kd, vd, cud = dev(q, k, v, cu)
+    o_buf = torch.full(((T + 64) * H * D,), -2.5, dtype=torch.float16, device="cuda")
+    l_buf = torch.full((H * T + 300,), 9.0, dtype=torch.float32, device="cuda")
+    o = o_buf[: T * H * D].view(T, H, D)
+    lse = l_buf[: H * T].view(H, T)
+    fa.fa_fwd_varlen(qd, kd, vd, o, lse, cud, cud, max(lengths), True, 0.125)
+    torch.cuda.synchronize()
+    assert torch.all(o_buf[T * H * D:] == -2.5)
+    assert torch.all(l_buf[H * T:] == 9.0)
+    ro, rl = oracle.attention_varlen(q, k, v, cu, cu, True, 0.125)
+    assert_close(o.cpu(), ro, O_TOL, "guarded O")
+    assert_close(lse.cpu(), rl, LSE_TOL, "guarded LSE")
+
+
+def test_varlen_poison_past_total_is_never_read():
+    """Buffers larger than total_tokens hold NaN past the end; the tensor maps
+    stop at total, so no NaN may reach any output."""
+    lengths = [100, 200]
+    H, D = 2, 128
+    _, cu, q, k, v = inputs.make_varlen(len(lengths), 0, 0, H, D, torch.bfloat16, seed=24, lengths=lengths)
+    T = int(cu[-1])
+    pad = torch.full((128, H, D), float("nan"), dtype=torch.bfloat16)
+    kp, vp = torch.cat([k, pad]), torch.cat([v, pad])
+    qd, kd, vd, cud = dev(q, kp, vp, cu)
+    o, lse = fa.flash_attention_varlen(qd, kd[:T], vd[:T], cud, cud, 200, causal=False, scale=0.1)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention_varlen(q, k, v, cu, cu, False, 0.1)
+    assert_close(o.cpu(), ro, O_TOL, "poisoned tail O")
+    assert_close(lse.cpu(), rl, LSE_TOL, "poisoned tail LSE")
+
+
+def test_varlen_workload_sampled_rows():
+    """16 sequences, lengths uniform on [64, 2048], H=16, D=128, bf16, causal:
+    every sequence checked on sampled rows (all heads)."""
+    w = inputs.WORKLOADS["varlen"]
+    lengths, cu, q, k, v = inputs.make_workload(w)
+    o, lse = run_varlen(q, k, v, cu, w.causal, w.scale)
+    for i in range(w.num_seqs):
+        a, b = int(cu[i]), int(cu[i + 1])
+        rows = sample_rows(b - a, n_random=8, seed=i)
+        qs, ks, vs = (x[a:b].transpose(0, 1) for x in (q, k, v))  # [H, L, D]
+        ro, rl = oracle.attention(qs, ks, vs, True, w.scale, rows=rows)
+        got_o = o[a:b].transpose(0, 1)[:, rows]
+        got_l = lse[:, a:b][:, rows]
+        assert_close(got_o, ro, O_TOL, f"seq {i} O")
+        assert_close(got_l, rl, LSE_TOL, f"seq {i} LSE")

@@ -54,6 +54,9 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=50, help="steps of the end-to-end (host buffer) loop")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end loop (profiling runs)")
+    ap.add_argument("--parts", default="prefill,decode",
+                    help="comma list of the path parts to run (profiling runs may isolate one)")
     return ap.parse_args(argv)
 
 
@@ -326,17 +329,23 @@ def run_gpu(args, rank, world, local):
     pf_flops = attention_flops(wp.B, wp.H, wp.Sq, wp.Sk, wp.D, wp.causal)
     dc_bytes = decode_bytes(wd.B, wd.H, wd.Sk, wd.D)
 
+    parts = set(args.parts.split(","))
+    run_pf, run_dc = "prefill" in parts, "decode" in parts
+
     def step(evs=None):
         flush.fill_(float(1.0))
         if evs:
             evs[0].record(stream)
-        fa.fa_fwd(q, k, v, o, lse, wp.causal, wp.scale, stream)
+        if run_pf:
+            fa.fa_fwd(q, k, v, o, lse, wp.causal, wp.scale, stream)
         if evs:
             evs[1].record(stream)
-        fa.fa_decode_splitkv(dq, dk, dv, *ws, S, wd.scale, stream)
+        if run_dc:
+            fa.fa_decode_splitkv(dq, dk, dv, *ws, S, wd.scale, stream)
         if evs:
             evs[2].record(stream)
-        fa.fa_splitkv_merge(*ws, do, dlse, stream)
+        if run_dc:
+            fa.fa_splitkv_merge(*ws, do, dlse, stream)
         if evs:
             evs[3].record(stream)
 
@@ -374,8 +383,11 @@ def run_gpu(args, rank, world, local):
     prefill_tflops = world * pf_flops * K / (pf_sum * 1e-3) / 1e12
     decode_gbs = world * dc_bytes * K / (dc_sum * 1e-3) / 1e9
 
+    if not (run_pf and run_dc):  # a profiling run of one part: no report
+        return None
     # end-to-end through host buffers (pinned), copies inside the timed region
-    e2e = run_e2e(args, fa, torch, stream, dev, wp, wd, (q, k, v), (dq, dk, dv), world)
+    e2e = ({"prefill": None, "decode": None} if args.no_e2e else
+           run_e2e(args, fa, torch, stream, dev, wp, wd, (q, k, v), (dq, dk, dv), world))
 
     peaks, peak_src = load_peaks()
     traffic = committed_traffic()

@@ -74,7 +74,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const int s = blockIdx.x % num_splits;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int sub = lane % kLanesPerKey;                  // which 8 elements of the row
-    const int g = warp * kKeysPerWarp + lane / kLanesPerKey;
+    const int gw = lane / kLanesPerKey;                   // lane group within the warp
+    const int g = warp * kKeysPerWarp + gw;
     const int k_lo = s * keys_per_split;
     const int k_hi = min(k_lo + keys_per_split, Sk);
 
@@ -90,7 +91,10 @@ __global__ void __launch_bounds__(kDecodeThreads)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
 
-    for (int key0 = k_lo + g; key0 < k_hi; key0 += kGroups * U) {
+    // The trip count depends on the warp only (never on the lane group), so every
+    // lane reaches every shuffle below; keys past k_hi are predicated off.
+    for (int base = k_lo + warp * kKeysPerWarp; base < k_hi; base += kGroups * U) {
+        const int key0 = base + gw;
         uint4 kr[U], vr[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {

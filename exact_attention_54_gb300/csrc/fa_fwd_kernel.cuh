@@ -152,8 +152,10 @@ __device__ void fwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
         if (wi > 0 && !(ok = ptx::bar_wait(bar(S::kQEmpty), (wi - 1) & 1, abort_flag, p.timeout_ns)))
             break;
         uint32_t qbytes = 0;
+        #pragma unroll
         for (int t = 0; t < 2; ++t) qbytes += wk.n_kv[t] > 0 ? S::kTileBytes : 0;
         ptx::bar_arrive_expect_tx(bar(S::kQFull), qbytes);
+        #pragma unroll
         for (int t = 0; t < 2; ++t) {
             if (wk.n_kv[t] == 0) continue;
             for (int c = 0; c < S::kColBlocks; ++c) {
@@ -244,6 +246,7 @@ __device__ void fwd_mma(const FwdParams &p, uint32_t sbase, uint32_t tmem, volat
             if (!(ok = ptx::bar_wait(bar(S::kKFull + st0), (it / S::kStages) & 1, abort_flag, p.timeout_ns)))
                 break;
             ptx::tc_fence_after();
+            #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (wk.n_kv[t] == 0) continue;
                 issue_qk(t, st0);
@@ -254,6 +257,7 @@ __device__ void fwd_mma(const FwdParams &p, uint32_t sbase, uint32_t tmem, volat
             const uint32_t itj = it + j;
             const uint32_t stage = itj % S::kStages;
             bool v_ready = false;
+            #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (j >= wk.n_kv[t]) continue;
                 if (!(ok = ptx::bar_wait(bar(S::kPFull + t), cnt[t] & 1, abort_flag, p.timeout_ns))) break;

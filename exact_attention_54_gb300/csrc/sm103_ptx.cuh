@@ -239,6 +239,18 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool b
            | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
+// Re-balance the register file between warpgroups; every warp of the
+// warpgroup must execute the same instruction. The sum over warpgroups must
+// stay within what the block was launched with.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------- math --
 
 __device__ __forceinline__ float ex2(float x) {

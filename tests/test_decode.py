@@ -57,6 +57,8 @@ def test_decode_workload_full_size():
     (2, 2, 1000, 64, torch.float16, 1),     # no split at all
     (1, 4, 4099, 128, torch.float16, 7),    # ragged partitions
     (3, 1, 513, 64, torch.bfloat16, 16),
+    (2, 2, 99, 128, torch.bfloat16, 33),    # three keys per partition: lane groups of a warp disagree
+    (1, 3, 10, 64, torch.float16, 5),       # two keys per partition, four lane groups per warp
 ])
 def test_decode_shapes(B, H, Sk, D, dtype, S):
     q, k, v = inputs.make_dense(B, H, 1, Sk, D, dtype, seed=Sk + S)

@@ -67,6 +67,6 @@ def test_decode_shapes(B, H, Sk, D, dtype, S):
 
 def test_decode_split_count_does_not_change_the_answer():
     q, k, v = inputs.make_dense(2, 2, 1, 2048, 128, torch.bfloat16, seed=31)
-    outs = [run_decode(q, k, v, S, 0.088)[0].float() for S in (1, 8, 32, 2048)]
+    outs = [run_decode(q, k, v, S, 0.088)[0].float() for S in (1, 8, 32, 1024)]
     for o in outs[1:]:
         assert_close(o, outs[0], 2 * O_TOL, "split count")

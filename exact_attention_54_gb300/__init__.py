@@ -198,3 +198,21 @@ def flash_decode(q, k, v, num_splits: int, scale: float | None = None, stream=No
     fa_decode_splitkv(q, k, v, o_part, m_part, l_part, num_splits, scale, stream)
     fa_splitkv_merge(o_part, m_part, l_part, o, lse, stream)
     return o, lse
+
+
+def fa_decode_noalloc(q, k, v, o, lse, num_splits: int, scale: float | None = None, stream=None):
+    """Split-KV decoding (both phases) with no device allocation and no
+    workspace argument, for callers that cannot allocate device memory when
+    they call in. The partials use a fixed device array built into the
+    library (FA_NOALLOC_SCRATCH_FLOATS floats); concurrent calls whose GPU work
+    overlaps race on it. q [B,H,1,D]; k, v [B,H,Sk,D]; o [B,H,1,D]; lse [B,H]."""
+    lib = load_library()
+    fn = lib.fa_decode_noalloc
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    fn.restype = ctypes.c_int
+    B, H, Sk, D = k.shape
+    _need_contig(q, k, v, o, lse)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    _check("fa_decode_noalloc", fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sk, D, int(num_splits),
+                                   float(scale), _dtype_code(k), _stream(stream)))

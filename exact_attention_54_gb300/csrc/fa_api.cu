@@ -107,6 +107,7 @@ const char *fa_status_string(fa_status_t s) {
         case FA_ERR_SCALE: return "scale must be finite and positive";
         case FA_ERR_CUDA: return "CUDA runtime error";
         case FA_ERR_DEVICE_TIMEOUT: return "a kernel abandoned a barrier wait (device timeout)";
+        case FA_ERR_SCRATCH: return "problem larger than the built-in decode scratch";
     }
     return "unknown status";
 }

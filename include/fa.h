@@ -53,7 +53,8 @@ typedef enum {
     FA_ERR_SPLITS = -6,         /* num_splits < 1 or > Sk (or > FA_MAX_SPLITS) */
     FA_ERR_SCALE = -7,          /* scale is not finite and > 0 */
     FA_ERR_CUDA = -8,           /* the CUDA runtime reported an error (launch, tensor map) */
-    FA_ERR_DEVICE_TIMEOUT = -9  /* a kernel gave up waiting on an on-chip barrier */
+    FA_ERR_DEVICE_TIMEOUT = -9, /* a kernel gave up waiting on an on-chip barrier */
+    FA_ERR_SCRATCH = -10        /* fa_decode_noalloc: problem larger than its built-in scratch */
 } fa_status_t;
 
 typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype_t;
@@ -152,6 +153,33 @@ FA_API fa_status_t fa_splitkv_merge(const float *o_part, const float *m_part, co
  * itself reports an error.
  */
 FA_API fa_status_t fa_check_device_error(void *stream);
+
+/*
+ * fa_decode_noalloc - split-KV decoding (phase 1 and phase 2 in one call) that
+ * allocates nothing and needs no caller workspace. The pages have no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory when they call in (an engine hook that must not allocate, a
+ * latency-critical loop that cannot take the device-wide synchronisation an
+ * allocation may bring, a process whose memory a pool has fully reserved).
+ *
+ * The partials live in a fixed device array built into the library, of
+ * FA_NOALLOC_SCRATCH_FLOATS floats (8 MiB), which every GPU that loads the
+ * library holds until the process exits. A call needs
+ * B*H*num_splits*D + 2*B*H*num_splits floats (each part rounded up to 4);
+ * larger problems return FA_ERR_SCRATCH before anything is enqueued. The
+ * first call on a device looks up the array's device address (with that
+ * device current); make it before any stream capture. All calls share the
+ * array: calls whose work overlaps on the GPU race and must be serialised by
+ * the caller. Nothing needs clearing between calls.
+ *
+ *   q [B,H,1,D], k and v [B,H,Sk,D], o [B,H,1,D] (dtype), lse [B,H] fp32.
+ *   Results equal fa_decode_splitkv followed by fa_splitkv_merge.
+ * Errors: as fa_decode_splitkv, plus FA_ERR_SCRATCH.
+ */
+#define FA_NOALLOC_SCRATCH_FLOATS (2 * 1024 * 1024)
+FA_API fa_status_t fa_decode_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                                     int B, int H, int Sk, int D, int num_splits, float scale,
+                                     fa_dtype_t dtype, void *stream);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 FA_API const char *fa_status_string(fa_status_t status);

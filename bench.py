@@ -380,11 +380,20 @@ def run_gpu(args, rank, world, local):
     pf_sum, sp_sum, mg_sum = sum(pf), sum(sp), sum(mg)
     pf_sum, dc_sum, wall = aggregate_max([pf_sum, sp_sum + mg_sum, wall], world)
     K = args.steps
+
+    if not (run_pf and run_dc):  # a profiling run of one part: a short record, not the report
+        rec = {"part": args.parts, "steps": args.steps, "clocks": clock}
+        if run_pf:
+            rec.update(prefill_tflops=pf_flops / (statistics.mean(pf) * 1e-3) / 1e12,
+                       prefill_ms=statistics.mean(pf), prefill_ms_median=statistics.median(pf))
+        if run_dc:
+            rec.update(decode_gbs=dc_bytes / ((statistics.mean(sp) + statistics.mean(mg)) * 1e-3) / 1e9,
+                       split_ms=statistics.mean(sp), merge_ms=statistics.mean(mg))
+        if rank == 0:
+            print(json.dumps(rec), flush=True)
+        return None
     prefill_tflops = world * pf_flops * K / (pf_sum * 1e-3) / 1e12
     decode_gbs = world * dc_bytes * K / (dc_sum * 1e-3) / 1e9
-
-    if not (run_pf and run_dc):  # a profiling run of one part: no report
-        return None
     # end-to-end through host buffers (pinned), copies inside the timed region
     e2e = ({"prefill": None, "decode": None} if args.no_e2e else
            run_e2e(args, fa, torch, stream, dev, wp, wd, (q, k, v), (dq, dk, dv), world))

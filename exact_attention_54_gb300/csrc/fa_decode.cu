@@ -20,6 +20,7 @@
 
 #include <cstdint>
 
+#include "fa.h"
 #include "fa_launch.h"
 #include "sm103_ptx.cuh"
 
@@ -171,36 +172,87 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
 }
 
-// grid: one CTA per head, D threads (one output element each).
+// grid: one CTA per head, kMergeThreads threads = kGroups groups of D (one
+// output element per thread and group). The weights e^{m_s - m_g} are computed
+// once per partition in parallel and kept in shared memory; each group then
+// sums every kGroups-th partition with eight independent loads in flight, and
+// the group sums are added through shared memory.
+constexpr int kMergeThreads = 256;
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float *red) {
+    constexpr int kWarps = kMergeThreads / 32;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, v, off);
+        v = is_max ? fmaxf(v, o) : v + o;
+    }
+    if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = v;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int i = 1; i < kWarps; ++i) r = is_max ? fmaxf(r, red[i]) : r + red[i];
+    __syncthreads();
+    return r;
+}
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(D)
+__global__ void __launch_bounds__(kMergeThreads)
     fa_splitkv_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ m_part,
                             const float *__restrict__ l_part, uint16_t *__restrict__ o, float *__restrict__ lse,
                             int num_splits) {
+    constexpr int kGroups = kMergeThreads / D;
+    constexpr int U = 8;
+    __shared__ float w[FA_MAX_SPLITS];
+    __shared__ float red[kMergeThreads / 32];
+    __shared__ float part[kGroups][D];
     const int bh = blockIdx.x;
-    const int d = threadIdx.x;
+    const int tid = threadIdx.x;
+    const int g = tid / D, d = tid % D;
     const float *mp = m_part + static_cast<size_t>(bh) * num_splits;
     const float *lp = l_part + static_cast<size_t>(bh) * num_splits;
     const float *op = o_part + static_cast<size_t>(bh) * num_splits * D + d;
-    float mg = -CUDART_INF_F;
-    for (int s = 0; s < num_splits; ++s) mg = fmaxf(mg, mp[s]);
-    float lg = 0.f, acc = 0.f;
-    if (mg != -CUDART_INF_F) {
-        for (int s = 0; s < num_splits; ++s) {
-            const float w = expf(mp[s] - mg);
-            lg = fmaf(w, lp[s], lg);
-            acc = fmaf(w, op[static_cast<size_t>(s) * D], acc);
+
+    float mx = -CUDART_INF_F;
+    for (int s = tid; s < num_splits; s += kMergeThreads) mx = fmaxf(mx, mp[s]);
+    const float mg = block_reduce(mx, true, red);
+    float lsum = 0.f;
+    for (int s = tid; s < num_splits; s += kMergeThreads) {
+        const float ws = (mg == -CUDART_INF_F) ? 0.f : expf(mp[s] - mg);
+        w[s] = ws;
+        lsum = fmaf(ws, lp[s], lsum);
+    }
+    const float lg = block_reduce(lsum, false, red);  // its barriers also publish w[]
+
+    float acc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) acc[u] = 0.f;
+    int s = g;
+    for (; s + (U - 1) * kGroups < num_splits; s += U * kGroups) {
+        float x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) x[u] = op[static_cast<size_t>(s + u * kGroups) * D];
+#pragma unroll
+        for (int u = 0; u < U; ++u) acc[u] = fmaf(w[s + u * kGroups], x[u], acc[u]);
+    }
+    for (; s < num_splits; s += kGroups) acc[0] = fmaf(w[s], op[static_cast<size_t>(s) * D], acc[0]);
+    float total = 0.f;
+#pragma unroll
+    for (int u = 0; u < U; ++u) total += acc[u];
+    part[g][d] = total;
+    __syncthreads();
+    if (g == 0) {
+#pragma unroll
+        for (int i = 1; i < kGroups; ++i) total += part[i][d];
+        const float out = lg > 0.f ? total / lg : 0.f;
+        if constexpr (BF16) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(out);
+            o[static_cast<size_t>(bh) * D + d] = *reinterpret_cast<const uint16_t *>(&h);
+        } else {
+            const __half h = __float2half_rn(out);
+            o[static_cast<size_t>(bh) * D + d] = *reinterpret_cast<const uint16_t *>(&h);
         }
+        if (d == 0) lse[bh] = lg > 0.f ? mg + logf(lg) : -CUDART_INF_F;
     }
-    const float out = lg > 0.f ? acc / lg : 0.f;
-    if constexpr (BF16) {
-        const __nv_bfloat16 h = __float2bfloat16_rn(out);
-        o[static_cast<size_t>(bh) * D + d] = *reinterpret_cast<const uint16_t *>(&h);
-    } else {
-        const __half h = __float2half_rn(out);
-        o[static_cast<size_t>(bh) * D + d] = *reinterpret_cast<const uint16_t *>(&h);
-    }
-    if (d == 0) lse[bh] = lg > 0.f ? mg + logf(lg) : -CUDART_INF_F;
 }
 
 template <int D, bool BF16>
@@ -216,7 +268,7 @@ static cudaError_t launch_split_t(const void *q, const void *k, const void *v, f
 template <int D, bool BF16>
 static cudaError_t launch_merge_t(const float *op, const float *mp, const float *lp, void *o, float *lse, int BH,
                                   int S, cudaStream_t st) {
-    fa_splitkv_merge_kernel<D, BF16><<<BH, D, 0, st>>>(op, mp, lp, static_cast<uint16_t *>(o), lse, S);
+    fa_splitkv_merge_kernel<D, BF16><<<BH, kMergeThreads, 0, st>>>(op, mp, lp, static_cast<uint16_t *>(o), lse, S);
     return cudaGetLastError();
 }
 

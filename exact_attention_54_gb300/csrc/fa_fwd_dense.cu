@@ -16,3 +16,4 @@ cudaError_t launch_fwd_dense(int D, bool bf16, bool causal, const CUtensorMap *m
 }
 
 }  // namespace fa
+

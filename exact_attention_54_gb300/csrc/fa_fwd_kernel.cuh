@@ -12,8 +12,11 @@
 // that straddle it are masked (k_idx <= q_idx, top-left aligned).
 //
 // GB300 mapping (one CTA per SM, persistent):
-//   warp 0        TMA producer: Q tile pair once per work item, then a ring of
-//                 K/V stages (128-byte swizzle, 128 rows x 64 columns per box)
+//   warp 0        TMA producer of Q (a tile pair once per work item, plus an L2
+//                 prefetch of the next item's pair) and of the K ring
+//                 (128-byte swizzle, 128 rows x 64 columns per box)
+//   warp 2        TMA producer of the V ring (K and V rings are separate, so K
+//                 tiles, needed first, are released and refilled earlier)
 //   warp 1        MMA issuer (one thread): S_t = Q_t K^T into TMEM, then
 //                 O_t += P_t V with P_t read from TMEM (A operand) and V
 //                 MN-major from shared memory. Also owns the TMEM allocation.
@@ -50,17 +53,19 @@ struct FwdShape {
     static constexpr int kColBlocks = D / 64;            // 128-byte column blocks per row
     static constexpr int kBlockBytes = kBlockM * 128;    // one 128-row x 64-column box
     static constexpr int kTileBytes = kBlockM * D * 2;   // one 128-row tile of Q, K or V
-    static constexpr int kStages = (D == 128) ? 2 : 4;   // K/V ring depth
+    static constexpr int kKStages = (D == 128) ? 3 : 4;  // K ring depth (K is needed first)
+    static constexpr int kVStages = (D == 128) ? 2 : 4;  // V ring depth
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + 2 * kTileBytes;
-    static constexpr int kOffV = kOffK + kStages * kTileBytes;
-    static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+    static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+    static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
     // barrier indices
     static constexpr int kQFull = 0, kQEmpty = 1, kTeardown = 2;
     static constexpr int kKFull = 3;
-    static constexpr int kVFull = kKFull + kStages;
-    static constexpr int kKVEmpty = kVFull + kStages;
-    static constexpr int kSFull = kKVEmpty + kStages;    // +t
+    static constexpr int kKEmpty = kKFull + kKStages;
+    static constexpr int kVFull = kKEmpty + kKStages;
+    static constexpr int kVEmpty = kVFull + kVStages;
+    static constexpr int kSFull = kVEmpty + kVStages;    // +t
     static constexpr int kPFull = kSFull + 2;            // +t
     static constexpr int kODone = kPFull + 2;            // +t
     static constexpr int kNumBars = kODone + 2;
@@ -69,6 +74,7 @@ struct FwdShape {
     static constexpr uint32_t kTmemS = 0;                     // + t * 128
     static constexpr uint32_t kTmemO = 256;                   // + t * D
     static constexpr uint32_t kTmemCols = 512;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
 // One unit of work: a pair of consecutive 128-row query tiles of one
@@ -135,13 +141,46 @@ __device__ __forceinline__ int work_index(int r) {
 
 // ------------------------------------------------------------------ roles --
 
+// Loads one K or V tile (all 64-column boxes) of key tile j into `dst`.
+template <int D, bool VARLEN>
+__device__ __forceinline__ void load_kv_tile(const CUtensorMap *tm, uint32_t dst, uint32_t bar, const Work &wk,
+                                             int j, int H) {
+    using S = FwdShape<D>;
+#pragma unroll
+    for (int c = 0; c < S::kColBlocks; ++c) {
+        if constexpr (VARLEN)
+            ptx::tma_load_3d(dst + c * S::kBlockBytes, tm, bar, c * 64, wk.h, wk.seq_k0 + j * kBlockN);
+        else
+            ptx::tma_load_3d(dst + c * S::kBlockBytes, tm, bar, c * 64, j * kBlockN, wk.b * H + wk.h);
+    }
+}
+
+// Q and K producer (one thread). Also asks L2 for the next work item's Q
+// tiles while the current item runs.
 template <int D, bool CAUSAL, bool VARLEN>
-__device__ void fwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
-                             const FwdParams &p, uint32_t sbase, volatile int *abort_flag) {
+__device__ void fwd_producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, const FwdParams &p, uint32_t sbase,
+                                volatile int *abort_flag) {
     using S = FwdShape<D>;
     const uint32_t bars = sbase + S::kOffBar;
     auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
-    uint32_t it = 0;  // K/V tiles issued
+    const bool leader = ptx::elect_one();
+    auto prefetch_q = [&](int w) {
+        if (w >= p.num_work) return;
+        const Work nx = get_work<CAUSAL, VARLEN>(p, w);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            if (nx.n_kv[t] == 0) continue;
+#pragma unroll
+            for (int c = 0; c < S::kColBlocks; ++c) {
+                if (!leader) continue;
+                if constexpr (VARLEN)
+                    ptx::tma_prefetch_3d(tq, c * 64, nx.h, nx.seq_q0 + nx.q_start[t]);
+                else
+                    ptx::tma_prefetch_3d(tq, c * 64, nx.q_start[t], nx.b * p.H + nx.h);
+            }
+        }
+    };
+    uint32_t it = 0;  // K tiles issued
     uint32_t wi = 0;  // work items loaded
     bool ok = true;
     for (int r = 0; ok; ++r) {
@@ -149,15 +188,16 @@ __device__ void fwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
         if (w >= p.num_work) break;
         const Work wk = get_work<CAUSAL, VARLEN>(p, w);
         if (wk.n_kv_max == 0) continue;
-        if (wi > 0 && !(ok = ptx::bar_wait(bar(S::kQEmpty), (wi - 1) & 1, abort_flag, p.timeout_ns)))
+        if (wi > 0 && !(ok = ptx::warp_all(ptx::bar_wait(bar(S::kQEmpty), (wi - 1) & 1, abort_flag, p.timeout_ns))))
             break;
         uint32_t qbytes = 0;
-        #pragma unroll
+#pragma unroll
         for (int t = 0; t < 2; ++t) qbytes += wk.n_kv[t] > 0 ? S::kTileBytes : 0;
-        ptx::bar_arrive_expect_tx(bar(S::kQFull), qbytes);
-        #pragma unroll
+        if (leader) ptx::bar_arrive_expect_tx(bar(S::kQFull), qbytes);
+#pragma unroll
         for (int t = 0; t < 2; ++t) {
-            if (wk.n_kv[t] == 0) continue;
+            if (wk.n_kv[t] == 0 || !leader) continue;
+#pragma unroll
             for (int c = 0; c < S::kColBlocks; ++c) {
                 const uint32_t dst = sbase + S::kOffQ + t * S::kTileBytes + c * S::kBlockBytes;
                 if constexpr (VARLEN)
@@ -166,39 +206,60 @@ __device__ void fwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
                     ptx::tma_load_3d(dst, tq, bar(S::kQFull), c * 64, wk.q_start[t], wk.b * p.H + wk.h);
             }
         }
+        prefetch_q(work_index(r + 1));
         for (int j = 0; j < wk.n_kv_max; ++j, ++it) {
-            const uint32_t stage = it % S::kStages;
-            if (it >= S::kStages &&
-                !(ok = ptx::bar_wait(bar(S::kKVEmpty + stage), ((it / S::kStages) - 1) & 1, abort_flag,
-                                     p.timeout_ns)))
+            const uint32_t stage = it % S::kKStages;
+            if (it >= S::kKStages &&
+                !(ok = ptx::warp_all(ptx::bar_wait(bar(S::kKEmpty + stage), ((it / S::kKStages) - 1) & 1, abort_flag,
+                                     p.timeout_ns))))
                 break;
-            ptx::bar_arrive_expect_tx(bar(S::kKFull + stage), S::kTileBytes);
-            for (int c = 0; c < S::kColBlocks; ++c) {
-                const uint32_t dst = sbase + S::kOffK + stage * S::kTileBytes + c * S::kBlockBytes;
-                if constexpr (VARLEN)
-                    ptx::tma_load_3d(dst, tk, bar(S::kKFull + stage), c * 64, wk.h, wk.seq_k0 + j * kBlockN);
-                else
-                    ptx::tma_load_3d(dst, tk, bar(S::kKFull + stage), c * 64, j * kBlockN, wk.b * p.H + wk.h);
-            }
-            ptx::bar_arrive_expect_tx(bar(S::kVFull + stage), S::kTileBytes);
-            for (int c = 0; c < S::kColBlocks; ++c) {
-                const uint32_t dst = sbase + S::kOffV + stage * S::kTileBytes + c * S::kBlockBytes;
-                if constexpr (VARLEN)
-                    ptx::tma_load_3d(dst, tv, bar(S::kVFull + stage), c * 64, wk.h, wk.seq_k0 + j * kBlockN);
-                else
-                    ptx::tma_load_3d(dst, tv, bar(S::kVFull + stage), c * 64, j * kBlockN, wk.b * p.H + wk.h);
+            if (leader) {
+                ptx::bar_arrive_expect_tx(bar(S::kKFull + stage), S::kTileBytes);
+                load_kv_tile<D, VARLEN>(tk, sbase + S::kOffK + stage * S::kTileBytes, bar(S::kKFull + stage), wk, j,
+                                        p.H);
             }
         }
         ++wi;
     }
     // Never leave with copies in flight: wait (bounded, even after an abort)
     // for the newest load into every stage and for the newest Q load.
-    for (uint32_t s = 0; s < S::kStages && s < it; ++s) {
-        const uint32_t last = (it - 1) - ((it - 1 - s) % S::kStages);
-        ptx::bar_wait(bar(S::kKFull + s), (last / S::kStages) & 1, nullptr, p.timeout_ns);
-        ptx::bar_wait(bar(S::kVFull + s), (last / S::kStages) & 1, nullptr, p.timeout_ns);
+    for (uint32_t s = 0; s < S::kKStages && s < it; ++s) {
+        const uint32_t last = (it - 1) - ((it - 1 - s) % S::kKStages);
+        ptx::bar_wait(bar(S::kKFull + s), (last / S::kKStages) & 1, nullptr, p.timeout_ns);
     }
     if (wi > 0) ptx::bar_wait(bar(S::kQFull), (wi - 1) & 1, nullptr, p.timeout_ns);
+}
+
+// V producer (one thread): runs ahead of the P V products as far as its ring allows.
+template <int D, bool CAUSAL, bool VARLEN>
+__device__ void fwd_producer_v(const CUtensorMap *tv, const FwdParams &p, uint32_t sbase, volatile int *abort_flag) {
+    using S = FwdShape<D>;
+    const uint32_t bars = sbase + S::kOffBar;
+    auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+    const bool leader = ptx::elect_one();
+    uint32_t it = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+        const int w = work_index(r);
+        if (w >= p.num_work) break;
+        const Work wk = get_work<CAUSAL, VARLEN>(p, w);
+        for (int j = 0; j < wk.n_kv_max; ++j, ++it) {
+            const uint32_t stage = it % S::kVStages;
+            if (it >= S::kVStages &&
+                !(ok = ptx::warp_all(ptx::bar_wait(bar(S::kVEmpty + stage), ((it / S::kVStages) - 1) & 1, abort_flag,
+                                     p.timeout_ns))))
+                break;
+            if (leader) {
+                ptx::bar_arrive_expect_tx(bar(S::kVFull + stage), S::kTileBytes);
+                load_kv_tile<D, VARLEN>(tv, sbase + S::kOffV + stage * S::kTileBytes, bar(S::kVFull + stage), wk, j,
+                                        p.H);
+            }
+        }
+    }
+    for (uint32_t s = 0; s < S::kVStages && s < it; ++s) {
+        const uint32_t last = (it - 1) - ((it - 1 - s) % S::kVStages);
+        ptx::bar_wait(bar(S::kVFull + s), (last / S::kVStages) & 1, nullptr, p.timeout_ns);
+    }
 }
 
 template <int D, bool BF16, bool CAUSAL, bool VARLEN>
@@ -209,30 +270,39 @@ __device__ void fwd_mma(const FwdParams &p, uint32_t sbase, uint32_t tmem, volat
     const uint32_t bars = sbase + S::kOffBar;
     auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
 
+    const bool leader = ptx::elect_one();
+    // Operand descriptors are built once; each MMA only advances the 14-bit
+    // start-address field (16-byte units), so issuing stays a few instructions
+    // per MMA. Stage buffers are contiguous, so stage s adds s * tile / 16.
+    const uint64_t dq0 = ptx::smem_desc_sw128(sbase + S::kOffQ, 16, 1024);
+    const uint64_t dk0 = ptx::smem_desc_sw128(sbase + S::kOffK, 16, 1024);
+    const uint64_t dv0 = ptx::smem_desc_sw128(sbase + S::kOffV, S::kBlockBytes, 1024);
+    constexpr uint64_t kTile16 = S::kTileBytes >> 4;
+
     // S_t = Q_t K^T: D/16 MMAs of K=16, both operands K-major, 128-byte swizzled.
     auto issue_qk = [&](int t, uint32_t stage) {
-        const uint32_t q0 = sbase + S::kOffQ + t * S::kTileBytes;
-        const uint32_t k0 = sbase + S::kOffK + stage * S::kTileBytes;
+        const uint64_t qd = dq0 + static_cast<uint64_t>(t) * kTile16;
+        const uint64_t kd = dk0 + static_cast<uint64_t>(stage) * kTile16;
+        const uint32_t dst = tmem + S::kTmemS + t * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * S::kBlockBytes + (kk % 4) * 32;
-            ptx::mma_ss(tmem + S::kTmemS + t * 128, ptx::smem_desc_sw128(q0 + off, 16, 1024),
-                        ptx::smem_desc_sw128(k0 + off, 16, 1024), kIdescQK, kk > 0);
+            constexpr uint64_t kBlock16 = S::kBlockBytes >> 4;
+            const uint64_t off = (kk / 4) * kBlock16 + (kk % 4) * 2;
+            ptx::mma_ss(dst, qd + off, kd + off, kIdescQK, kk > 0);
         }
     };
     // O_t (+)= P_t V: 128/16 MMAs of K=16; P_t from TMEM (two 16-bit values per
     // column), V MN-major: 64-column boxes 16 KB apart, 8-key atoms 1 KB apart.
     auto issue_pv = [&](int t, uint32_t stage, bool accumulate) {
-        const uint32_t v0 = sbase + S::kOffV + stage * S::kTileBytes;
+        const uint64_t vd = dv0 + static_cast<uint64_t>(stage) * kTile16;
+        const uint32_t dst = tmem + S::kTmemO + t * D;
+        const uint32_t pa = tmem + S::kTmemS + t * 128;
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-            ptx::mma_ts(tmem + S::kTmemO + t * D, tmem + S::kTmemS + t * 128 + kk * 8,
-                        ptx::smem_desc_sw128(v0 + kk * 2048, S::kBlockBytes, 1024), kIdescPV,
-                        (accumulate || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+            ptx::mma_ts(dst, pa + kk * 8, vd + kk * (2048 >> 4), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
     };
 
-    uint32_t it = 0, wi = 0;
+    uint32_t it = 0, wi = 0;   // K/V tiles consumed, work items consumed
     uint32_t cnt[2] = {0, 0};  // PV steps issued per query tile (= P_FULL phases consumed)
     bool ok = true;
     for (int r = 0; ok; ++r) {
@@ -240,57 +310,71 @@ __device__ void fwd_mma(const FwdParams &p, uint32_t sbase, uint32_t tmem, volat
         if (w >= p.num_work) break;
         const Work wk = get_work<CAUSAL, VARLEN>(p, w);
         if (wk.n_kv_max == 0) continue;
-        if (!(ok = ptx::bar_wait(bar(S::kQFull), wi & 1, abort_flag, p.timeout_ns))) break;
+        if (!(ok = ptx::warp_all(ptx::bar_wait(bar(S::kQFull), wi & 1, abort_flag, p.timeout_ns)))) break;
         {
-            const uint32_t st0 = it % S::kStages;
-            if (!(ok = ptx::bar_wait(bar(S::kKFull + st0), (it / S::kStages) & 1, abort_flag, p.timeout_ns)))
+            const uint32_t ks = it % S::kKStages;
+            if (!(ok = ptx::warp_all(ptx::bar_wait(bar(S::kKFull + ks), (it / S::kKStages) & 1, abort_flag, p.timeout_ns))))
                 break;
             ptx::tc_fence_after();
-            #pragma unroll
+#pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (wk.n_kv[t] == 0) continue;
-                issue_qk(t, st0);
-                ptx::mma_commit(bar(S::kSFull + t));
+                if (leader) {
+                    issue_qk(t, ks);
+                    ptx::mma_commit(bar(S::kSFull + t));
+                }
             }
+            if (leader) ptx::mma_commit(bar(S::kKEmpty + ks));  // K tile 0 has all its readers
         }
         for (int j = 0; j < wk.n_kv_max && ok; ++j) {
             const uint32_t itj = it + j;
-            const uint32_t stage = itj % S::kStages;
-            bool v_ready = false;
-            #pragma unroll
+            const uint32_t vs = itj % S::kVStages;
+            const uint32_t kn = (itj + 1) % S::kKStages;
+            bool v_ready = false, k_next_used = false;
+#pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (j >= wk.n_kv[t]) continue;
-                if (!(ok = ptx::bar_wait(bar(S::kPFull + t), cnt[t] & 1, abort_flag, p.timeout_ns))) break;
+                if (!(ok = ptx::warp_all(ptx::bar_wait(bar(S::kPFull + t), cnt[t] & 1, abort_flag, p.timeout_ns)))) break;
                 if (!v_ready) {
-                    if (!(ok = ptx::bar_wait(bar(S::kVFull + stage), (itj / S::kStages) & 1, abort_flag,
-                                             p.timeout_ns)))
+                    if (!(ok = ptx::warp_all(ptx::bar_wait(bar(S::kVFull + vs), (itj / S::kVStages) & 1, abort_flag,
+                                             p.timeout_ns))))
                         break;
                     v_ready = true;
                 }
                 ptx::tc_fence_after();
-                issue_pv(t, stage, j > 0);
-                ptx::mma_commit(bar(S::kODone + t));
+                if (leader) {
+                    issue_pv(t, vs, j > 0);
+                    ptx::mma_commit(bar(S::kODone + t));
+                }
                 ++cnt[t];
                 if (j + 1 < wk.n_kv[t]) {
-                    const uint32_t itn = itj + 1;
-                    const uint32_t sn = itn % S::kStages;
-                    if (!(ok = ptx::bar_wait(bar(S::kKFull + sn), (itn / S::kStages) & 1, abort_flag,
-                                             p.timeout_ns)))
-                        break;
+                    if (!k_next_used) {
+                        if (!(ok = ptx::warp_all(ptx::bar_wait(bar(S::kKFull + kn), ((itj + 1) / S::kKStages) & 1, abort_flag,
+                                                 p.timeout_ns))))
+                            break;
+                        k_next_used = true;
+                    }
                     ptx::tc_fence_after();
-                    issue_qk(t, sn);
-                    ptx::mma_commit(bar(S::kSFull + t));
+                    if (leader) {
+                        issue_qk(t, kn);
+                        ptx::mma_commit(bar(S::kSFull + t));
+                    }
                 }
             }
-            if (ok) ptx::mma_commit(bar(S::kKVEmpty + stage));
+            if (!ok) break;
+            if (leader) {
+                ptx::mma_commit(bar(S::kVEmpty + vs));                 // V tile j: both P V products issued
+                if (k_next_used) ptx::mma_commit(bar(S::kKEmpty + kn));  // K tile j+1: both Q K^T issued
+            }
         }
         if (!ok) break;
-        ptx::mma_commit(bar(S::kQEmpty));
+        if (leader) ptx::mma_commit(bar(S::kQEmpty));
         it += wk.n_kv_max;
         ++wi;
     }
     // Every MMA issued above must finish before TMEM is released.
-    ptx::mma_commit(bar(S::kTeardown));
+    if (leader) ptx::mma_commit(bar(S::kTeardown));
+    __syncwarp();
     ptx::bar_wait(bar(S::kTeardown), 0, nullptr, p.timeout_ns);
 }
 
@@ -325,31 +409,42 @@ __device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, i
             ok = ptx::bar_wait(bar(S::kSFull + t), cnt & 1, abort_flag, p.timeout_ns);
             if (!__all_sync(kFull, ok)) { ok = false; break; }
             ptx::tc_fence_after();
+            // S row in two halves: the second TMEM load overlaps the first half's max.
             uint32_t s[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, s[c]);
+            ptx::tmem_ld32(tS, s[0]);
+            ptx::tmem_ld32(tS + 32, s[1]);
             ptx::tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) ptx::reg_fence(s[c]);
+            ptx::reg_fence(s[0]);
+            ptx::reg_fence(s[1]);
+            ptx::tmem_ld32(tS + 64, s[2]);
+            ptx::tmem_ld32(tS + 96, s[3]);
 
             const int k0 = j * kBlockN;
             const bool need_mask = (k0 + kBlockN > wk.Lk) || (CAUSAL && k0 + kBlockN - 1 > wk.q_start[t]);
-            if (need_mask) {
+            auto mask_half = [&](int h) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
+                for (int c = 64 * h; c < 64 * h + 64; ++c) {
                     const int key = k0 + c;
                     const bool vis = key < wk.Lk && (!CAUSAL || key <= q_row);
                     if (!vis) s[c / 32][c % 32] = 0xff800000u;  // -inf
                 }
-            }
-            // row maximum of the raw scores (8 independent chains)
-            float mx8[8];
+            };
+            // row maximum of the raw scores: four chains of three-input max
+            float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+            auto max_half = [&](int h) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(s[0][i]);
-#pragma unroll
-            for (int c = 8; c < 128; ++c) mx8[c % 8] = fmaxf(mx8[c % 8], __uint_as_float(s[c / 32][c % 32]));
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                for (int c = 64 * h; c < 64 * h + 64; c += 2)
+                    mx4[(c / 2) % 4] = ptx::fmax3(mx4[(c / 2) % 4], __uint_as_float(s[c / 32][c % 32]),
+                                                  __uint_as_float(s[(c + 1) / 32][(c + 1) % 32]));
+            };
+            if (need_mask) mask_half(0);
+            max_half(0);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence(s[2]);
+            ptx::reg_fence(s[3]);
+            if (need_mask) mask_half(1);
+            max_half(1);
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
             const float m_cand = mx * scale_log2;
             const bool need = m_cand > m_used + kRescaleThreshold;
             float alpha = 1.f;
@@ -360,20 +455,34 @@ __device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, i
             l *= alpha;
             const float m_sub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
 
-            // P = 2^(s * scale_log2 - m), packed two per 32-bit TMEM column
-            uint32_t pk[2][32];
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            // P = 2^(s * scale_log2 - m), packed two per 32-bit TMEM column and
+            // stored 32 columns (64 keys) at a time.
+            const uint64_t scale2 = ptx::pk2(scale_log2, scale_log2);
+            const uint64_t negm2 = ptx::pk2(-m_sub, -m_sub);
+            uint64_t sum2[2] = {ptx::pk2(0.f, 0.f), ptx::pk2(0.f, 0.f)};
 #pragma unroll
-            for (int c2 = 0; c2 < 64; ++c2) {
-                const int c = 2 * c2;
-                const float a = ptx::ex2(fmaf(__uint_as_float(s[c / 32][c % 32]), scale_log2, -m_sub));
-                const float b = ptx::ex2(fmaf(__uint_as_float(s[(c + 1) / 32][(c + 1) % 32]), scale_log2, -m_sub));
-                ls[c2 % 4] += a + b;
-                pk[c2 / 32][c2 % 32] = ptx::pack2<BF16>(a, b);
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int c = 64 * h + 2 * i;
+                    const uint64_t x = ptx::ffma2(ptx::pk2(__uint_as_float(s[c / 32][c % 32]),
+                                                           __uint_as_float(s[(c + 1) / 32][(c + 1) % 32])),
+                                                  scale2, negm2);
+                    float x0, x1;
+                    ptx::upk2(x, x0, x1);
+                    const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1);
+                    sum2[i % 2] = ptx::fadd2(sum2[i % 2], ptx::pk2(e0, e1));
+                    pk[i] = ptx::pack2<BF16>(e0, e1);
+                }
+                ptx::tmem_st32(tS + 32 * h, pk);
             }
-            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            ptx::tmem_st32(tS, pk[0]);
-            ptx::tmem_st32(tS + 32, pk[1]);
+            {
+                float a0, a1, b0, b1;
+                ptx::upk2(sum2[0], a0, a1);
+                ptx::upk2(sum2[1], b0, b1);
+                l += (a0 + a1) + (b0 + b1);
+            }
 
             // O *= alpha, once the previous P V has landed (only when a row of
             // this warp moved its maximum)
@@ -394,7 +503,8 @@ __device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, i
             }
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
-            ptx::bar_arrive(bar(S::kPFull + t));
+            __syncwarp();
+            if (lane == 0) ptx::bar_arrive(bar(S::kPFull + t));
             ++cnt;
         }
         if (!ok) break;
@@ -461,7 +571,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint32_t bars = sbase + S::kOffBar;
         for (int i = 0; i < S::kNumBars; ++i) {
             const bool p_full = (i == S::kPFull || i == S::kPFull + 1);
-            ptx::bar_init(bars + 8u * i, p_full ? kBlockM : 1u);
+            ptx::bar_init(bars + 8u * i, p_full ? kBlockM / 32 : 1u);  // one arrival per softmax warp
         }
         *abort_flag = 0;
         ptx::bar_init_fence();
@@ -480,11 +590,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        if (lane == 0) fwd_producer<D, CAUSAL, VARLEN>(&tm_q, &tm_k, &tm_v, p, sbase, abort_flag);
-    } else if (warp == 1) {
-        if (lane == 0) fwd_mma<D, BF16, CAUSAL, VARLEN>(p, sbase, tmem, abort_flag);
-    } else if (warp >= 4) {
+    if (warp < 4) {
+        // Whole warps run the producer and MMA loops (uniform control flow and
+        // operands); the TMA, MMA and commit instructions come from one elected lane.
+        if (warp == 0) {
+            fwd_producer_qk<D, CAUSAL, VARLEN>(&tm_q, &tm_k, p, sbase, abort_flag);
+        } else if (warp == 1) {
+            fwd_mma<D, BF16, CAUSAL, VARLEN>(p, sbase, tmem, abort_flag);
+        } else if (warp == 2) {
+            fwd_producer_v<D, CAUSAL, VARLEN>(&tm_v, p, sbase, abort_flag);
+        }
+    } else {
         fwd_softmax<D, BF16, CAUSAL, VARLEN>(p, sbase, tmem, (warp - 4) / 4, warp % 4, lane, abort_flag);
     }
 

@@ -24,6 +24,19 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
+// One lane of a converged warp (the lowest active one) gets true. Used to issue
+// single-thread instructions (TMA, MMA, commit) from a loop the whole warp
+// runs, which keeps loop state and descriptors in the uniform datapath.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ---------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
@@ -78,6 +91,9 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile
     }
 }
 
+// True on every lane iff it is true on every lane of the (converged) warp.
+__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
+
 // --------------------------------------------------------------------- TMA --
 
 // 3-D tiled tensor load into shared memory; completion is signalled on `bar`
@@ -89,6 +105,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+
+// Ask L2 to fetch a tile ahead of its use (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
@@ -239,20 +263,34 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool b
            | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
-// Re-balance the register file between warpgroups; every warp of the
-// warpgroup must execute the same instruction. The sum over warpgroups must
-// stay within what the block was launched with.
-template <int N>
-__device__ __forceinline__ void regs_dec() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void regs_inc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // ------------------------------------------------------------------- math --
 
+// Packed fp32 pairs (Blackwell f32x2 instructions): one instruction, two lanes.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// 2^x on MUFU (ex2.approx.ftz: relative error ~2^-22, subnormal results flush to 0).
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

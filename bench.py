@@ -394,6 +394,7 @@ def run_gpu(args, rank, world, local):
         return None
     prefill_tflops = world * pf_flops * K / (pf_sum * 1e-3) / 1e12
     decode_gbs = world * dc_bytes * K / (dc_sum * 1e-3) / 1e9
+    paged = run_paged(args, fa, torch, stream, dev, flush, world)
     # end-to-end through host buffers (pinned), copies inside the timed region
     e2e = ({"prefill": None, "decode": None} if args.no_e2e else
            run_e2e(args, fa, torch, stream, dev, wp, wd, (q, k, v), (dq, dk, dv), world))
@@ -428,11 +429,52 @@ def run_gpu(args, rank, world, local):
             "e2e": e2e["decode"],
         },
         "e2e": e2e["prefill"],
+        "paged_decode": paged,
         "gpu_launches": 3 * K,
         "clocks": clock,
         "wall_ms_per_step": 1e3 * wall / K,
     }
     return line
+
+
+def run_paged(args, fa, torch, stream, dev, flush, world):
+    """Split-KV decode over a paged cache (16-key pages, permuted block table),
+    same shapes and bytes as the decode workload; timed on its own loop with
+    the same L2 flush and CUDA events (split + merge)."""
+    from exact_attention_54_gb300 import inputs
+    from exact_attention_54_gb300.metrics import decode_bytes
+    w = inputs.WORKLOADS["paged_decode"]
+    q, kc, vc, bt, sl = (t.to(dev) for t in inputs.make_workload(w))
+    S = w.num_splits
+    ws = (torch.empty(w.B, w.H, S, w.D, dtype=torch.float32, device=dev),
+          torch.empty(w.B, w.H, S, dtype=torch.float32, device=dev),
+          torch.empty(w.B, w.H, S, dtype=torch.float32, device=dev))
+    o = torch.empty(w.B, w.H, 1, w.D, dtype=w.dtype, device=dev)
+    lse = torch.empty(w.B, w.H, dtype=torch.float32, device=dev)
+    n = max(1, min(args.steps, 500))
+
+    def step(evs=None):
+        flush.fill_(float(1.0))
+        if evs:
+            evs[0].record(stream)
+        fa.fa_decode_paged_splitkv(q, kc, vc, bt, sl, *ws, S, w.scale, stream)
+        fa.fa_splitkv_merge(*ws, o, lse, stream)
+        if evs:
+            evs[1].record(stream)
+
+    for _ in range(3):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        step(evs[i])
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    ms = aggregate_max([sum(e[0].elapsed_time(e[1]) for e in evs) / n], world)[0]
+    nbytes = decode_bytes(w.B, w.H, w.Sk, w.D)
+    peaks, src = load_peaks()
+    gbs = world * nbytes / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "value": gbs, "unit": "GB/s", "ms_per_step": ms, "steps": n,
+            "frac_of_hbm": gbs / peaks["hbm_gbs"], "block_size": w.extra["block_size"]}
 
 
 def run_e2e(args, fa, torch, stream, dev, wp, wd, pre, dec, world):

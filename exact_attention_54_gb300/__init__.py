@@ -20,9 +20,9 @@ import threading
 
 import torch
 
-__all__ = ["FAError", "fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_splitkv_merge",
+__all__ = ["FAError", "fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_decode_paged_splitkv", "fa_splitkv_merge",
            "fa_check_device_error", "fa_status_string", "flash_attention", "flash_attention_varlen",
-           "flash_decode", "library_path", "load_library", "EXPORTED_SYMBOLS"]
+           "flash_decode", "flash_decode_paged", "library_path", "load_library", "EXPORTED_SYMBOLS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libfa.so")
@@ -31,7 +31,7 @@ _lib = None
 
 FA_FP16, FA_BF16 = 0, 1
 FA_MAX_SPLITS = 1024
-EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_splitkv_merge",
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_decode_paged_splitkv", "fa_splitkv_merge",
                     "fa_check_device_error", "fa_status_string", "fa_version")
 
 
@@ -149,6 +149,28 @@ def fa_decode_splitkv(q, k, v, o_part, m_part, l_part, num_splits: int, scale: f
     _check("fa_decode_splitkv", st)
 
 
+def fa_decode_paged_splitkv(q, k_cache, v_cache, block_table, seq_lens, o_part, m_part, l_part, num_splits: int,
+                            scale: float | None = None, stream=None):
+    """Phase 1 over a paged cache: q [B,H,1,D]; k_cache, v_cache
+    [num_blocks,H,block_size,D]; block_table [B,max_blocks] and seq_lens [B]
+    int32 CUDA tensors; partials as in fa_decode_splitkv."""
+    B, H = q.shape[0], q.shape[1]
+    num_blocks, _, block_size, D = k_cache.shape
+    _need_contig(q, k_cache, v_cache, block_table, seq_lens, o_part, m_part, l_part)
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    lib = load_library()
+    fn = lib.fa_decode_paged_splitkv
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
+    fn.restype = ctypes.c_int
+    _check("fa_decode_paged_splitkv",
+           fn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(o_part), _ptr(m_part),
+              _ptr(l_part), B, H, D, num_blocks, block_size, block_table.shape[1], int(num_splits), float(scale),
+              _dtype_code(q), _stream(stream)))
+
+
 def fa_splitkv_merge(o_part, m_part, l_part, o, lse, stream=None):
     """Phase 2: partials from phase 1 -> o [B,H,1,D] (16-bit), lse [B,H] fp32."""
     B, H, S, D = o_part.shape
@@ -181,6 +203,25 @@ def flash_attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: in
     o = torch.empty_like(q)
     lse = torch.empty(H, Tq, dtype=torch.float32, device=q.device)
     fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, causal, scale, stream)
+    return o, lse
+
+
+def flash_decode_paged(q, k_cache, v_cache, block_table, seq_lens, num_splits: int, scale: float | None = None,
+                       stream=None, workspace=None):
+    """Split-KV decoding over a paged cache (phase 1 + phase 2). Returns
+    (o [B,H,1,D], lse [B,H])."""
+    B, H = q.shape[0], q.shape[1]
+    D = k_cache.shape[3]
+    if workspace is None:
+        workspace = (torch.empty(B, H, num_splits, D, dtype=torch.float32, device=q.device),
+                     torch.empty(B, H, num_splits, dtype=torch.float32, device=q.device),
+                     torch.empty(B, H, num_splits, dtype=torch.float32, device=q.device))
+    o_part, m_part, l_part = workspace
+    o = torch.empty(B, H, 1, D, dtype=q.dtype, device=q.device)
+    lse = torch.empty(B, H, dtype=torch.float32, device=q.device)
+    fa_decode_paged_splitkv(q, k_cache, v_cache, block_table, seq_lens, o_part, m_part, l_part, num_splits, scale,
+                            stream)
+    fa_splitkv_merge(o_part, m_part, l_part, o, lse, stream)
     return o, lse
 
 

@@ -55,12 +55,15 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
 }
 
 // grid: one CTA per (head, partition), x = bh * num_splits + s.
-template <int D, bool BF16>
+// PAGED: K and V live in pages [num_blocks, H, block_size, D]; key position p
+// of sequence b is row p % block_size of page block_table[b][p / block_size],
+// and the sequence holds seq_lens[b] keys ("Adaptive High-Performance
+// Attention Kernels in CUDA", Advanced Production Features 4). A page index
+// outside [0, num_blocks) is never dereferenced: its keys are skipped and the
+// device error word records kDeviceErrBadIndex.
+template <int D, bool BF16, bool PAGED>
 __global__ void __launch_bounds__(kDecodeThreads)
-    fa_decode_split_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
-                           const uint16_t *__restrict__ v, float *__restrict__ o_part,
-                           float *__restrict__ m_part, float *__restrict__ l_part, int Sk, int num_splits,
-                           int keys_per_split, float scale_log2) {
+    fa_decode_split_kernel(const DecodeParams p) {
     constexpr int kLanesPerKey = D / 8;                  // 16-byte pieces per key row
     constexpr int kKeysPerWarp = 32 / kLanesPerKey;      // key rows one warp load covers
     constexpr int kWarps = kDecodeThreads / 32;
@@ -71,38 +74,72 @@ __global__ void __launch_bounds__(kDecodeThreads)
     __shared__ float sm_l[kGroups];
     __shared__ __align__(16) float sm_acc[kGroups][D];
 
+    const int num_splits = p.num_splits;
     const int bh = blockIdx.x / num_splits;
     const int s = blockIdx.x % num_splits;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int sub = lane % kLanesPerKey;                  // which 8 elements of the row
     const int gw = lane / kLanesPerKey;                   // lane group within the warp
     const int g = warp * kKeysPerWarp + gw;
-    const int k_lo = s * keys_per_split;
-    const int k_hi = min(k_lo + keys_per_split, Sk);
+    int seq_len, part;
+    if constexpr (PAGED) {
+        const int cap = p.max_blocks << p.log2_bs;
+        seq_len = p.seq_lens[bh / p.H];
+        seq_len = seq_len < 0 ? 0 : (seq_len > cap ? cap : seq_len);
+        part = (seq_len + num_splits - 1) / num_splits;
+    } else {
+        seq_len = p.Sk;
+        part = p.keys_per_split;
+    }
+    const int k_lo = s * part;
+    const int k_hi = min(k_lo + part, seq_len);
 
     float qf[8];
-    unpack8<BF16>(*reinterpret_cast<const uint4 *>(q + static_cast<size_t>(bh) * D + sub * 8), qf);
+    unpack8<BF16>(*reinterpret_cast<const uint4 *>(p.q + static_cast<size_t>(bh) * D + sub * 8), qf);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) qf[e] *= scale_log2;  // scores in base-2 units
+    for (int e = 0; e < 8; ++e) qf[e] *= p.scale_log2;  // scores in base-2 units
 
-    const uint16_t *kb = k + static_cast<size_t>(bh) * Sk * D + sub * 8;
-    const uint16_t *vb = v + static_cast<size_t>(bh) * Sk * D + sub * 8;
+    // address of row `key` of this head (dense), or nullptr offset semantics for a bad page (paged)
+    const int b = bh / p.H, h = bh % p.H;
+    const int *bt = PAGED ? p.block_table + static_cast<size_t>(b) * p.max_blocks : nullptr;
+    auto row_offset = [&](int key, bool &ok) -> size_t {
+        if constexpr (PAGED) {
+            const int blk = bt[key >> p.log2_bs];
+            ok = static_cast<unsigned>(blk) < static_cast<unsigned>(p.num_blocks);
+            const int blk_safe = ok ? blk : 0;
+            return ((static_cast<size_t>(blk_safe) * p.H + h) << p.log2_bs | (key & ((1 << p.log2_bs) - 1))) * D;
+        } else {
+            ok = true;
+            return (static_cast<size_t>(bh) * p.Sk + key) * D;
+        }
+    };
+    const uint16_t *kb = p.k + sub * 8;
+    const uint16_t *vb = p.v + sub * 8;
     float m = -CUDART_INF_F, l = 0.f;
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    bool bad_page = false;
 
     // The trip count depends on the warp only (never on the lane group), so every
     // lane reaches every shuffle below; keys past k_hi are predicated off.
     for (int base = k_lo + warp * kKeysPerWarp; base < k_hi; base += kGroups * U) {
         const int key0 = base + gw;
         uint4 kr[U], vr[U];
+        bool valid[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int key = key0 + u * kGroups;
+            bool ok = false;
+            size_t off = 0;
             if (key < k_hi) {
-                kr[u] = ldg_stream(kb + static_cast<size_t>(key) * D);
-                vr[u] = ldg_stream(vb + static_cast<size_t>(key) * D);
+                off = row_offset(key, ok);
+                bad_page |= !ok;
+            }
+            valid[u] = ok;
+            if (ok) {
+                kr[u] = ldg_stream(kb + off);
+                vr[u] = ldg_stream(vb + off);
             } else {
                 kr[u] = make_uint4(0, 0, 0, 0);
                 vr[u] = make_uint4(0, 0, 0, 0);
@@ -119,7 +156,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
             // butterfly over the lanes of one key row: every lane ends with the same bits
 #pragma unroll
             for (int off = kLanesPerKey / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-            sc[u] = (key0 + u * kGroups < k_hi) ? d : -CUDART_INF_F;
+            sc[u] = valid[u] ? d : -CUDART_INF_F;
         }
         float mx = sc[0];
 #pragma unroll
@@ -141,6 +178,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
         }
         m = m_new;
     }
+    if (PAGED && bad_page) atomicExch(p.err, kDeviceErrBadIndex);
 
     // merge the lane groups of this CTA (same log-sum-exp rule as phase 2)
     if (sub == 0) {
@@ -164,10 +202,10 @@ __global__ void __launch_bounds__(kDecodeThreads)
             }
         }
         const size_t ps = static_cast<size_t>(bh) * num_splits + s;
-        o_part[ps * D + d] = O;
+        p.o_part[ps * D + d] = O;
         if (d == 0) {
-            m_part[ps] = (M == -CUDART_INF_F) ? -CUDART_INF_F : M * 0.69314718055994531f;
-            l_part[ps] = L;
+            p.m_part[ps] = (M == -CUDART_INF_F) ? -CUDART_INF_F : M * 0.69314718055994531f;
+            p.l_part[ps] = L;
         }
     }
 }
@@ -255,14 +293,20 @@ __global__ void __launch_bounds__(kMergeThreads)
     }
 }
 
-template <int D, bool BF16>
-static cudaError_t launch_split_t(const void *q, const void *k, const void *v, float *op, float *mp, float *lp,
-                                  int BH, int Sk, int S, int P, float scale_log2, cudaStream_t st) {
-    const long long grid = static_cast<long long>(BH) * S;
-    fa_decode_split_kernel<D, BF16><<<static_cast<unsigned>(grid), kDecodeThreads, 0, st>>>(
-        static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(v), op,
-        mp, lp, Sk, S, P, scale_log2);
+template <int D, bool BF16, bool PAGED>
+static cudaError_t launch_split_t(const DecodeParams &p, int BH, cudaStream_t st) {
+    const long long grid = static_cast<long long>(BH) * p.num_splits;
+    fa_decode_split_kernel<D, BF16, PAGED><<<static_cast<unsigned>(grid), kDecodeThreads, 0, st>>>(p);
     return cudaGetLastError();
+}
+
+template <bool PAGED>
+static cudaError_t launch_split_any(int D, bool bf16, const DecodeParams &p, int BH, cudaStream_t st) {
+    if (D == 64 && !bf16) return launch_split_t<64, false, PAGED>(p, BH, st);
+    if (D == 64 && bf16) return launch_split_t<64, true, PAGED>(p, BH, st);
+    if (D == 128 && !bf16) return launch_split_t<128, false, PAGED>(p, BH, st);
+    if (D == 128 && bf16) return launch_split_t<128, true, PAGED>(p, BH, st);
+    return cudaErrorInvalidValue;
 }
 
 template <int D, bool BF16>
@@ -275,11 +319,23 @@ static cudaError_t launch_merge_t(const float *op, const float *mp, const float 
 cudaError_t launch_decode_split(int D, bool bf16, const void *q, const void *k, const void *v, float *o_part,
                                 float *m_part, float *l_part, int BH, int Sk, int num_splits, int keys_per_split,
                                 float scale_log2, cudaStream_t stream) {
-    if (D == 64 && !bf16) return launch_split_t<64, false>(q, k, v, o_part, m_part, l_part, BH, Sk, num_splits, keys_per_split, scale_log2, stream);
-    if (D == 64 && bf16) return launch_split_t<64, true>(q, k, v, o_part, m_part, l_part, BH, Sk, num_splits, keys_per_split, scale_log2, stream);
-    if (D == 128 && !bf16) return launch_split_t<128, false>(q, k, v, o_part, m_part, l_part, BH, Sk, num_splits, keys_per_split, scale_log2, stream);
-    if (D == 128 && bf16) return launch_split_t<128, true>(q, k, v, o_part, m_part, l_part, BH, Sk, num_splits, keys_per_split, scale_log2, stream);
-    return cudaErrorInvalidValue;
+    DecodeParams p{};
+    p.q = static_cast<const uint16_t *>(q);
+    p.k = static_cast<const uint16_t *>(k);
+    p.v = static_cast<const uint16_t *>(v);
+    p.o_part = o_part;
+    p.m_part = m_part;
+    p.l_part = l_part;
+    p.H = 1;
+    p.Sk = Sk;
+    p.num_splits = num_splits;
+    p.keys_per_split = keys_per_split;
+    p.scale_log2 = scale_log2;
+    return launch_split_any<false>(D, bf16, p, BH, stream);
+}
+
+cudaError_t launch_decode_split_paged(int D, bool bf16, const DecodeParams &p, int BH, cudaStream_t stream) {
+    return launch_split_any<true>(D, bf16, p, BH, stream);
 }
 
 cudaError_t launch_splitkv_merge(int D, bool bf16, const float *o_part, const float *m_part, const float *l_part,

@@ -8,8 +8,10 @@
 
 namespace fa {
 
-// Value written to the device error word when a kernel abandons a wait.
+// Values written to the device error word: a kernel abandoned a wait, or met
+// an out-of-range device-side index (a page number in a block table).
 constexpr int kDeviceErrTimeout = 1;
+constexpr int kDeviceErrBadIndex = 2;
 
 // Default bound on any single wait on an on-chip barrier.
 constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;  // 1 s
@@ -34,6 +36,23 @@ struct FwdParams {
 
 int fwd_smem_bytes(int D);
 
+// Parameters of the split-KV decode kernel (dense and paged K/V).
+struct DecodeParams {
+    const uint16_t *q, *k, *v;   // q [B*H, D]; k, v dense [B*H, Sk, D] or pages [num_blocks, H, bs, D]
+    float *o_part, *m_part, *l_part;
+    int H;                       // heads (paged: to locate the head inside a page)
+    int Sk;                      // dense: keys per head
+    int num_splits;
+    int keys_per_split;          // dense: ceil(Sk / num_splits)
+    float scale_log2;
+    const int *block_table;      // paged: [B, max_blocks] page numbers
+    const int *seq_lens;         // paged: [B] keys per sequence
+    int max_blocks;              // paged: row length of block_table
+    int log2_bs;                 // paged: log2(block_size)
+    int num_blocks;              // paged: pages in the cache
+    int *err;                    // paged: device error word
+};
+
 // maps: {Q, K, V} tensor maps (see fa_api.cu for their geometry).
 cudaError_t launch_fwd_dense(int D, bool bf16, bool causal, const CUtensorMap *maps,
                              const FwdParams &p, int grid, cudaStream_t stream);
@@ -44,6 +63,8 @@ cudaError_t launch_decode_split(int D, bool bf16, const void *q, const void *k, 
                                 float *o_part, float *m_part, float *l_part, int BH, int Sk,
                                 int num_splits, int keys_per_split, float scale_log2,
                                 cudaStream_t stream);
+
+cudaError_t launch_decode_split_paged(int D, bool bf16, const DecodeParams &p, int BH, cudaStream_t stream);
 
 cudaError_t launch_splitkv_merge(int D, bool bf16, const float *o_part, const float *m_part,
                                  const float *l_part, void *o, float *lse, int BH,

@@ -11,6 +11,7 @@ Workloads (shapes from the pages' own benchmark tables; none is a dataset):
   llama_prefill B=1 H=32 Sq=Sk=4096 D=128 bf16, causal     ("FlashAttention-2 MMA", LLaMA-7B Prefill row)
   decode      B=16 H=8  Sq=1 Sk=8192 D=128 bf16, 32 KV partitions ("FlashAttention-2 MMA", Decode KV row, batched)
   varlen      16 sequences, lengths uniform on [64, 2048], H=16 D=128 bf16, causal
+  paged_decode the decode workload with K/V in 16-key pages behind a permuted block table
 """
 from __future__ import annotations
 
@@ -53,6 +54,8 @@ WORKLOADS = {
                        False, 1004, num_splits=32),
     "varlen": Workload("varlen_16seq_len64to2048_h16d128_bf16_causal", "varlen", 0, 16, 0, 0, 128,
                        torch.bfloat16, True, 1005, num_seqs=16, len_lo=64, len_hi=2048),
+    "paged_decode": Workload("paged_decode_b16h8sk8192d128_bf16_block16_split32", "paged", 16, 8, 1, 8192, 128,
+                             torch.bfloat16, False, 1006, num_splits=32, extra={"block_size": 16}),
 }
 
 
@@ -99,6 +102,31 @@ def make_varlen(num_seqs: int, lo: int, hi: int, H: int, D: int, dtype: torch.dt
     return lengths, cu, q, k, v
 
 
+def make_paged(B: int, H: int, D: int, block_size: int, seq_lens, dtype: torch.dtype, seed: int,
+               spare_blocks: int = 3):
+    """Paged KV cache: pages [num_blocks, H, block_size, D] filled with N(0,1)
+    (spare pages included), each sequence's logical blocks mapped to pages by a
+    seeded permutation. Table entries past a sequence's blocks hold an
+    out-of-range page number (they must never be read).
+    Returns q [B,H,1,D], k_cache, v_cache, block_table [B, max_blocks] int32,
+    seq_lens [B] int32."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    lens = [int(x) for x in seq_lens]
+    per = [-(-L // block_size) for L in lens]
+    max_blocks = max(max(per), 1)
+    num_blocks = sum(per) + spare_blocks
+    perm = torch.randperm(num_blocks, generator=g)
+    q = randn((B, H, 1, D), dtype, g)
+    k_cache = randn((num_blocks, H, block_size, D), dtype, g)
+    v_cache = randn((num_blocks, H, block_size, D), dtype, g)
+    table = torch.full((B, max_blocks), num_blocks + 1000, dtype=torch.int32)
+    pos = 0
+    for b, n in enumerate(per):
+        table[b, :n] = perm[pos:pos + n].to(torch.int32)
+        pos += n
+    return q, k_cache, v_cache, table, torch.tensor(lens, dtype=torch.int32)
+
+
 def make_workload(w: Workload):
     """Inputs for a named workload (CPU tensors)."""
     if w.kind == "dense":
@@ -107,5 +135,7 @@ def make_workload(w: Workload):
         return make_dense(w.B, w.H, 1, w.Sk, w.D, w.dtype, w.seed)
     if w.kind == "varlen":
         return make_varlen(w.num_seqs, w.len_lo, w.len_hi, w.H, w.D, w.dtype, w.seed)
+    if w.kind == "paged":
+        return make_paged(w.B, w.H, w.D, w.extra["block_size"], [w.Sk] * w.B, w.dtype, w.seed)
     raise ValueError(w.kind)
 

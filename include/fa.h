@@ -54,7 +54,8 @@ typedef enum {
     FA_ERR_SCALE = -7,          /* scale is not finite and > 0 */
     FA_ERR_CUDA = -8,           /* the CUDA runtime reported an error (launch, tensor map) */
     FA_ERR_DEVICE_TIMEOUT = -9, /* a kernel gave up waiting on an on-chip barrier */
-    FA_ERR_SCRATCH = -10        /* fa_decode_noalloc: problem larger than its built-in scratch */
+    FA_ERR_SCRATCH = -10,       /* fa_decode_noalloc: problem larger than its built-in scratch */
+    FA_ERR_DEVICE_INDEX = -11   /* a kernel met an out-of-range block-table entry */
 } fa_status_t;
 
 typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype_t;
@@ -130,6 +131,37 @@ FA_API fa_status_t fa_decode_splitkv(const void *q, const void *k, const void *v
                               int num_splits, float scale, fa_dtype_t dtype, void *stream);
 
 /*
+ * fa_decode_paged_splitkv - split-KV decoding, phase 1, over a paged KV cache.
+ *
+ * Defined by "Adaptive High-Performance Attention Kernels in CUDA" (Advanced
+ * Production Features 4: the KV cache is kept as physical pages
+ * [num_blocks, H, block_size, d] and a per-sequence block table translates a
+ * logical key position into a page) combined with the split-KV phase 1 above.
+ *
+ *   q            [B,H,1,D] fp16/bf16
+ *   k_cache, v_cache [num_blocks,H,block_size,D], same dtype
+ *   block_table  device int32 [B, max_blocks_per_seq]: page of each logical
+ *                block; entries past a sequence's length are never read
+ *   seq_lens     device int32 [B]: keys of each sequence (clamped to
+ *                [0, max_blocks_per_seq * block_size])
+ *   o_part [B,H,S,D], m_part and l_part [B,H,S] fp32 outputs, as in
+ *                fa_decode_splitkv, with partition size ceil(seq_lens[b]/S)
+ *                per sequence (a length-0 sequence has only empty partitions).
+ *   block_size   a power of two, 1..1024.
+ * Page numbers outside [0, num_blocks) are never dereferenced: their keys are
+ * skipped and fa_check_device_error later returns FA_ERR_DEVICE_INDEX.
+ * Phase 2 is fa_splitkv_merge, unchanged.
+ * Errors: FA_ERR_NULL, FA_ERR_SHAPE, FA_ERR_HEADDIM, FA_ERR_DTYPE,
+ * FA_ERR_ALIGN, FA_ERR_SPLITS, FA_ERR_SCALE, FA_ERR_CUDA.
+ */
+FA_API fa_status_t fa_decode_paged_splitkv(const void *q, const void *k_cache, const void *v_cache,
+                                           const int32_t *block_table, const int32_t *seq_lens,
+                                           float *o_part, float *m_part, float *l_part, int B, int H,
+                                           int D, int num_blocks, int block_size,
+                                           int max_blocks_per_seq, int num_splits, float scale,
+                                           fa_dtype_t dtype, void *stream);
+
+/*
  * fa_splitkv_merge - split-KV decoding, phase 2 (log-sum-exp reduction).
  *
  * Defined by "Adaptive High-Performance Attention Kernels in CUDA" (Advanced
@@ -149,8 +181,9 @@ FA_API fa_status_t fa_splitkv_merge(const float *o_part, const float *m_part, co
  * fa_check_device_error - synchronise `stream`, then read and clear the
  * current device's error word. Kernels bound every wait on an on-chip barrier;
  * a wait that runs out sets the word, releases what the CTA holds and returns.
- * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT, or FA_ERR_CUDA when the runtime
- * itself reports an error.
+ * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT, FA_ERR_DEVICE_INDEX (an out-of-range
+ * block-table entry was skipped), or FA_ERR_CUDA when the runtime itself
+ * reports an error.
  */
 FA_API fa_status_t fa_check_device_error(void *stream);
 

@@ -192,6 +192,40 @@ class Oracle:
                 raise ValueError(f"oracle_splitkv_merge failed ({rc})")
         return o.reshape(*lead, D), lse.reshape(*lead)
 
+    def paged_gather(self, cache, block_table, seq_lens):
+        """Contiguous keys (or values) of every sequence from a paged cache
+        ("Adaptive High-Performance Attention Kernels in CUDA", Advanced
+        Production Features 4: physical pages [num_blocks, H, block_size, d],
+        logical position p of sequence b lives in page block_table[b][p //
+        block_size] at offset p % block_size). Returns a list of [H, L_b, d]
+        float64 arrays."""
+        cache = _f64(cache)
+        bt = np.asarray(block_table).astype(np.int64)
+        lens = [int(x) for x in np.asarray(seq_lens).tolist()]
+        bs = cache.shape[2]
+        out = []
+        for b, L in enumerate(lens):
+            pages = [cache[bt[b, p // bs], :, p % bs, :] for p in range(L)]  # each [H, d]
+            out.append(np.stack(pages, axis=1) if pages else np.zeros((cache.shape[1], 0, cache.shape[3])))
+        return out
+
+    def decode_paged(self, q, k_cache, v_cache, block_table, seq_lens, scale: float):
+        """Single-query attention per (sequence, head) over the keys a block
+        table maps into a paged cache: gather, then exact attention. q is
+        [B, H, 1, d]; returns o [B, H, 1, d] and lse [B, H, 1] (a sequence of
+        length 0 gives o = 0 and lse = -inf)."""
+        q = _f64(q)
+        ks = self.paged_gather(k_cache, block_table, seq_lens)
+        vs = self.paged_gather(v_cache, block_table, seq_lens)
+        B, H, _, D = q.shape
+        o = np.zeros((B, H, 1, D))
+        lse = np.full((B, H, 1), -np.inf)
+        for b in range(B):
+            if ks[b].shape[1] == 0:
+                continue
+            o[b], lse[b] = self.attention(q[b], ks[b], vs[b], False, scale)
+        return o, lse
+
     def decode(self, q, k, v, scale: float, nthreads: int | None = None):
         """Single-query attention (Sq = 1) computed without splitting: the
         result the split/merge pair must reproduce."""
@@ -225,3 +259,7 @@ def splitkv_merge(*a, **kw):
 
 def decode(*a, **kw):
     return get().decode(*a, **kw)
+
+
+def decode_paged(*a, **kw):
+    return get().decode_paged(*a, **kw)

@@ -222,6 +222,50 @@ def pin_varlen_block_diag(orc):
         _close(lse, torch.logsumexp(s, -1).numpy(), what=f"varlen LSE causal={causal}")
 
 
+def pin_paged_gather(orc):
+    """A paged cache built by scattering dense K/V into randomly permuted pages
+    (and sharing one prefix page between two sequences) gives exactly the
+    dense single-query attention of each sequence; a length-0 sequence gives
+    O = 0, LSE = -inf."""
+    H, D, bs = 2, 8, 4
+    lens = [9, 4, 0, 13]
+    g = torch.Generator().manual_seed(121)
+    nblk = sum(-(-L // bs) for L in lens) + 3
+    perm = torch.randperm(nblk, generator=g).tolist()
+    kc = torch.zeros(nblk, H, bs, D, dtype=torch.float64)
+    vc = torch.zeros(nblk, H, bs, D, dtype=torch.float64)
+    maxb = max(-(-L // bs) for L in lens)
+    bt = torch.zeros(len(lens), maxb, dtype=torch.int32)
+    q = _rand((len(lens), H, 1, D), 122)
+    dense = []
+    nxt = 0
+    for b, L in enumerate(lens):
+        k, v = _rand((H, L, D), 123 + b), _rand((H, L, D), 223 + b)
+        if b == 3:  # share sequence 0's first page (same key/value content)
+            k[:, :bs], v[:, :bs] = dense[0][0][:, :bs], dense[0][1][:, :bs]
+        dense.append((k, v))
+        for i in range(-(-L // bs)):
+            if b == 3 and i == 0:
+                bt[b, i] = bt[0, 0]
+                continue
+            page = perm[nxt]
+            nxt += 1
+            bt[b, i] = page
+            n = min(bs, L - i * bs)
+            kc[page, :, :n] = k[:, i * bs:i * bs + n]
+            vc[page, :, :n] = v[:, i * bs:i * bs + n]
+    o, lse = orc.decode_paged(q, kc, vc, bt, torch.tensor(lens, dtype=torch.int32), 0.35)
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert np.all(o[b] == 0) and np.all(lse[b] == -np.inf)
+            continue
+        k, v = dense[b]
+        ref = F.scaled_dot_product_attention(q[b], k, v, scale=0.35)
+        _close(o[b], ref.numpy(), what=f"paged O seq {b}")
+        _close(lse[b, :, 0], torch.logsumexp(0.35 * (q[b] @ k.transpose(-1, -2))[:, 0], -1).numpy(),
+               what=f"paged LSE seq {b}")
+
+
 PINS = [pin_sdpa, pin_rows_sum_to_one, pin_single_key, pin_equal_scores, pin_causal_row0,
         pin_two_keys, pin_shift, pin_permutation, pin_rows_subset, pin_partials_definition,
-        pin_merge_identity, pin_varlen_block_diag]
+        pin_merge_identity, pin_varlen_block_diag, pin_paged_gather]

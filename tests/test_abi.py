@@ -46,7 +46,7 @@ def test_only_the_abi_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    for code in range(-9, 1):
+    for code in range(-11, 1):
         s = fa.fa_status_string(code)
         assert s and s != "unknown status"
     assert fa.fa_status_string(-1234) == "unknown status"
@@ -109,6 +109,28 @@ def test_decode_validation(lib):
     assert _split(lib, scale=0.0) == SCALE
     assert _split(lib, v=MIS) == ALIGN
     assert _split(lib, mp=A + 2) == ALIGN
+
+
+def _paged(lib, q=A, kc=A, vc=A, bt=A, sl=A, op=A, mp=A, lp=A, B=2, H=2, D=128, nb=64, bs=16, mb=8, S=4,
+           scale=0.1, dtype=1):
+    return lib.fa_decode_paged_splitkv(q, kc, vc, bt, sl, op, mp, lp, B, H, D, nb, bs, mb, S, scale, dtype, None)
+
+
+def test_paged_validation(lib):
+    import ctypes as C
+    vp, i, f = C.c_void_p, C.c_int, C.c_float
+    lib.fa_decode_paged_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
+    assert _paged(lib, bt=None) == NULL
+    assert _paged(lib, sl=None) == NULL
+    assert _paged(lib, dtype=3) == DTYPE
+    assert _paged(lib, D=32) == HEADDIM
+    for kw in ({"B": 0}, {"H": 0}, {"nb": 0}, {"mb": 0}, {"bs": 0}, {"bs": 24}, {"bs": 2048}):
+        assert _paged(lib, **kw) == SHAPE, kw
+    assert _paged(lib, S=0) == SPLITS
+    assert _paged(lib, S=1025) == SPLITS
+    assert _paged(lib, scale=float("nan")) == SCALE
+    assert _paged(lib, kc=MIS) == ALIGN
+    assert _paged(lib, bt=A + 2) == ALIGN
 
 
 def test_merge_validation(lib):

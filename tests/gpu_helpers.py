@@ -20,10 +20,11 @@ def max_abs_err(actual, expected):
     assert a.shape == e.shape, (a.shape, e.shape)
     if a.size == 0:
         return 0.0, None
-    if not np.all(np.isfinite(a)):
-        bad = np.argwhere(~np.isfinite(a))[0]
-        return float("inf"), tuple(int(x) for x in bad)
-    d = np.abs(a - e)
+    same = a == e  # includes equal infinities (e.g. LSE = -inf of an empty sequence)
+    bad = ~same & ~(np.isfinite(a) & np.isfinite(e))
+    if np.any(bad):
+        return float("inf"), tuple(int(x) for x in np.argwhere(bad)[0])
+    d = np.where(same, 0.0, np.abs(a - e))
     idx = np.unravel_index(int(np.argmax(d)), d.shape)
     return float(d[idx]), tuple(int(x) for x in idx)
 

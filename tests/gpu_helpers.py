@@ -24,7 +24,8 @@ def max_abs_err(actual, expected):
     bad = ~same & ~(np.isfinite(a) & np.isfinite(e))
     if np.any(bad):
         return float("inf"), tuple(int(x) for x in np.argwhere(bad)[0])
-    d = np.where(same, 0.0, np.abs(a - e))
+    with np.errstate(invalid="ignore"):
+        d = np.where(same, 0.0, np.abs(a - e))
     idx = np.unravel_index(int(np.argmax(d)), d.shape)
     return float(d[idx]), tuple(int(x) for x in idx)
 

@@ -344,7 +344,8 @@ __device__ void fwd_mma(const FwdParams &p, uint32_t sbase, uint32_t tmem, volat
                 ptx::tc_fence_after();
                 if (leader) {
                     issue_pv(t, vs, j > 0);
-                    ptx::mma_commit(bar(S::kODone + t));
+                    // the epilogue needs the last product; earlier ones are covered by S_FULL
+                    if (j + 1 == wk.n_kv[t]) ptx::mma_commit(bar(S::kODone + t));
                 }
                 ++cnt[t];
                 if (j + 1 < wk.n_kv[t]) {
@@ -391,7 +392,8 @@ __device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, i
     const uint32_t tO = tmem + lane_base + S::kTmemO + t * D;
     const float scale_log2 = p.scale_log2;
     constexpr unsigned kFull = 0xffffffffu;
-    uint32_t cnt = 0;  // S tiles consumed by this warpgroup
+    uint32_t cnt = 0;    // S tiles consumed by this warpgroup
+    uint32_t items = 0;  // work items finished by this warpgroup
     bool ok = true;
 
     for (int r = 0; ok; ++r) {
@@ -484,12 +486,10 @@ __device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, i
                 l += (a0 + a1) + (b0 + b1);
             }
 
-            // O *= alpha, once the previous P V has landed (only when a row of
-            // this warp moved its maximum)
+            // O *= alpha (only when a row of this warp moved its maximum). The
+            // previous P V has landed: Q K^T j was issued after it, and S_FULL
+            // tracks every MMA issued before that Q K^T.
             if (j > 0 && __any_sync(kFull, need)) {
-                ok = ptx::bar_wait(bar(S::kODone + t), (cnt - 1) & 1, abort_flag, p.timeout_ns);
-                if (!__all_sync(kFull, ok)) { ok = false; break; }
-                ptx::tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
@@ -509,11 +509,13 @@ __device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, i
         }
         if (!ok) break;
 
-        // epilogue: O / l in the input dtype, LSE = (m + log2 l) * ln 2
+        // epilogue: O / l in the input dtype, LSE = (m + log2 l) * ln 2. O_DONE
+        // completes once per work item of this tile, after its last P V.
         if (nkv > 0) {
-            ok = ptx::bar_wait(bar(S::kODone + t), (cnt - 1) & 1, abort_flag, p.timeout_ns);
+            ok = ptx::bar_wait(bar(S::kODone + t), items & 1, abort_flag, p.timeout_ns);
             if (!__all_sync(kFull, ok)) { ok = false; break; }
             ptx::tc_fence_after();
+            ++items;
         }
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
         const float lse = l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;

@@ -71,13 +71,12 @@ __device__ __forceinline__ bool bar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
-// Wait until the phase with the given parity has completed. Returns false if
-// the CTA abort flag is (or becomes) set or the wait exceeds timeout_ns; a
-// timeout sets the abort flag itself. With abort_flag == nullptr only the
-// timeout ends the wait (used when draining after an abort).
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                         uint64_t timeout_ns) {
-    if (bar_try_wait(bar, parity)) return true;
+// Slow path of bar_wait(): the phase was not complete at the first test. Kept
+// out of line so that the common case (a phase that has already completed)
+// costs one mbarrier test and a branch: with the timer and the retry loop
+// inlined, every wait paid for them.
+static __device__ __noinline__ bool bar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                           uint64_t timeout_ns) {
     const uint64_t t0 = globaltimer();
     for (;;) {
 #pragma unroll 1
@@ -89,6 +88,16 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile
             return false;
         }
     }
+}
+
+// Wait until the phase with the given parity has completed. Returns false if
+// the CTA abort flag is (or becomes) set or the wait exceeds timeout_ns; a
+// timeout sets the abort flag itself. With abort_flag == nullptr only the
+// timeout ends the wait (used when draining after an abort).
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         uint64_t timeout_ns) {
+    if (bar_try_wait(bar, parity)) return true;
+    return bar_wait_slow(bar, parity, abort_flag, timeout_ns);
 }
 
 // True on every lane iff it is true on every lane of the (converged) warp.

@@ -5,7 +5,9 @@ One step = one pass of the whole path over one batch of synthetic inputs:
   * prefill: FlashAttention-2 forward, B=1 H=32 Sq=Sk=4096 D=128 bf16, causal
     (the LLaMA-7B prefill shape of the pages' benchmark table), and
   * decode: split-KV decoding, B=16 H=8 Sk=8192 D=128 bf16, 32 partitions,
-    phase 1 + log-sum-exp merge.
+    phase 1 + log-sum-exp merge in one launch (the last partition of each head
+    merges it); the two-launch form (phase 1, then a merge launch) is timed
+    beside it.
 The headline `value` is prefill attention TFLOPS (causal FLOPs counted at half
 of 4*B*H*S^2*D); the decode throughput in GB/s (K and V read once, plus q and
 O) sits in the `decode` object. Inputs are resident in HBM, and L2 is flushed
@@ -322,6 +324,7 @@ def run_gpu(args, rank, world, local):
     ws = (torch.empty(wd.B, wd.H, S, wd.D, dtype=torch.float32, device=dev),
           torch.empty(wd.B, wd.H, S, dtype=torch.float32, device=dev),
           torch.empty(wd.B, wd.H, S, dtype=torch.float32, device=dev))
+    counters = torch.zeros(wd.B * wd.H, dtype=torch.int32, device=dev)
     do = torch.empty(wd.B, wd.H, 1, wd.D, dtype=wd.dtype, device=dev)
     dlse = torch.empty(wd.B, wd.H, dtype=torch.float32, device=dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
@@ -341,20 +344,16 @@ def run_gpu(args, rank, world, local):
         if evs:
             evs[1].record(stream)
         if run_dc:
-            fa.fa_decode_splitkv(dq, dk, dv, *ws, S, wd.scale, stream)
+            fa.fa_decode_splitkv_fused(dq, dk, dv, do, dlse, *ws, counters, S, wd.scale, stream)
         if evs:
             evs[2].record(stream)
-        if run_dc:
-            fa.fa_splitkv_merge(*ws, do, dlse, stream)
-        if evs:
-            evs[3].record(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     fa.fa_check_device_error()
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     if world > 1:
         import torch.distributed as dist
@@ -375,10 +374,8 @@ def run_gpu(args, rank, world, local):
     fa.fa_check_device_error()
 
     pf = [e[0].elapsed_time(e[1]) for e in events]  # ms
-    sp = [e[1].elapsed_time(e[2]) for e in events]
-    mg = [e[2].elapsed_time(e[3]) for e in events]
-    pf_sum, sp_sum, mg_sum = sum(pf), sum(sp), sum(mg)
-    pf_sum, dc_sum, wall = aggregate_max([pf_sum, sp_sum + mg_sum, wall], world)
+    dc = [e[1].elapsed_time(e[2]) for e in events]
+    pf_sum, dc_sum, wall = aggregate_max([sum(pf), sum(dc), wall], world)
     K = args.steps
 
     if not (run_pf and run_dc):  # a profiling run of one part: a short record, not the report
@@ -387,13 +384,13 @@ def run_gpu(args, rank, world, local):
             rec.update(prefill_tflops=pf_flops / (statistics.mean(pf) * 1e-3) / 1e12,
                        prefill_ms=statistics.mean(pf), prefill_ms_median=statistics.median(pf))
         if run_dc:
-            rec.update(decode_gbs=dc_bytes / ((statistics.mean(sp) + statistics.mean(mg)) * 1e-3) / 1e9,
-                       split_ms=statistics.mean(sp), merge_ms=statistics.mean(mg))
+            rec.update(decode_gbs=dc_bytes / (statistics.mean(dc) * 1e-3) / 1e9, decode_ms=statistics.mean(dc))
         if rank == 0:
             print(json.dumps(rec), flush=True)
         return None
     prefill_tflops = world * pf_flops * K / (pf_sum * 1e-3) / 1e12
     decode_gbs = world * dc_bytes * K / (dc_sum * 1e-3) / 1e9
+    two = run_two_launch(args, fa, torch, stream, flush, world, (dq, dk, dv), ws, do, dlse, wd)
     paged = run_paged(args, fa, torch, stream, dev, flush, world)
     # end-to-end through host buffers (pinned), copies inside the timed region
     e2e = ({"prefill": None, "decode": None} if args.no_e2e else
@@ -402,10 +399,9 @@ def run_gpu(args, rank, world, local):
     peaks, peak_src = load_peaks()
     traffic = committed_traffic()
     pf_avg_ms = statistics.mean(pf)
-    sp_avg_ms = statistics.mean(sp)
+    dc_avg_ms = statistics.mean(dc)
     achieved_tf = pf_flops / (pf_avg_ms * 1e-3) / 1e12
-    achieved_gbs = dc_bytes / ((sp_avg_ms + statistics.mean(mg)) * 1e-3) / 1e9
-    split_gbs = dc_bytes / (sp_avg_ms * 1e-3) / 1e9
+    achieved_gbs = dc_bytes / (dc_avg_ms * 1e-3) / 1e9
     tb = traffic.get("fa_fwd_kernel")
     line = {
         "metric": METRIC, "value": prefill_tflops, "unit": "TFLOPS", "n_gpus": world, "steps": K,
@@ -419,28 +415,64 @@ def run_gpu(args, rank, world, local):
                      "per_launch_flops": pf_flops, "avg_launch_ms": pf_avg_ms},
         "decode": {
             "metric": "split-KV decode HBM GB/s", "value": decode_gbs, "unit": "GB/s",
-            "ms_per_step": dc_sum / K, "split_ms": sp_avg_ms, "merge_ms": statistics.mean(mg),
-            "roofline": {"bound": "hbm", "kernel": "fa_decode_split_kernel<128,bf16> + fa_splitkv_merge_kernel",
+            "ms_per_step": dc_sum / K, "path": "fa_decode_splitkv_fused (phase 1 + merge, one launch)",
+            "roofline": {"bound": "hbm", "kernel": "fa_decode_split_kernel<128,bf16,dense,fused>",
                          "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved_gbs / peaks["hbm_gbs"], "frac_of_8000_nominal": achieved_gbs / 8000.0,
-                         "split_only_gbs": split_gbs, "split_only_frac": split_gbs / peaks["hbm_gbs"],
-                         "traffic": traffic.get("fa_decode_split_kernel"), "peak_source": f"{peak_src} copy",
-                         "per_step_bytes": dc_bytes},
+                         "traffic": traffic.get("fa_decode_split_kernel_fused"), "peak_source": f"{peak_src} copy",
+                         "per_step_bytes": dc_bytes, "avg_launch_ms": dc_avg_ms},
+            "two_launch": two,
             "e2e": e2e["decode"],
         },
         "e2e": e2e["prefill"],
         "paged_decode": paged,
-        "gpu_launches": 3 * K,
+        "gpu_launches": 2 * K,
         "clocks": clock,
         "wall_ms_per_step": 1e3 * wall / K,
     }
     return line
 
 
+def run_two_launch(args, fa, torch, stream, flush, world, dec, ws, o, lse, wd):
+    """The two-launch decode (fa_decode_splitkv, then fa_splitkv_merge) on the
+    decode workload, timed on its own loop with the same L2 flush."""
+    from exact_attention_54_gb300.metrics import decode_bytes
+    dq, dk, dv = dec
+    S = wd.num_splits
+    n = max(1, min(args.steps, 500))
+
+    def step(evs=None):
+        flush.fill_(float(1.0))
+        if evs:
+            evs[0].record(stream)
+        fa.fa_decode_splitkv(dq, dk, dv, *ws, S, wd.scale, stream)
+        if evs:
+            evs[1].record(stream)
+        fa.fa_splitkv_merge(*ws, o, lse, stream)
+        if evs:
+            evs[2].record(stream)
+
+    for _ in range(3):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    for i in range(n):
+        step(evs[i])
+    torch.cuda.synchronize()
+    sp, mg = aggregate_max([sum(e[0].elapsed_time(e[1]) for e in evs) / n,
+                            sum(e[1].elapsed_time(e[2]) for e in evs) / n], world)
+    nbytes = decode_bytes(wd.B, wd.H, wd.Sk, wd.D)
+    peaks, _ = load_peaks()
+    gbs = world * nbytes / ((sp + mg) * 1e-3) / 1e9
+    return {"value": gbs, "unit": "GB/s", "split_ms": sp, "merge_ms": mg, "steps": n,
+            "frac_of_hbm": gbs / peaks["hbm_gbs"], "split_only_gbs": world * nbytes / (sp * 1e-3) / 1e9,
+            "traffic_split": committed_traffic().get("fa_decode_split_kernel"),
+            "traffic_merge": committed_traffic().get("fa_splitkv_merge_kernel")}
+
+
 def run_paged(args, fa, torch, stream, dev, flush, world):
     """Split-KV decode over a paged cache (16-key pages, permuted block table),
     same shapes and bytes as the decode workload; timed on its own loop with
-    the same L2 flush and CUDA events (split + merge)."""
+    the same L2 flush and CUDA events, one-launch (fused) and two-launch."""
     from exact_attention_54_gb300 import inputs
     from exact_attention_54_gb300.metrics import decode_bytes
     w = inputs.WORKLOADS["paged_decode"]
@@ -451,30 +483,40 @@ def run_paged(args, fa, torch, stream, dev, flush, world):
           torch.empty(w.B, w.H, S, dtype=torch.float32, device=dev))
     o = torch.empty(w.B, w.H, 1, w.D, dtype=w.dtype, device=dev)
     lse = torch.empty(w.B, w.H, dtype=torch.float32, device=dev)
+    counters = torch.zeros(w.B * w.H, dtype=torch.int32, device=dev)
     n = max(1, min(args.steps, 500))
 
-    def step(evs=None):
+    def step(fused, evs=None):
         flush.fill_(float(1.0))
         if evs:
             evs[0].record(stream)
-        fa.fa_decode_paged_splitkv(q, kc, vc, bt, sl, *ws, S, w.scale, stream)
-        fa.fa_splitkv_merge(*ws, o, lse, stream)
+        if fused:
+            fa.fa_decode_paged_splitkv_fused(q, kc, vc, bt, sl, o, lse, *ws, counters, S, w.scale, stream)
+        else:
+            fa.fa_decode_paged_splitkv(q, kc, vc, bt, sl, *ws, S, w.scale, stream)
+            fa.fa_splitkv_merge(*ws, o, lse, stream)
         if evs:
             evs[1].record(stream)
 
-    for _ in range(3):
-        step()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
-    for i in range(n):
-        step(evs[i])
-    torch.cuda.synchronize()
-    fa.fa_check_device_error()
-    ms = aggregate_max([sum(e[0].elapsed_time(e[1]) for e in evs) / n], world)[0]
+    res = {}
+    for fused in (True, False):
+        for _ in range(3):
+            step(fused)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for i in range(n):
+            step(fused, evs[i])
+        torch.cuda.synchronize()
+        fa.fa_check_device_error()
+        res[fused] = aggregate_max([sum(e[0].elapsed_time(e[1]) for e in evs) / n], world)[0]
     nbytes = decode_bytes(w.B, w.H, w.Sk, w.D)
     peaks, src = load_peaks()
-    gbs = world * nbytes / (ms * 1e-3) / 1e9
-    return {"workload": w.name, "value": gbs, "unit": "GB/s", "ms_per_step": ms, "steps": n,
-            "frac_of_hbm": gbs / peaks["hbm_gbs"], "block_size": w.extra["block_size"]}
+    gbs = world * nbytes / (res[True] * 1e-3) / 1e9
+    gbs2 = world * nbytes / (res[False] * 1e-3) / 1e9
+    return {"workload": w.name, "value": gbs, "unit": "GB/s", "ms_per_step": res[True], "steps": n,
+            "path": "fa_decode_paged_splitkv_fused", "frac_of_hbm": gbs / peaks["hbm_gbs"],
+            "block_size": w.extra["block_size"],
+            "two_launch": {"value": gbs2, "unit": "GB/s", "ms_per_step": res[False],
+                           "frac_of_hbm": gbs2 / peaks["hbm_gbs"]}}
 
 
 def run_e2e(args, fa, torch, stream, dev, wp, wd, pre, dec, world):
@@ -494,6 +536,7 @@ def run_e2e(args, fa, torch, stream, dev, wp, wd, pre, dec, world):
     ws = (torch.empty(wd.B, wd.H, S, wd.D, dtype=torch.float32, device=dev),
           torch.empty(wd.B, wd.H, S, dtype=torch.float32, device=dev),
           torch.empty(wd.B, wd.H, S, dtype=torch.float32, device=dev))
+    counters = torch.zeros(wd.B * wd.H, dtype=torch.int32, device=dev)
     do = torch.empty(wd.B, wd.H, 1, wd.D, dtype=wd.dtype, device=dev)
     dlse = torch.empty(wd.B, wd.H, dtype=torch.float32, device=dev)
     hdo = torch.empty(wd.B, wd.H, 1, wd.D, dtype=wd.dtype).pin_memory()
@@ -509,8 +552,7 @@ def run_e2e(args, fa, torch, stream, dev, wp, wd, pre, dec, world):
     def dec_step():
         for d, h in ((dq, gq), (dk, gk), (dv, gv)):
             d.copy_(h, non_blocking=True)
-        fa.fa_decode_splitkv(dq, dk, dv, *ws, S, wd.scale, stream)
-        fa.fa_splitkv_merge(*ws, do, dlse, stream)
+        fa.fa_decode_splitkv_fused(dq, dk, dv, do, dlse, *ws, counters, S, wd.scale, stream)
         hdo.copy_(do, non_blocking=True)
         hdl.copy_(dlse, non_blocking=True)
 

@@ -21,7 +21,7 @@ import threading
 import torch
 
 __all__ = ["FAError", "fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_decode_paged_splitkv", "fa_splitkv_merge",
-           "fa_check_device_error", "fa_status_string", "flash_attention", "flash_attention_varlen",
+           "fa_decode_splitkv_fused", "fa_decode_paged_splitkv_fused", "fa_check_device_error", "fa_status_string", "flash_attention", "flash_attention_varlen",
            "flash_decode", "flash_decode_paged", "library_path", "load_library", "EXPORTED_SYMBOLS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -32,7 +32,8 @@ _lib = None
 FA_FP16, FA_BF16 = 0, 1
 FA_MAX_SPLITS = 1024
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_decode_paged_splitkv", "fa_splitkv_merge",
-                    "fa_check_device_error", "fa_status_string", "fa_version")
+                    "fa_decode_splitkv_fused", "fa_decode_paged_splitkv_fused", "fa_check_device_error",
+                    "fa_status_string", "fa_version")
 
 
 class FAError(RuntimeError):
@@ -63,12 +64,15 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
         lib.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         lib.fa_splitkv_merge.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp]
+        lib.fa_decode_splitkv_fused.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        lib.fa_decode_paged_splitkv_fused.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i,
+                                                      f, i, vp]
         lib.fa_check_device_error.argtypes = [vp]
         lib.fa_status_string.argtypes = [i]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_version.argtypes = []
-        for name in ("fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_splitkv_merge",
-                     "fa_check_device_error", "fa_version"):
+        for name in ("fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_splitkv_merge", "fa_decode_splitkv_fused",
+                     "fa_decode_paged_splitkv_fused", "fa_check_device_error", "fa_version"):
             getattr(lib, name).restype = ctypes.c_int
         if path is None:
             _lib = lib
@@ -180,6 +184,39 @@ def fa_splitkv_merge(o_part, m_part, l_part, o, lse, stream=None):
     _check("fa_splitkv_merge", st)
 
 
+def fa_decode_splitkv_fused(q, k, v, o, lse, o_part, m_part, l_part, counters, num_splits: int,
+                            scale: float | None = None, stream=None):
+    """Both decode phases in one launch. Arguments as fa_decode_splitkv plus
+    o [B,H,1,D], lse [B,H] and counters, an int32 [B*H] CUDA tensor that is
+    zero before the first call and is left zero by every completed call."""
+    B, H, Sk, D = k.shape
+    _need_contig(q, k, v, o, lse, o_part, m_part, l_part, counters)
+    if counters.dtype != torch.int32:
+        raise TypeError("counters must be int32")
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    st = load_library().fa_decode_splitkv_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(o_part),
+                                                _ptr(m_part), _ptr(l_part), _ptr(counters), B, H, Sk, D,
+                                                int(num_splits), float(scale), _dtype_code(k), _stream(stream))
+    _check("fa_decode_splitkv_fused", st)
+
+
+def fa_decode_paged_splitkv_fused(q, k_cache, v_cache, block_table, seq_lens, o, lse, o_part, m_part, l_part,
+                                  counters, num_splits: int, scale: float | None = None, stream=None):
+    """Both decode phases over a paged cache in one launch (arguments as
+    fa_decode_paged_splitkv plus o, lse and counters as fa_decode_splitkv_fused)."""
+    B, H = q.shape[0], q.shape[1]
+    num_blocks, _, block_size, D = k_cache.shape
+    _need_contig(q, k_cache, v_cache, block_table, seq_lens, o, lse, o_part, m_part, l_part, counters)
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32 or counters.dtype != torch.int32:
+        raise TypeError("block_table, seq_lens and counters must be int32")
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    st = load_library().fa_decode_paged_splitkv_fused(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(o), _ptr(lse), _ptr(o_part),
+        _ptr(m_part), _ptr(l_part), _ptr(counters), B, H, D, num_blocks, block_size, block_table.shape[1],
+        int(num_splits), float(scale), _dtype_code(q), _stream(stream))
+    _check("fa_decode_paged_splitkv_fused", st)
+
+
 def fa_check_device_error(stream=None):
     """Synchronise the stream and raise if a kernel abandoned a barrier wait."""
     _check("fa_check_device_error", load_library().fa_check_device_error(_stream(stream)))
@@ -206,36 +243,49 @@ def flash_attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: in
     return o, lse
 
 
+def _decode_workspace(B, H, S, D, device, fused):
+    ws = (torch.empty(B, H, S, D, dtype=torch.float32, device=device),
+          torch.empty(B, H, S, dtype=torch.float32, device=device),
+          torch.empty(B, H, S, dtype=torch.float32, device=device))
+    return ws + (torch.zeros(B * H, dtype=torch.int32, device=device),) if fused else ws
+
+
 def flash_decode_paged(q, k_cache, v_cache, block_table, seq_lens, num_splits: int, scale: float | None = None,
-                       stream=None, workspace=None):
+                       stream=None, workspace=None, fused: bool = False):
     """Split-KV decoding over a paged cache (phase 1 + phase 2). Returns
-    (o [B,H,1,D], lse [B,H])."""
+    (o [B,H,1,D], lse [B,H]). ``workspace`` may pass preallocated (o_part,
+    m_part, l_part), plus the int32 [B*H] counters when ``fused``."""
     B, H = q.shape[0], q.shape[1]
     D = k_cache.shape[3]
     if workspace is None:
-        workspace = (torch.empty(B, H, num_splits, D, dtype=torch.float32, device=q.device),
-                     torch.empty(B, H, num_splits, dtype=torch.float32, device=q.device),
-                     torch.empty(B, H, num_splits, dtype=torch.float32, device=q.device))
-    o_part, m_part, l_part = workspace
+        workspace = _decode_workspace(B, H, num_splits, D, q.device, fused)
     o = torch.empty(B, H, 1, D, dtype=q.dtype, device=q.device)
     lse = torch.empty(B, H, dtype=torch.float32, device=q.device)
+    if fused:
+        fa_decode_paged_splitkv_fused(q, k_cache, v_cache, block_table, seq_lens, o, lse, *workspace, num_splits,
+                                      scale, stream)
+        return o, lse
+    o_part, m_part, l_part = workspace[:3]
     fa_decode_paged_splitkv(q, k_cache, v_cache, block_table, seq_lens, o_part, m_part, l_part, num_splits, scale,
                             stream)
     fa_splitkv_merge(o_part, m_part, l_part, o, lse, stream)
     return o, lse
 
 
-def flash_decode(q, k, v, num_splits: int, scale: float | None = None, stream=None, workspace=None):
+def flash_decode(q, k, v, num_splits: int, scale: float | None = None, stream=None, workspace=None,
+                 fused: bool = False):
     """Split-KV decoding (phase 1 + phase 2). Returns (o [B,H,1,D], lse [B,H]).
-    ``workspace`` may pass preallocated (o_part, m_part, l_part)."""
+    ``workspace`` may pass preallocated (o_part, m_part, l_part), plus the
+    int32 [B*H] counters when ``fused`` (one launch instead of two)."""
     B, H, Sk, D = k.shape
     if workspace is None:
-        workspace = (torch.empty(B, H, num_splits, D, dtype=torch.float32, device=k.device),
-                     torch.empty(B, H, num_splits, dtype=torch.float32, device=k.device),
-                     torch.empty(B, H, num_splits, dtype=torch.float32, device=k.device))
-    o_part, m_part, l_part = workspace
+        workspace = _decode_workspace(B, H, num_splits, D, k.device, fused)
     o = torch.empty(B, H, 1, D, dtype=k.dtype, device=k.device)
     lse = torch.empty(B, H, dtype=torch.float32, device=k.device)
+    if fused:
+        fa_decode_splitkv_fused(q, k, v, o, lse, *workspace, num_splits, scale, stream)
+        return o, lse
+    o_part, m_part, l_part = workspace[:3]
     fa_decode_splitkv(q, k, v, o_part, m_part, l_part, num_splits, scale, stream)
     fa_splitkv_merge(o_part, m_part, l_part, o, lse, stream)
     return o, lse

@@ -269,6 +269,89 @@ fa_status_t fa_decode_paged_splitkv(const void *q, const void *k_cache, const vo
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+fa_status_t fa_decode_splitkv_fused(const void *q, const void *k, const void *v, void *o, float *lse, float *o_part,
+                                    float *m_part, float *l_part, int32_t *counters, int B, int H, int Sk, int D,
+                                    int num_splits, float scale, fa_dtype_t dtype, void *stream) {
+    if (!q || !k || !v || !o || !lse || !o_part || !m_part || !l_part || !counters) return FA_ERR_NULL;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+    if (D != 64 && D != 128) return FA_ERR_HEADDIM;
+    if (B < 1 || H < 1 || Sk < 1 || Sk > kMaxLen) return FA_ERR_SHAPE;
+    if (num_splits < 1 || num_splits > Sk || num_splits > FA_MAX_SPLITS) return FA_ERR_SPLITS;
+    const long long BH = static_cast<long long>(B) * H;
+    if (BH * num_splits > INT_MAX) return FA_ERR_SHAPE;
+    if (!scale_ok(scale)) return FA_ERR_SCALE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) || !aligned4(o_part) ||
+        !aligned4(m_part) || !aligned4(l_part) || !aligned4(counters))
+        return FA_ERR_ALIGN;
+    fa::DecodeParams p{};
+    p.q = static_cast<const uint16_t *>(q);
+    p.k = static_cast<const uint16_t *>(k);
+    p.v = static_cast<const uint16_t *>(v);
+    p.o_part = o_part;
+    p.m_part = m_part;
+    p.l_part = l_part;
+    p.H = H;
+    p.Sk = Sk;
+    p.num_splits = num_splits;
+    p.keys_per_split = (Sk + num_splits - 1) / num_splits;
+    p.scale_log2 = scale * kLog2e;
+    p.o = o;
+    p.lse = lse;
+    p.counters = counters;
+    const cudaError_t e = fa::launch_decode_fused(D, dtype == FA_BF16, false, p, static_cast<int>(BH),
+                                                  static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status_t fa_decode_paged_splitkv_fused(const void *q, const void *k_cache, const void *v_cache,
+                                          const int32_t *block_table, const int32_t *seq_lens, void *o, float *lse,
+                                          float *o_part, float *m_part, float *l_part, int32_t *counters, int B,
+                                          int H, int D, int num_blocks, int block_size, int max_blocks_per_seq,
+                                          int num_splits, float scale, fa_dtype_t dtype, void *stream) {
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !lse || !o_part || !m_part || !l_part ||
+        !counters)
+        return FA_ERR_NULL;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+    if (D != 64 && D != 128) return FA_ERR_HEADDIM;
+    if (B < 1 || H < 1 || num_blocks < 1 || max_blocks_per_seq < 1) return FA_ERR_SHAPE;
+    if (block_size < 1 || block_size > 1024 || (block_size & (block_size - 1)) != 0) return FA_ERR_SHAPE;
+    if (static_cast<long long>(max_blocks_per_seq) * block_size > kMaxLen) return FA_ERR_SHAPE;
+    if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_SPLITS;
+    const long long BH = static_cast<long long>(B) * H;
+    if (BH * num_splits > INT_MAX || static_cast<long long>(num_blocks) * H > INT_MAX) return FA_ERR_SHAPE;
+    if (!scale_ok(scale)) return FA_ERR_SCALE;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned4(block_table) ||
+        !aligned4(seq_lens) || !aligned16(o) || !aligned4(lse) || !aligned4(o_part) || !aligned4(m_part) ||
+        !aligned4(l_part) || !aligned4(counters))
+        return FA_ERR_ALIGN;
+    int *err = device_error_word();
+    if (err == nullptr) return FA_ERR_CUDA;
+    int log2_bs = 0;
+    while ((1 << log2_bs) < block_size) ++log2_bs;
+    fa::DecodeParams p{};
+    p.q = static_cast<const uint16_t *>(q);
+    p.k = static_cast<const uint16_t *>(k_cache);
+    p.v = static_cast<const uint16_t *>(v_cache);
+    p.o_part = o_part;
+    p.m_part = m_part;
+    p.l_part = l_part;
+    p.H = H;
+    p.num_splits = num_splits;
+    p.scale_log2 = scale * kLog2e;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.max_blocks = max_blocks_per_seq;
+    p.log2_bs = log2_bs;
+    p.num_blocks = num_blocks;
+    p.err = err;
+    p.o = o;
+    p.lse = lse;
+    p.counters = counters;
+    const cudaError_t e = fa::launch_decode_fused(D, dtype == FA_BF16, true, p, static_cast<int>(BH),
+                                                  static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 fa_status_t fa_splitkv_merge(const float *o_part, const float *m_part, const float *l_part, void *o, float *lse,
                              int B, int H, int D, int num_splits, fa_dtype_t dtype, void *stream) {
     if (!o_part || !m_part || !l_part || !o || !lse) return FA_ERR_NULL;

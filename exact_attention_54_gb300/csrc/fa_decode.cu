@@ -13,6 +13,10 @@
 //
 // Phase 2 (same passage): O = sum_s e^{m_s - m_g} / l_g * O_s with
 // m_g = max_s m_s, l_g = sum_s e^{m_s - m_g} l_s, and LSE = m_g + ln l_g.
+// It runs either as its own launch (one CTA per head) or fused into phase 1:
+// every partition CTA counts itself done on a per-head counter after its
+// partials are out, and the CTA that finishes last merges the head with the
+// same routine, then resets the counter for the next call.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -54,6 +58,89 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
     return r;
 }
 
+// Phase 2 for one head, run by a whole CTA of THREADS threads = kGroups groups
+// of D (one output element per thread and group). The weights e^{m_s - m_g}
+// are computed once per partition in parallel and kept in shared memory; each
+// group then sums every kGroups-th partition with eight independent loads in
+// flight, and the group sums are added through shared memory. Partials are
+// read through L2 (ld.global.cg): in the fused path other CTAs wrote them
+// during this launch.
+template <int THREADS>
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float *red) {
+    constexpr int kWarps = THREADS / 32;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, v, off);
+        v = is_max ? fmaxf(v, o) : v + o;
+    }
+    if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = v;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int i = 1; i < kWarps; ++i) r = is_max ? fmaxf(r, red[i]) : r + red[i];
+    __syncthreads();
+    return r;
+}
+
+template <int D, bool BF16, int THREADS>
+__device__ __forceinline__ void merge_head(const float *o_part, const float *m_part, const float *l_part,
+                                           uint16_t *o, float *lse, int bh, int num_splits) {
+    constexpr int kGroups = THREADS / D;
+    constexpr int U = 8;
+    __shared__ float w[FA_MAX_SPLITS];
+    __shared__ float red[THREADS / 32];
+    __shared__ float part[kGroups][D];
+    const int tid = threadIdx.x;
+    const int g = tid / D, d = tid % D;
+    const float *mp = m_part + static_cast<size_t>(bh) * num_splits;
+    const float *lp = l_part + static_cast<size_t>(bh) * num_splits;
+    const float *op = o_part + static_cast<size_t>(bh) * num_splits * D + d;
+
+    float mx = -CUDART_INF_F;
+    for (int s = tid; s < num_splits; s += THREADS) mx = fmaxf(mx, __ldcg(mp + s));
+    const float mg = block_reduce<THREADS>(mx, true, red);
+    float lsum = 0.f;
+    for (int s = tid; s < num_splits; s += THREADS) {
+        const float ws = (mg == -CUDART_INF_F) ? 0.f : expf(__ldcg(mp + s) - mg);
+        w[s] = ws;
+        lsum = fmaf(ws, __ldcg(lp + s), lsum);
+    }
+    const float lg = block_reduce<THREADS>(lsum, false, red);  // its barriers also publish w[]
+
+    float acc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) acc[u] = 0.f;
+    int s = g;
+    for (; s + (U - 1) * kGroups < num_splits; s += U * kGroups) {
+        float x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) x[u] = __ldcg(op + static_cast<size_t>(s + u * kGroups) * D);
+#pragma unroll
+        for (int u = 0; u < U; ++u) acc[u] = fmaf(w[s + u * kGroups], x[u], acc[u]);
+    }
+    for (; s < num_splits; s += kGroups) acc[0] = fmaf(w[s], __ldcg(op + static_cast<size_t>(s) * D), acc[0]);
+    float total = 0.f;
+#pragma unroll
+    for (int u = 0; u < U; ++u) total += acc[u];
+    if constexpr (kGroups > 1) {
+        part[g][d] = total;
+        __syncthreads();
+    }
+    if (g == 0) {
+#pragma unroll
+        for (int i = 1; i < kGroups; ++i) total += part[i][d];
+        const float out = lg > 0.f ? total / lg : 0.f;
+        if constexpr (BF16) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(out);
+            o[static_cast<size_t>(bh) * D + d] = *reinterpret_cast<const uint16_t *>(&h);
+        } else {
+            const __half h = __float2half_rn(out);
+            o[static_cast<size_t>(bh) * D + d] = *reinterpret_cast<const uint16_t *>(&h);
+        }
+        if (d == 0) lse[bh] = lg > 0.f ? mg + logf(lg) : -CUDART_INF_F;
+    }
+}
+
 // grid: one CTA per (head, partition), x = bh * num_splits + s.
 // PAGED: K and V live in pages [num_blocks, H, block_size, D]; key position p
 // of sequence b is row p % block_size of page block_table[b][p / block_size],
@@ -61,7 +148,7 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
 // Attention Kernels in CUDA", Advanced Production Features 4). A page index
 // outside [0, num_blocks) is never dereferenced: its keys are skipped and the
 // device error word records kDeviceErrBadIndex.
-template <int D, bool BF16, bool PAGED>
+template <int D, bool BF16, bool PAGED, bool FUSED>
 __global__ void __launch_bounds__(kDecodeThreads)
     fa_decode_split_kernel(const DecodeParams p) {
     constexpr int kLanesPerKey = D / 8;                  // 16-byte pieces per key row
@@ -208,104 +295,47 @@ __global__ void __launch_bounds__(kDecodeThreads)
             p.l_part[ps] = L;
         }
     }
-}
-
-// grid: one CTA per head, kMergeThreads threads = kGroups groups of D (one
-// output element per thread and group). The weights e^{m_s - m_g} are computed
-// once per partition in parallel and kept in shared memory; each group then
-// sums every kGroups-th partition with eight independent loads in flight, and
-// the group sums are added through shared memory.
-constexpr int kMergeThreads = 256;
-
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float *red) {
-    constexpr int kWarps = kMergeThreads / 32;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float o = __shfl_xor_sync(0xffffffffu, v, off);
-        v = is_max ? fmaxf(v, o) : v + o;
+    if constexpr (FUSED) {
+        // Count this partition done once its partials are visible device-wide;
+        // the last one of the head merges it and re-arms the counter.
+        __shared__ int is_last;
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) is_last = atomicAdd(p.counters + bh, 1) == num_splits - 1;
+        __syncthreads();
+        if (is_last) {
+            __threadfence();
+            merge_head<D, BF16, kDecodeThreads>(p.o_part, p.m_part, p.l_part, static_cast<uint16_t *>(p.o), p.lse,
+                                                bh, num_splits);
+            if (threadIdx.x == 0) p.counters[bh] = 0;
+        }
     }
-    if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = v;
-    __syncthreads();
-    float r = red[0];
-#pragma unroll
-    for (int i = 1; i < kWarps; ++i) r = is_max ? fmaxf(r, red[i]) : r + red[i];
-    __syncthreads();
-    return r;
 }
+
+// Phase 2 as its own launch: one CTA per head.
+constexpr int kMergeThreads = 256;
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kMergeThreads)
     fa_splitkv_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ m_part,
                             const float *__restrict__ l_part, uint16_t *__restrict__ o, float *__restrict__ lse,
                             int num_splits) {
-    constexpr int kGroups = kMergeThreads / D;
-    constexpr int U = 8;
-    __shared__ float w[FA_MAX_SPLITS];
-    __shared__ float red[kMergeThreads / 32];
-    __shared__ float part[kGroups][D];
-    const int bh = blockIdx.x;
-    const int tid = threadIdx.x;
-    const int g = tid / D, d = tid % D;
-    const float *mp = m_part + static_cast<size_t>(bh) * num_splits;
-    const float *lp = l_part + static_cast<size_t>(bh) * num_splits;
-    const float *op = o_part + static_cast<size_t>(bh) * num_splits * D + d;
-
-    float mx = -CUDART_INF_F;
-    for (int s = tid; s < num_splits; s += kMergeThreads) mx = fmaxf(mx, mp[s]);
-    const float mg = block_reduce(mx, true, red);
-    float lsum = 0.f;
-    for (int s = tid; s < num_splits; s += kMergeThreads) {
-        const float ws = (mg == -CUDART_INF_F) ? 0.f : expf(mp[s] - mg);
-        w[s] = ws;
-        lsum = fmaf(ws, lp[s], lsum);
-    }
-    const float lg = block_reduce(lsum, false, red);  // its barriers also publish w[]
-
-    float acc[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) acc[u] = 0.f;
-    int s = g;
-    for (; s + (U - 1) * kGroups < num_splits; s += U * kGroups) {
-        float x[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) x[u] = op[static_cast<size_t>(s + u * kGroups) * D];
-#pragma unroll
-        for (int u = 0; u < U; ++u) acc[u] = fmaf(w[s + u * kGroups], x[u], acc[u]);
-    }
-    for (; s < num_splits; s += kGroups) acc[0] = fmaf(w[s], op[static_cast<size_t>(s) * D], acc[0]);
-    float total = 0.f;
-#pragma unroll
-    for (int u = 0; u < U; ++u) total += acc[u];
-    part[g][d] = total;
-    __syncthreads();
-    if (g == 0) {
-#pragma unroll
-        for (int i = 1; i < kGroups; ++i) total += part[i][d];
-        const float out = lg > 0.f ? total / lg : 0.f;
-        if constexpr (BF16) {
-            const __nv_bfloat16 h = __float2bfloat16_rn(out);
-            o[static_cast<size_t>(bh) * D + d] = *reinterpret_cast<const uint16_t *>(&h);
-        } else {
-            const __half h = __float2half_rn(out);
-            o[static_cast<size_t>(bh) * D + d] = *reinterpret_cast<const uint16_t *>(&h);
-        }
-        if (d == 0) lse[bh] = lg > 0.f ? mg + logf(lg) : -CUDART_INF_F;
-    }
+    merge_head<D, BF16, kMergeThreads>(o_part, m_part, l_part, o, lse, static_cast<int>(blockIdx.x), num_splits);
 }
 
-template <int D, bool BF16, bool PAGED>
+template <int D, bool BF16, bool PAGED, bool FUSED>
 static cudaError_t launch_split_t(const DecodeParams &p, int BH, cudaStream_t st) {
     const long long grid = static_cast<long long>(BH) * p.num_splits;
-    fa_decode_split_kernel<D, BF16, PAGED><<<static_cast<unsigned>(grid), kDecodeThreads, 0, st>>>(p);
+    fa_decode_split_kernel<D, BF16, PAGED, FUSED><<<static_cast<unsigned>(grid), kDecodeThreads, 0, st>>>(p);
     return cudaGetLastError();
 }
 
-template <bool PAGED>
+template <bool PAGED, bool FUSED = false>
 static cudaError_t launch_split_any(int D, bool bf16, const DecodeParams &p, int BH, cudaStream_t st) {
-    if (D == 64 && !bf16) return launch_split_t<64, false, PAGED>(p, BH, st);
-    if (D == 64 && bf16) return launch_split_t<64, true, PAGED>(p, BH, st);
-    if (D == 128 && !bf16) return launch_split_t<128, false, PAGED>(p, BH, st);
-    if (D == 128 && bf16) return launch_split_t<128, true, PAGED>(p, BH, st);
+    if (D == 64 && !bf16) return launch_split_t<64, false, PAGED, FUSED>(p, BH, st);
+    if (D == 64 && bf16) return launch_split_t<64, true, PAGED, FUSED>(p, BH, st);
+    if (D == 128 && !bf16) return launch_split_t<128, false, PAGED, FUSED>(p, BH, st);
+    if (D == 128 && bf16) return launch_split_t<128, true, PAGED, FUSED>(p, BH, st);
     return cudaErrorInvalidValue;
 }
 
@@ -336,6 +366,11 @@ cudaError_t launch_decode_split(int D, bool bf16, const void *q, const void *k, 
 
 cudaError_t launch_decode_split_paged(int D, bool bf16, const DecodeParams &p, int BH, cudaStream_t stream) {
     return launch_split_any<true>(D, bf16, p, BH, stream);
+}
+
+cudaError_t launch_decode_fused(int D, bool bf16, bool paged, const DecodeParams &p, int BH, cudaStream_t stream) {
+    return paged ? launch_split_any<true, true>(D, bf16, p, BH, stream)
+                 : launch_split_any<false, true>(D, bf16, p, BH, stream);
 }
 
 cudaError_t launch_splitkv_merge(int D, bool bf16, const float *o_part, const float *m_part, const float *l_part,

@@ -51,6 +51,9 @@ struct DecodeParams {
     int log2_bs;                 // paged: log2(block_size)
     int num_blocks;              // paged: pages in the cache
     int *err;                    // paged: device error word
+    void *o;                     // fused: [B*H, D] output (input dtype)
+    float *lse;                  // fused: [B*H] log-sum-exp
+    int *counters;               // fused: [B*H] finished partitions per head, zero between calls
 };
 
 // maps: {Q, K, V} tensor maps (see fa_api.cu for their geometry).
@@ -65,6 +68,10 @@ cudaError_t launch_decode_split(int D, bool bf16, const void *q, const void *k, 
                                 cudaStream_t stream);
 
 cudaError_t launch_decode_split_paged(int D, bool bf16, const DecodeParams &p, int BH, cudaStream_t stream);
+
+// Phase 1 and phase 2 in one launch: the last partition of each head to
+// finish merges that head (p.o, p.lse, p.counters must be set).
+cudaError_t launch_decode_fused(int D, bool bf16, bool paged, const DecodeParams &p, int BH, cudaStream_t stream);
 
 cudaError_t launch_splitkv_merge(int D, bool bf16, const float *o_part, const float *m_part,
                                  const float *l_part, void *o, float *lse, int BH,

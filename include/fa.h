@@ -6,6 +6,8 @@
  *   fa_fwd_varlen      the same forward over packed variable-length sequences.
  *   fa_decode_splitkv  split-KV decoding, phase 1: per-partition partials.
  *   fa_splitkv_merge   split-KV decoding, phase 2: log-sum-exp merge.
+ *   fa_decode_splitkv_fused, fa_decode_paged_splitkv_fused
+ *                      both phases in one launch (last partition merges).
  *
  * Common rules
  *   - Every tensor pointer is a DEVICE pointer owned by the caller. The library
@@ -176,6 +178,53 @@ FA_API fa_status_t fa_decode_paged_splitkv(const void *q, const void *k_cache, c
 FA_API fa_status_t fa_splitkv_merge(const float *o_part, const float *m_part, const float *l_part,
                              void *o, float *lse, int B, int H, int D, int num_splits,
                              fa_dtype_t dtype, void *stream);
+
+/*
+ * fa_decode_splitkv_fused - split-KV decoding, phase 1 and phase 2 in one
+ * launch.
+ *
+ * Computes what fa_decode_splitkv followed by fa_splitkv_merge computes
+ * ("Adaptive High-Performance Attention Kernels in CUDA", Advanced Production
+ * Features 1: partial attention per partition, then the log-sum-exp merge),
+ * without the second launch: each partition's CTA writes its partials to
+ * o_part, m_part, l_part (same layout and values as fa_decode_splitkv), then
+ * counts itself done on the head's counter; the CTA that finishes last merges
+ * the head into o and lse and sets the counter back to zero.
+ *
+ *   q, k, v, o_part, m_part, l_part, B, H, Sk, D, num_splits, scale, dtype:
+ *             as fa_decode_splitkv
+ *   o         [B,H,1,D] output (dtype), lse [B,H] fp32: as fa_splitkv_merge
+ *   counters  device int32 [B*H], caller-owned. All zero before the first
+ *             call; a call that completes leaves it all zero again, so it can
+ *             be reused without clearing. If a call fails to launch, clear it.
+ * Calls that share counters or partial buffers must not overlap on the GPU.
+ * Errors: as fa_decode_splitkv, plus FA_ERR_NULL when o, lse or counters is
+ * NULL and FA_ERR_ALIGN when o is not 16-byte or lse/counters not 4-byte
+ * aligned.
+ */
+FA_API fa_status_t fa_decode_splitkv_fused(const void *q, const void *k, const void *v, void *o, float *lse,
+                                           float *o_part, float *m_part, float *l_part, int32_t *counters,
+                                           int B, int H, int Sk, int D, int num_splits, float scale,
+                                           fa_dtype_t dtype, void *stream);
+
+/*
+ * fa_decode_paged_splitkv_fused - fa_decode_paged_splitkv and
+ * fa_splitkv_merge in one launch, over a paged KV cache ("Adaptive ...",
+ * Advanced Production Features 4 and 1).
+ *
+ *   arguments as fa_decode_paged_splitkv, plus o, lse and counters as
+ *   fa_decode_splitkv_fused (same rules for counters).
+ * A length-0 sequence gives o = 0 and lse = -inf. Out-of-range page numbers
+ * are skipped and reported as by fa_decode_paged_splitkv.
+ * Errors: as fa_decode_paged_splitkv, plus those of fa_decode_splitkv_fused
+ * for o, lse and counters.
+ */
+FA_API fa_status_t fa_decode_paged_splitkv_fused(const void *q, const void *k_cache, const void *v_cache,
+                                                 const int32_t *block_table, const int32_t *seq_lens, void *o,
+                                                 float *lse, float *o_part, float *m_part, float *l_part,
+                                                 int32_t *counters, int B, int H, int D, int num_blocks,
+                                                 int block_size, int max_blocks_per_seq, int num_splits,
+                                                 float scale, fa_dtype_t dtype, void *stream);
 
 /*
  * fa_check_device_error - synchronise `stream`, then read and clear the

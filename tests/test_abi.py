@@ -133,6 +133,44 @@ def test_paged_validation(lib):
     assert _paged(lib, bt=A + 2) == ALIGN
 
 
+def _fused(lib, q=A, k=A, v=A, o=A, lse=A, op=A, mp=A, lp=A, cnt=A, B=2, H=2, Sk=100, D=128, S=32, scale=0.1,
+           dtype=1):
+    return lib.fa_decode_splitkv_fused(q, k, v, o, lse, op, mp, lp, cnt, B, H, Sk, D, S, scale, dtype, None)
+
+
+def test_fused_decode_validation(lib):
+    for kw in ("q", "o", "lse", "op", "cnt"):
+        assert _fused(lib, **{kw: None}) == NULL, kw
+    assert _fused(lib, dtype=4) == DTYPE
+    assert _fused(lib, D=96) == HEADDIM
+    assert _fused(lib, Sk=0) == SHAPE
+    assert _fused(lib, S=0) == SPLITS
+    assert _fused(lib, S=101) == SPLITS
+    assert _fused(lib, scale=-1.0) == SCALE
+    assert _fused(lib, o=MIS) == ALIGN
+    assert _fused(lib, cnt=A + 2) == ALIGN
+    assert _fused(lib, lse=A + 1) == ALIGN
+
+
+def _paged_fused(lib, q=A, kc=A, vc=A, bt=A, sl=A, o=A, lse=A, op=A, mp=A, lp=A, cnt=A, B=2, H=2, D=128, nb=64, bs=16,
+                 mb=8, S=4, scale=0.1, dtype=1):
+    return lib.fa_decode_paged_splitkv_fused(q, kc, vc, bt, sl, o, lse, op, mp, lp, cnt, B, H, D, nb, bs, mb, S, scale,
+                                             dtype, None)
+
+
+def test_paged_fused_validation(lib):
+    for kw in ("bt", "sl", "o", "lse", "cnt"):
+        assert _paged_fused(lib, **{kw: None}) == NULL, kw
+    assert _paged_fused(lib, dtype=2) == DTYPE
+    assert _paged_fused(lib, D=256) == HEADDIM
+    for kw in ({"nb": 0}, {"bs": 12}, {"mb": 0}):
+        assert _paged_fused(lib, **kw) == SHAPE, kw
+    assert _paged_fused(lib, S=2000) == SPLITS
+    assert _paged_fused(lib, scale=float("inf")) == SCALE
+    assert _paged_fused(lib, o=MIS) == ALIGN
+    assert _paged_fused(lib, cnt=A + 1) == ALIGN
+
+
 def test_merge_validation(lib):
     m = lib.fa_splitkv_merge
     assert m(None, A, A, A, A, 2, 2, 128, 8, 1, None) == NULL

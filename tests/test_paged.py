@@ -1,6 +1,7 @@
 """Split-KV decoding over a paged KV cache (fa_decode_paged_splitkv +
-fa_splitkv_merge) against the oracle's gather-then-attend definition, plus
-exact checks of the page bookkeeping."""
+fa_splitkv_merge, and the one-launch fa_decode_paged_splitkv_fused) against
+the oracle's gather-then-attend definition, plus exact checks of the page
+bookkeeping."""
 import numpy as np
 import pytest
 import torch
@@ -107,3 +108,40 @@ def test_paged_workload_full_size():
     ro, rl = oracle.decode_paged(q, kc, vc, bt, sl, w.scale)
     assert_close(o, ro, O_TOL, f"O {w.name}")
     assert_close(lse, rl[..., 0], LSE_TOL, f"LSE {w.name}")
+
+
+@pytest.mark.parametrize("D,dtype,bs,lens,S", [
+    (128, torch.bfloat16, 16, [1000, 1, 0, 257], 8),
+    (64, torch.float16, 64, [64, 65, 4096], 16),
+])
+def test_paged_fused_matches_oracle_and_two_launch_path(D, dtype, bs, lens, S):
+    B, H = len(lens), 3
+    q, kc, vc, bt, sl = inputs.make_paged(B, H, D, bs, lens, dtype, seed=sum(lens) + bs + 1)
+    scale = 1.0 / D ** 0.5
+    qd, kd, vd, btd, sld = dev(q, kc, vc, bt, sl)
+    cnt = torch.zeros(B * H, dtype=torch.int32, device="cuda")
+    ws = (torch.empty(B, H, S, D, device="cuda"), torch.empty(B, H, S, device="cuda"),
+          torch.empty(B, H, S, device="cuda"), cnt)
+    o, lse = fa.flash_decode_paged(qd, kd, vd, btd, sld, S, scale=scale, workspace=ws, fused=True)
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    assert torch.count_nonzero(cnt) == 0
+    ro, rl = oracle.decode_paged(q, kc, vc, bt, sl, scale)
+    assert_close(o.cpu(), ro, O_TOL, "paged fused O")
+    assert_close(lse.cpu(), rl[..., 0], LSE_TOL, "paged fused LSE")
+    o2, lse2, (op2, mp2, lp2) = run_paged(q, kc, vc, bt, sl, S, scale)
+    assert torch.equal(ws[0].cpu().view(torch.int32), op2.view(torch.int32))
+    assert torch.equal(ws[1].cpu().view(torch.int32), mp2.view(torch.int32))
+    assert torch.equal(ws[2].cpu().view(torch.int32), lp2.view(torch.int32))
+
+
+def test_paged_fused_workload_full_size():
+    w = inputs.WORKLOADS["paged_decode"]
+    q, kc, vc, bt, sl = inputs.make_workload(w)
+    qd, kd, vd, btd, sld = dev(q, kc, vc, bt, sl)
+    o, lse = fa.flash_decode_paged(qd, kd, vd, btd, sld, w.num_splits, scale=w.scale, fused=True)
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    ro, rl = oracle.decode_paged(q, kc, vc, bt, sl, w.scale)
+    assert_close(o.cpu(), ro, O_TOL, f"fused O {w.name}")
+    assert_close(lse.cpu(), rl[..., 0], LSE_TOL, f"fused LSE {w.name}")

@@ -391,6 +391,7 @@ def run_gpu(args, rank, world, local):
     prefill_tflops = world * pf_flops * K / (pf_sum * 1e-3) / 1e12
     decode_gbs = world * dc_bytes * K / (dc_sum * 1e-3) / 1e9
     two = run_two_launch(args, fa, torch, stream, flush, world, (dq, dk, dv), ws, do, dlse, wd)
+    d256 = run_d256(args, fa, torch, stream, dev, flush, world)
     paged = run_paged(args, fa, torch, stream, dev, flush, world)
     # end-to-end through host buffers (pinned), copies inside the timed region
     e2e = ({"prefill": None, "decode": None} if args.no_e2e else
@@ -426,6 +427,7 @@ def run_gpu(args, rank, world, local):
         },
         "e2e": e2e["prefill"],
         "paged_decode": paged,
+        "d256_prefill": d256,
         "gpu_launches": 2 * K,
         "clocks": clock,
         "wall_ms_per_step": 1e3 * wall / K,
@@ -467,6 +469,41 @@ def run_two_launch(args, fa, torch, stream, flush, world, dec, ws, o, lse, wd):
             "frac_of_hbm": gbs / peaks["hbm_gbs"], "split_only_gbs": world * nbytes / (sp * 1e-3) / 1e9,
             "traffic_split": committed_traffic().get("fa_decode_split_kernel"),
             "traffic_merge": committed_traffic().get("fa_splitkv_merge_kernel")}
+
+
+def run_d256(args, fa, torch, stream, dev, flush, world):
+    """The pages' large-head row (1, 16, 2048, 2048, 256), fp16, non-causal:
+    the D = 256 forward kernel, timed on its own loop with the same L2 flush."""
+    from exact_attention_54_gb300 import inputs
+    from exact_attention_54_gb300.metrics import attention_flops
+    w = inputs.WORKLOADS["d256"]
+    q, k, v = (t.to(dev) for t in inputs.make_workload(w))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.Sq, dtype=torch.float32, device=dev)
+    n = max(1, min(args.steps, 500))
+
+    def step(evs=None):
+        flush.fill_(float(1.0))
+        if evs:
+            evs[0].record(stream)
+        fa.fa_fwd(q, k, v, o, lse, w.causal, w.scale, stream)
+        if evs:
+            evs[1].record(stream)
+
+    for _ in range(3):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        step(evs[i])
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    ms = aggregate_max([sum(e[0].elapsed_time(e[1]) for e in evs) / n], world)[0]
+    flops = attention_flops(w.B, w.H, w.Sq, w.Sk, w.D, w.causal)
+    peaks, src = load_peaks()
+    tf = world * flops / (ms * 1e-3) / 1e12
+    return {"workload": w.name, "value": tf, "unit": "TFLOPS", "ms_per_launch": ms, "steps": n,
+            "kernel": "fa_fwd_d256_kernel<fp16,non-causal,dense>", "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+            "per_launch_flops": flops}
 
 
 def run_paged(args, fa, torch, stream, dev, flush, world):

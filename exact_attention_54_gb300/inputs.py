@@ -54,6 +54,10 @@ WORKLOADS = {
                        False, 1004, num_splits=32),
     "varlen": Workload("varlen_16seq_len64to2048_h16d128_bf16_causal", "varlen", 0, 16, 0, 0, 128,
                        torch.bfloat16, True, 1005, num_seqs=16, len_lo=64, len_hi=2048),
+    # the pages' large-head row, "GPT-4 style" (1, 16, 2048, 2048, 256): its
+    # printed TFLOPS match the non-causal FLOP count; fp16 (the page's T4 has
+    # no bf16)
+    "d256": Workload("gpt4style_b1h16s2048d256_fp16", "dense", 1, 16, 2048, 2048, 256, torch.float16, False, 1007),
     "paged_decode": Workload("paged_decode_b16h8sk8192d128_bf16_block16_split32", "paged", 16, 8, 1, 8192, 128,
                              torch.bfloat16, False, 1006, num_splits=32, extra={"block_size": 16}),
 }

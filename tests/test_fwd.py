@@ -53,6 +53,13 @@ SHAPES = [
     (2, 2, 640, 640, 128, torch.bfloat16, True),   # several tile pairs, odd tile count
     (1, 1, 1000, 1000, 64, torch.float16, False),
     (3, 2, 384, 512, 128, torch.bfloat16, False),
+    # D = 256 (one query tile per CTA, 64-key K/V tiles)
+    (1, 1, 1, 1, 256, torch.float16, True),
+    (1, 2, 300, 300, 256, torch.bfloat16, True),
+    (1, 2, 200, 77, 256, torch.float16, False),
+    (2, 1, 129, 500, 256, torch.bfloat16, False),
+    (1, 2, 77, 300, 256, torch.float16, True),
+    (2, 2, 640, 640, 256, torch.bfloat16, True),
 ]
 
 
@@ -75,10 +82,19 @@ def test_llama_prefill_full_size_sampled_rows():
     check(q, k, v, True, w.scale, rows=rows, what=w.name)
 
 
-def test_causal_skipped_tiles_never_read():
+def test_d256_workload_full_size_sampled_rows():
+    w = inputs.WORKLOADS["d256"]
+    q, k, v = inputs.make_workload(w)
+    rows = sample_rows(w.Sq, n_random=24, seed=w.seed)
+    check(q, k, v, w.causal, w.scale, rows=rows, what=w.name)
+    check(q, k, v, True, w.scale, rows=rows, what=w.name + " causal")
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_causal_skipped_tiles_never_read(D):
     """Causal, Sq = 256 < Sk = 512: keys 256.. are above every row's diagonal,
     so their tiles are skipped. NaN there must not change a single bit."""
-    q, k, v = inputs.make_dense(2, 2, 256, 512, 128, torch.bfloat16, seed=11)
+    q, k, v = inputs.make_dense(2, 2, 256, 512, D, torch.bfloat16, seed=11)
     o1, l1 = run(q, k, v, True, 0.1)
     k2, v2 = k.clone(), v.clone()
     k2[:, :, 256:] = float("nan")
@@ -88,12 +104,13 @@ def test_causal_skipped_tiles_never_read():
     assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
 
 
-def test_causal_mask_inside_diagonal_tiles_is_exact():
+@pytest.mark.parametrize("D", [64, 256])
+def test_causal_mask_inside_diagonal_tiles_is_exact(D):
     """Rows [0, r) of a causal run depend on keys [0, r) only. With huge K/V
     values planted in keys [r, S) (masked inside the straddling tile), rows
     [0, r) must equal, bit for bit, a run on the first r rows and keys."""
     S, r = 384, 200
-    q, k, v = inputs.make_dense(1, 2, S, S, 64, torch.float16, seed=12)
+    q, k, v = inputs.make_dense(1, 2, S, S, D, torch.float16, seed=12)
     k2, v2 = k.clone(), v.clone()
     k2[:, :, r:] = 3.0e4
     v2[:, :, r:] = -3.0e4
@@ -110,8 +127,9 @@ def test_ragged_key_tail_is_masked():
     check(q, k, v, False, 0.125, what="ragged key tail")
 
 
-def test_outputs_do_not_spill_past_the_buffer():
-    B, H, Sq, D = 1, 2, 200, 128
+@pytest.mark.parametrize("D", [128, 256])
+def test_outputs_do_not_spill_past_the_buffer(D):
+    B, H, Sq = 1, 2, 200
     q, k, v = dev(*inputs.make_dense(B, H, Sq, Sq, D, torch.bfloat16, seed=14))
     o_buf = torch.full((B * H * Sq * D + 4096,), 1.5, dtype=torch.bfloat16, device="cuda")
     l_buf = torch.full((B * H * Sq + 256,), 7.0, dtype=torch.float32, device="cuda")

@@ -11,7 +11,9 @@ out the outputs. Each function names the passage it follows.
 Parity pins live in tests/test_oracle.py: torch's fp64
 scaled_dot_product_attention and logsumexp on tiny shapes, closed forms and
 invariants, the split/merge identity, block-diagonal SDPA for the varlen
-bookkeeping, and mutation tests that plant mistakes in a copy of the C source.
+bookkeeping, torch fp64 autograd and central finite differences of the
+oracle's own forward for the backward pass, and mutation tests that plant
+mistakes in a copy of the C source.
 """
 from __future__ import annotations
 
@@ -82,6 +84,10 @@ class Oracle:
         lib.oracle_splitkv_partials.restype = ctypes.c_int
         lib.oracle_splitkv_merge.argtypes = [_dp, _dp, _dp, ctypes.c_int, ctypes.c_int, _dp, _dp]
         lib.oracle_splitkv_merge.restype = ctypes.c_int
+        lib.oracle_attention_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                             ctypes.c_int]
+        lib.oracle_attention_bwd.restype = ctypes.c_int
         self.lib = lib
         self.path = path
 
@@ -115,6 +121,29 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle_attention failed ({rc})")
         return o.reshape(*lead, nrows, D), lse.reshape(*lead, nrows)
+
+    def attention_bwd(self, q, k, v, dout, causal: bool, scale: float, nthreads: int | None = None):
+        """Gradients (dq, dk, dv) of sum(O * dout) for O = attention(q, k, v)
+        ("Adaptive High-Performance Attention Kernels in CUDA", Advanced
+        Production Features 2: S and P recomputed, D_i = sum_k dO_ik O_ik,
+        dS = P (dP - D); dV = P^T dO, dP = dO V^T, dQ = scale dS K,
+        dK = scale dS^T Q). Tensors laid out [..., S, D]; float64 results."""
+        q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+        lead = q.shape[:-2]
+        Sq, D = q.shape[-2:]
+        Sk = k.shape[-2]
+        if k.shape[:-2] != lead or v.shape != k.shape or dout.shape != q.shape or k.shape[-1] != D:
+            raise ValueError("shape mismatch between q, k, v and dout")
+        BH = int(np.prod(lead)) if lead else 1
+        dq = np.zeros((BH, Sq, D), np.float64)
+        dk = np.zeros((BH, Sk, D), np.float64)
+        dv = np.zeros((BH, Sk, D), np.float64)
+        rc = self.lib.oracle_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                                           BH, Sq, Sk, D, int(bool(causal)), float(scale),
+                                           nthreads or default_threads())
+        if rc != 0:
+            raise ValueError(f"oracle_attention_bwd failed ({rc})")
+        return dq.reshape(*lead, Sq, D), dk.reshape(*lead, Sk, D), dv.reshape(*lead, Sk, D)
 
     def attention_varlen(self, q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool, scale: float,
                          nthreads: int | None = None, seqs=None):
@@ -263,3 +292,7 @@ def decode(*a, **kw):
 
 def decode_paged(*a, **kw):
     return get().decode_paged(*a, **kw)
+
+
+def attention_bwd(*a, **kw):
+    return get().attention_bwd(*a, **kw)

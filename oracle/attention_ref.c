@@ -35,6 +35,16 @@
  *     and l_g = sum_s e^{m_s - m_g} l_s with O_s unnormalised, the only reading
  *     under which the printed sum equals full attention. LSE = m_g + ln l_g.
  *
+ *   oracle_attention_bwd_head / oracle_attention_bwd
+ *     Gradients of the loss L = sum(O * dO) with respect to Q, K and V for
+ *     O = softmax(scale * Q K^T [+ causal mask]) V ("Adaptive High-Performance
+ *     Attention Kernels in CUDA", Advanced Production Features 2, Custom CUDA
+ *     Backward Pass): S and P are recomputed (here from scratch, in full),
+ *     D_i = sum_k dO_ik O_ik, dS_ij = P_ij (dP_ij - D_i). The page names dS
+ *     and D_i only; the remaining steps are the chain rule of the same
+ *     definition: dV = P^T dO, dP = dO V^T, dQ = scale * dS K,
+ *     dK = scale * dS^T Q.
+ *
  * All arrays are row-major doubles owned by the caller. Return value 0 on
  * success, -1 on a bad argument, -2 on an allocation failure.
  */
@@ -222,4 +232,127 @@ int oracle_splitkv_merge(const double *o_part, const double *m_part, const doubl
     }
     *lse = mg + log(lg);
     return 0;
+}
+
+/* ---- backward pass ------------------------------------------------------ */
+
+/* One head. q, dout: [Sq][D]; k, v: [Sk][D]. Outputs dq: [Sq][D],
+ * dk and dv: [Sk][D]. */
+int oracle_attention_bwd_head(const double *q, const double *k, const double *v,
+                              const double *dout, int Sq, int Sk, int D, int causal,
+                              double scale, double *dq, double *dk, double *dv)
+{
+    if (Sq < 1 || Sk < 1 || D < 1) return -1;
+    double *P = (double *)malloc((size_t)Sq * (size_t)Sk * sizeof(double));
+    double *dS = (double *)malloc((size_t)Sq * (size_t)Sk * sizeof(double));
+    double *o = (double *)malloc((size_t)D * sizeof(double));
+    if (!P || !dS || !o) { free(P); free(dS); free(o); return -2; }
+
+    for (int i = 0; i < Sq; ++i) {
+        double *Pi = P + (size_t)i * Sk;
+        /* S_ij = scale * q_i . k_j, masked; P_i = softmax(S_i) */
+        double m = -INFINITY;
+        for (int j = 0; j < Sk; ++j) {
+            double qk = 0.0;
+            for (int d = 0; d < D; ++d) qk += q[(size_t)i * D + d] * k[(size_t)j * D + d];
+            Pi[j] = (causal && j > i) ? -INFINITY : scale * qk;
+            if (Pi[j] > m) m = Pi[j];
+        }
+        double l = 0.0;
+        for (int j = 0; j < Sk; ++j) {
+            Pi[j] = exp(Pi[j] - m);
+            l += Pi[j];
+        }
+        for (int j = 0; j < Sk; ++j) Pi[j] /= l;
+        /* O_i = sum_j P_ij v_j, then D_i = sum_k dO_ik O_ik */
+        double Di = 0.0;
+        for (int d = 0; d < D; ++d) {
+            double acc = 0.0;
+            for (int j = 0; j < Sk; ++j) acc += Pi[j] * v[(size_t)j * D + d];
+            o[d] = acc;
+            Di += dout[(size_t)i * D + d] * acc;
+        }
+        /* dP_ij = dO_i . v_j, dS_ij = P_ij (dP_ij - D_i) */
+        for (int j = 0; j < Sk; ++j) {
+            double dp = 0.0;
+            for (int d = 0; d < D; ++d) dp += dout[(size_t)i * D + d] * v[(size_t)j * D + d];
+            dS[(size_t)i * Sk + j] = Pi[j] * (dp - Di);
+        }
+    }
+    /* dQ_i = scale * sum_j dS_ij k_j */
+    for (int i = 0; i < Sq; ++i)
+        for (int d = 0; d < D; ++d) {
+            double acc = 0.0;
+            for (int j = 0; j < Sk; ++j) acc += dS[(size_t)i * Sk + j] * k[(size_t)j * D + d];
+            dq[(size_t)i * D + d] = scale * acc;
+        }
+    /* dK_j = scale * sum_i dS_ij q_i, dV_j = sum_i P_ij dO_i */
+    for (int j = 0; j < Sk; ++j)
+        for (int d = 0; d < D; ++d) {
+            double ak = 0.0, av = 0.0;
+            for (int i = 0; i < Sq; ++i) {
+                ak += dS[(size_t)i * Sk + j] * q[(size_t)i * D + d];
+                av += P[(size_t)i * Sk + j] * dout[(size_t)i * D + d];
+            }
+            dk[(size_t)j * D + d] = scale * ak;
+            dv[(size_t)j * D + d] = av;
+        }
+    free(P);
+    free(dS);
+    free(o);
+    return 0;
+}
+
+typedef struct {
+    const double *q, *k, *v, *dout;
+    double *dq, *dk, *dv;
+    int Sq, Sk, D, causal;
+    double scale;
+    int head_begin, head_end;
+    int status;
+} bwd_job;
+
+static void *run_bwd_heads(void *arg)
+{
+    bwd_job *jb = (bwd_job *)arg;
+    jb->status = 0;
+    for (int h = jb->head_begin; h < jb->head_end && jb->status == 0; ++h) {
+        const size_t qo = (size_t)h * jb->Sq * jb->D, ko = (size_t)h * jb->Sk * jb->D;
+        jb->status = oracle_attention_bwd_head(jb->q + qo, jb->k + ko, jb->v + ko, jb->dout + qo,
+                                               jb->Sq, jb->Sk, jb->D, jb->causal, jb->scale,
+                                               jb->dq + qo, jb->dk + ko, jb->dv + ko);
+    }
+    return NULL;
+}
+
+/* q, dout, dq: [BH][Sq][D]; k, v, dk, dv: [BH][Sk][D]. */
+int oracle_attention_bwd(const double *q, const double *k, const double *v, const double *dout,
+                         double *dq, double *dk, double *dv, int BH, int Sq, int Sk, int D,
+                         int causal, double scale, int nthreads)
+{
+    if (BH < 0) return -1;
+    if (BH == 0) return 0;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > BH) nthreads = BH;
+    bwd_job *jobs = (bwd_job *)calloc((size_t)nthreads, sizeof(bwd_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tids) { free(jobs); free(tids); return -2; }
+    for (int t = 0; t < nthreads; ++t) {
+        bwd_job *jb = &jobs[t];
+        jb->q = q; jb->k = k; jb->v = v; jb->dout = dout;
+        jb->dq = dq; jb->dk = dk; jb->dv = dv;
+        jb->Sq = Sq; jb->Sk = Sk; jb->D = D; jb->causal = causal; jb->scale = scale;
+        jb->head_begin = (int)((long long)BH * t / nthreads);
+        jb->head_end = (int)((long long)BH * (t + 1) / nthreads);
+    }
+    int status = 0, started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        if (pthread_create(&tids[t], NULL, run_bwd_heads, &jobs[t]) != 0) { status = -2; break; }
+        ++started;
+    }
+    for (int t = 0; t < started; ++t) pthread_join(tids[t], NULL);
+    for (int t = 0; t < started && status == 0; ++t) status = jobs[t].status;
+    free(jobs);
+    free(tids);
+    return status;
 }

@@ -8,7 +8,9 @@ oracle disagrees with
   * a closed form or invariant of exact attention (rows of P summing to 1,
     a single key, all-equal scores, causal row 0, two keys, score shift,
     permutation equivariance), or
-  * the split-K decoding identity (phase 1 + phase 2 equal full attention).
+  * the split-K decoding identity (phase 1 + phase 2 equal full attention), or
+  * for the backward pass: torch fp64 autograd through SDPA, central finite
+    differences of the oracle's own forward, and gradient invariants.
 tests/test_oracle_mutants.py plants mistakes in copies of the C source and
 checks that every one of them trips at least one pin here.
 """
@@ -266,6 +268,73 @@ def pin_paged_gather(orc):
                what=f"paged LSE seq {b}")
 
 
+def _sdpa_grads(q, k, v, do, causal, scale):
+    q, k, v = (t.clone().requires_grad_() for t in (q, k, v))
+    o = F.scaled_dot_product_attention(q, k, v, is_causal=causal, scale=scale)
+    o.backward(do)
+    return q.grad, k.grad, v.grad
+
+
+def pin_bwd_autograd(orc):
+    """dq, dk, dv against torch fp64 autograd through scaled_dot_product_attention
+    (is_causal = top-left tril mask) on tiny shapes, Sq != Sk included."""
+    seed = 3000
+    for D in (1, 4, 16):
+        for Sq, Sk in ((1, 1), (2, 3), (3, 2), (5, 5), (9, 17), (17, 9)):
+            for causal in (False, True):
+                seed += 1
+                q, do = _rand((2, Sq, D), seed), _rand((2, Sq, D), seed + 1)
+                k, v = _rand((2, Sk, D), seed + 2), _rand((2, Sk, D), seed + 3)
+                scale = 0.25 + 0.1 * (seed % 5)
+                got = orc.attention_bwd(q, k, v, do, causal, scale)
+                ref = _sdpa_grads(q, k, v, do, causal, scale)
+                for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+                    _close(a, b.numpy(), 1e-11, f"{name} D={D} Sq={Sq} Sk={Sk} causal={causal}")
+
+
+def pin_bwd_finite_differences(orc):
+    """Every element of dq, dk, dv equals the central difference of
+    L = sum(O * dO) computed with the oracle's forward (an independent code
+    path), on a tiny case, causal and not."""
+    h = 1e-6
+    for causal in (False, True):
+        q, k, v = _rand((1, 3, 3), 41).numpy(), _rand((1, 4, 3), 42).numpy(), _rand((1, 4, 3), 43).numpy()
+        do = _rand((1, 3, 3), 44).numpy()
+        scale = 0.7
+        grads = orc.attention_bwd(q, k, v, do, causal, scale)
+
+        def loss(qq, kk, vv):
+            return float(np.sum(orc.attention(qq, kk, vv, causal, scale)[0] * do))
+
+        for idx, (x, g) in enumerate(zip((q, k, v), grads)):
+            for pos in np.ndindex(x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[pos] += h
+                xm[pos] -= h
+                args_p = [q, k, v]
+                args_m = [q, k, v]
+                args_p[idx], args_m[idx] = xp, xm
+                fd = (loss(*args_p) - loss(*args_m)) / (2 * h)
+                assert abs(fd - g[pos]) <= 1e-7, f"{'qkv'[idx]}{pos} causal={causal}: fd {fd} vs {g[pos]}"
+
+
+def pin_bwd_invariants(orc):
+    """sum_j dK_j = 0 (every row of dS sums to zero); sum_j dV_j = sum_i dO_i
+    (every row of P sums to one); adding one vector to every key changes no
+    probability, so dQ and dV are unchanged."""
+    for causal in (False, True):
+        q, do = _rand((2, 7, 5), 51), _rand((2, 7, 5), 52)
+        k, v = _rand((2, 9, 5), 53), _rand((2, 9, 5), 54)
+        dq, dk, dv = orc.attention_bwd(q, k, v, do, causal, 0.6)
+        _close(dk.sum(axis=1), np.zeros((2, 5)), 1e-12, f"sum dK causal={causal}")
+        _close(dv.sum(axis=1), do.sum(dim=1).numpy(), 1e-12, f"sum dV causal={causal}")
+        shift = _rand((1, 1, 5), 55)
+        dq2, _, dv2 = orc.attention_bwd(q, k + shift, v, do, causal, 0.6)
+        _close(dq2, dq, 1e-11, f"dq under key shift causal={causal}")
+        _close(dv2, dv, 1e-11, f"dv under key shift causal={causal}")
+
+
 PINS = [pin_sdpa, pin_rows_sum_to_one, pin_single_key, pin_equal_scores, pin_causal_row0,
         pin_two_keys, pin_shift, pin_permutation, pin_rows_subset, pin_partials_definition,
-        pin_merge_identity, pin_varlen_block_diag, pin_paged_gather]
+        pin_merge_identity, pin_varlen_block_diag, pin_paged_gather, pin_bwd_autograd,
+        pin_bwd_finite_differences, pin_bwd_invariants]

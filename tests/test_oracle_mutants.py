@@ -35,6 +35,21 @@ MUTANTS = [
      "acc += 1.0 / lg * o_part[(size_t)s * D + d];"),
     ("merge LSE sign", "*lse = mg + log(lg);", "*lse = mg - log(lg);"),
     ("merge sum unweighted", "lg += exp(m_part[s] - mg) * l_part[s];", "lg += l_part[s];"),
+    ("bwd drops D_i", "dS[(size_t)i * Sk + j] = Pi[j] * (dp - Di);", "dS[(size_t)i * Sk + j] = Pi[j] * dp;"),
+    ("bwd D_i from dO.dO", "Di += dout[(size_t)i * D + d] * acc;",
+     "Di += dout[(size_t)i * D + d] * dout[(size_t)i * D + d];"),
+    ("bwd dP against K", "dp += dout[(size_t)i * D + d] * v[(size_t)j * D + d];",
+     "dp += dout[(size_t)i * D + d] * k[(size_t)j * D + d];"),
+    ("bwd dQ unscaled", "dq[(size_t)i * D + d] = scale * acc;", "dq[(size_t)i * D + d] = acc;"),
+    ("bwd dQ against V", "acc += dS[(size_t)i * Sk + j] * k[(size_t)j * D + d];",
+     "acc += dS[(size_t)i * Sk + j] * v[(size_t)j * D + d];"),
+    ("bwd dK from P", "ak += dS[(size_t)i * Sk + j] * q[(size_t)i * D + d];",
+     "ak += P[(size_t)i * Sk + j] * q[(size_t)i * D + d];"),
+    ("bwd dV from dS", "av += P[(size_t)i * Sk + j] * dout[(size_t)i * D + d];",
+     "av += dS[(size_t)i * Sk + j] * dout[(size_t)i * D + d];"),
+    ("bwd mask direction", "Pi[j] = (causal && j > i) ? -INFINITY : scale * qk;",
+     "Pi[j] = (causal && j < i) ? -INFINITY : scale * qk;"),
+    ("bwd softmax unnormalised", "for (int j = 0; j < Sk; ++j) Pi[j] /= l;", "for (int j = 0; j < Sk; ++j) Pi[j] /= 1.0;"),
 ]
 
 

@@ -392,6 +392,7 @@ def run_gpu(args, rank, world, local):
     decode_gbs = world * dc_bytes * K / (dc_sum * 1e-3) / 1e9
     two = run_two_launch(args, fa, torch, stream, flush, world, (dq, dk, dv), ws, do, dlse, wd)
     d256 = run_d256(args, fa, torch, stream, dev, flush, world)
+    bwd = run_bwd(args, fa, torch, stream, dev, flush, world, (q, k, v), o, lse, wp)
     paged = run_paged(args, fa, torch, stream, dev, flush, world)
     # end-to-end through host buffers (pinned), copies inside the timed region
     e2e = ({"prefill": None, "decode": None} if args.no_e2e else
@@ -428,6 +429,7 @@ def run_gpu(args, rank, world, local):
         "e2e": e2e["prefill"],
         "paged_decode": paged,
         "d256_prefill": d256,
+        "backward": bwd,
         "gpu_launches": 2 * K,
         "clocks": clock,
         "wall_ms_per_step": 1e3 * wall / K,
@@ -469,6 +471,43 @@ def run_two_launch(args, fa, torch, stream, flush, world, dec, ws, o, lse, wd):
             "frac_of_hbm": gbs / peaks["hbm_gbs"], "split_only_gbs": world * nbytes / (sp * 1e-3) / 1e9,
             "traffic_split": committed_traffic().get("fa_decode_split_kernel"),
             "traffic_merge": committed_traffic().get("fa_splitkv_merge_kernel")}
+
+
+def run_bwd(args, fa, torch, stream, dev, flush, world, qkv, o, lse, wp):
+    """Backward pass on the prefill workload (causal LLaMA-7B shape, bf16),
+    dO seeded like the inputs; the three launches of fa_bwd timed together
+    on their own loop with the same L2 flush. FLOPs: 2.5x the forward's (five
+    products of the same size instead of two), causal at half."""
+    from exact_attention_54_gb300 import inputs
+    from exact_attention_54_gb300.metrics import attention_flops
+    q, k, v = qkv
+    fa.fa_fwd(q, k, v, o, lse, wp.causal, wp.scale, stream)
+    do = inputs.make_dense(wp.B, wp.H, wp.Sq, wp.Sq, wp.D, wp.dtype, seed=wp.seed + 100)[0].to(dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(wp.B, wp.H, wp.Sq, wp.D) // 4, dtype=torch.float32, device=dev)
+    n = max(1, min(args.steps, 300))
+
+    def step(evs=None):
+        flush.fill_(float(1.0))
+        if evs:
+            evs[0].record(stream)
+        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, wp.causal, wp.scale, stream)
+        if evs:
+            evs[1].record(stream)
+
+    for _ in range(3):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        step(evs[i])
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    ms = aggregate_max([sum(e[0].elapsed_time(e[1]) for e in evs) / n], world)[0]
+    flops = 2.5 * attention_flops(wp.B, wp.H, wp.Sq, wp.Sk, wp.D, wp.causal)
+    peaks, _ = load_peaks()
+    tf = world * flops / (ms * 1e-3) / 1e12
+    return {"workload": wp.name, "value": tf, "unit": "TFLOPS", "ms_per_call": ms, "steps": n,
+            "launches_per_call": 3, "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "per_call_flops": flops}
 
 
 def run_d256(args, fa, torch, stream, dev, flush, world):

@@ -21,8 +21,10 @@ import threading
 import torch
 
 __all__ = ["FAError", "fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_decode_paged_splitkv", "fa_splitkv_merge",
-           "fa_decode_splitkv_fused", "fa_decode_paged_splitkv_fused", "fa_check_device_error", "fa_status_string", "flash_attention", "flash_attention_varlen",
-           "flash_decode", "flash_decode_paged", "library_path", "load_library", "EXPORTED_SYMBOLS"]
+           "fa_decode_splitkv_fused", "fa_decode_paged_splitkv_fused", "fa_bwd", "fa_bwd_workspace_bytes",
+           "fa_check_device_error", "fa_status_string", "flash_attention", "flash_attention_varlen",
+           "flash_attention_bwd", "flash_decode", "flash_decode_paged", "library_path", "load_library",
+           "EXPORTED_SYMBOLS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libfa.so")
@@ -32,8 +34,8 @@ _lib = None
 FA_FP16, FA_BF16 = 0, 1
 FA_MAX_SPLITS = 1024
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_decode_paged_splitkv", "fa_splitkv_merge",
-                    "fa_decode_splitkv_fused", "fa_decode_paged_splitkv_fused", "fa_check_device_error",
-                    "fa_status_string", "fa_version")
+                    "fa_decode_splitkv_fused", "fa_decode_paged_splitkv_fused", "fa_bwd", "fa_bwd_workspace_bytes",
+                    "fa_check_device_error", "fa_status_string", "fa_version")
 
 
 class FAError(RuntimeError):
@@ -67,6 +69,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.fa_decode_splitkv_fused.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         lib.fa_decode_paged_splitkv_fused.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i,
                                                       f, i, vp]
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, i, f, i, vp]
+        lib.fa_bwd.restype = ctypes.c_int
+        lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
+        lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_check_device_error.argtypes = [vp]
         lib.fa_status_string.argtypes = [i]
         lib.fa_status_string.restype = ctypes.c_char_p
@@ -217,6 +223,24 @@ def fa_decode_paged_splitkv_fused(q, k_cache, v_cache, block_table, seq_lens, o,
     _check("fa_decode_paged_splitkv_fused", st)
 
 
+def fa_bwd_workspace_bytes(B: int, H: int, Sq: int, D: int) -> int:
+    return int(load_library().fa_bwd_workspace_bytes(B, H, Sq, D))
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal: bool, scale: float | None = None, stream=None):
+    """Backward pass: q, o, dout, dq [B,H,Sq,D]; k, v, dk, dv [B,H,Sk,D];
+    lse [B,H,Sq] fp32 from the forward; workspace a CUDA tensor of at least
+    fa_bwd_workspace_bytes(B, H, Sq, D) bytes."""
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    _need_contig(q, k, v, o, dout, lse, dq, dk, dv, workspace)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    st = load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                               _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(), B, H, Sq,
+                               Sk, D, int(bool(causal)), float(scale), _dtype_code(q), _stream(stream))
+    _check("fa_bwd", st)
+
+
 def fa_check_device_error(stream=None):
     """Synchronise the stream and raise if a kernel abandoned a barrier wait."""
     _check("fa_check_device_error", load_library().fa_check_device_error(_stream(stream)))
@@ -231,6 +255,18 @@ def flash_attention(q, k, v, causal: bool = False, scale: float | None = None, s
     lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
     fa_fwd(q, k, v, o, lse, causal, scale, stream)
     return o, lse
+
+
+def flash_attention_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, stream=None,
+                        workspace=None):
+    """Returns (dq, dk, dv) for dense [B,H,S,D] CUDA tensors, given the
+    forward's o and lse."""
+    B, H, Sq, D = q.shape
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_bytes(B, H, Sq, D) // 4, dtype=torch.float32, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal, scale, stream)
+    return dq, dk, dv
 
 
 def flash_attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal: bool = False,

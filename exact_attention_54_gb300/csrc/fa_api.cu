@@ -109,6 +109,7 @@ const char *fa_status_string(fa_status_t s) {
         case FA_ERR_DEVICE_TIMEOUT: return "a kernel abandoned a barrier wait (device timeout)";
         case FA_ERR_SCRATCH: return "problem larger than the built-in decode scratch";
         case FA_ERR_DEVICE_INDEX: return "a kernel met an out-of-range block-table entry";
+        case FA_ERR_WORKSPACE: return "workspace smaller than fa_bwd_workspace_bytes()";
     }
     return "unknown status";
 }
@@ -355,6 +356,64 @@ fa_status_t fa_decode_paged_splitkv_fused(const void *q, const void *k_cache, co
     p.counters = counters;
     const cudaError_t e = fa::launch_decode_fused(D, dtype == FA_BF16, true, p, static_cast<int>(BH),
                                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int Sq, int D) {
+    if (B < 1 || H < 1 || Sq < 1 || Sq > kMaxLen || (D != 64 && D != 128)) return 0;
+    const long long BH = static_cast<long long>(B) * H;
+    if (BH > INT_MAX) return 0;
+    const long long pad = (static_cast<long long>(Sq) + 127) / 128 * 128;
+    return static_cast<size_t>(BH * Sq * D + 2 * BH * pad) * sizeof(float);
+}
+
+fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse,
+                   void *dq, void *dk, void *dv, float *workspace, size_t workspace_bytes, int B, int H, int Sq,
+                   int Sk, int D, int causal, float scale, fa_dtype_t dtype, void *stream) {
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return FA_ERR_NULL;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+    if (D != 64 && D != 128) return FA_ERR_HEADDIM;
+    if (B < 1 || H < 1 || Sq < 1 || Sk < 1 || Sq > kMaxLen || Sk > kMaxLen) return FA_ERR_SHAPE;
+    const long long BH = static_cast<long long>(B) * H;
+    const long long n_kt = (Sk + 127) / 128;
+    if (BH > INT_MAX || BH * n_kt > INT_MAX) return FA_ERR_SHAPE;
+    if (!scale_ok(scale)) return FA_ERR_SCALE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned4(lse) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+        return FA_ERR_ALIGN;
+    const size_t need = fa_bwd_workspace_bytes(B, H, Sq, D);
+    if (need == 0) return FA_ERR_SHAPE;
+    if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+
+    const bool bf16 = dtype == FA_BF16;
+    CUtensorMap maps[4];
+    const uint64_t row = static_cast<uint64_t>(D) * 2;
+    if (!encode_map(&maps[0], bf16, q, D, Sq, BH, row, row * Sq, 128, 1) ||
+        !encode_map(&maps[1], bf16, k, D, Sk, BH, row, row * Sk, 128, 1) ||
+        !encode_map(&maps[2], bf16, v, D, Sk, BH, row, row * Sk, 128, 1) ||
+        !encode_map(&maps[3], bf16, dout, D, Sq, BH, row, row * Sq, 128, 1))
+        return FA_ERR_CUDA;
+    int *err = device_error_word();
+    if (err == nullptr) return FA_ERR_CUDA;
+
+    fa::BwdParams p{};
+    p.BH = static_cast<int>(BH);
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.n_qtiles = (Sq + 127) / 128;
+    p.n_ktiles = static_cast<int>(n_kt);
+    p.Sq_pad = p.n_qtiles * 128;
+    p.dq_acc = workspace;
+    p.lse2 = workspace + static_cast<size_t>(BH) * Sq * D;
+    p.delta = p.lse2 + static_cast<size_t>(BH) * p.Sq_pad;
+    p.dk = dk;
+    p.dv = dv;
+    p.scale = scale;
+    p.scale_log2 = scale * kLog2e;
+    p.err = err;
+    p.timeout_ns = fa::kWaitTimeoutNs;
+    const cudaError_t e = fa::launch_bwd(D, bf16, causal != 0, maps, o, dout, lse, dq, p,
+                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -1,0 +1,472 @@
+// FlashAttention-2 backward pass on sm_103a.
+//
+// Method ("Adaptive High-Performance Attention Kernels in CUDA", Advanced
+// Production Features 2, Custom CUDA Backward Pass): the N x N probability
+// matrix is never stored. S = scale Q K^T and P = exp(S - LSE) are recomputed
+// tile by tile from the forward pass's per-row LSE, D_i = sum_k dO_ik O_ik is
+// precomputed, and dS = P (dP - D_i) with dP = dO V^T. The gradients follow by
+// the chain rule: dV = P^T dO, dK = scale dS^T Q, dQ = scale dS K.
+//
+// Three launches:
+//   fa_bwd_prep_kernel  per query row: D_i, the LSE in base 2 (padded to whole
+//                       128-row tiles with +inf, which zeroes P there), and a
+//                       zeroed fp32 dQ accumulator row.
+//   fa_bwd_kernel       one CTA per (head, 128-key tile), looping over the
+//                       query tiles that see those keys (causal: from the
+//                       diagonal on). Per query tile, on the tensor core:
+//                         S^T  = K Q^T     (TMEM, lanes = keys)
+//                         dP^T = V dO^T    (TMEM)
+//                       the key-row warps turn them into P^T (16-bit, back into
+//                       TMEM over S^T) and dS^T (16-bit, shared memory, in the
+//                       128-byte-swizzled layout a TMA load would produce), then
+//                         dV  += P^T dO    (P^T from TMEM, dO MN-major)
+//                         dK  += dS^T Q    (dS^T K-major, Q MN-major)
+//                         dQ_t = dS K      (dS^T read as an MN-major A operand)
+//                       and the query-row warps add dQ_t into the fp32
+//                       accumulator with vector reductions. dK and dV stay in
+//                       TMEM for the whole loop and are written once.
+//   fa_bwd_dq_kernel    dQ = scale * accumulator, in the input dtype.
+//
+// Roles of fa_bwd_kernel (384 threads): warp 0 TMA producer (K, V once; Q and
+// dO double-buffered), warp 1 MMA issuer and TMEM owner, warps 4..7 one key
+// row per thread (P^T, dS^T, then the dK/dV epilogue), warps 8..11 one query
+// row per thread (dQ reduction). TMEM columns: S^T [0,128), dP^T and then dQ_t
+// [128,256), dV [256, 256+D), dK [256+D, 256+2D).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include <cstdint>
+
+#include "fa_launch.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace bwd {
+
+constexpr int kBlock = 128;  // keys per work item and queries per inner step
+constexpr int kThreads = 384;
+
+template <int D>
+struct Shape {
+    static_assert(D == 64 || D == 128, "head dim");
+    static constexpr int kColBlocks = D / 64;
+    static constexpr int kBoxBytes = 128 * 128;         // 128 rows x 64 columns of 16-bit values
+    static constexpr int kTileBytes = kBlock * D * 2;   // one 128-row tile of Q, K, V or dO
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kOffK + kTileBytes;
+    static constexpr int kOffQ = kOffV + kTileBytes;    // + s * tile, s = 0, 1
+    static constexpr int kOffDO = kOffQ + 2 * kTileBytes;
+    static constexpr int kOffDS = kOffDO + 2 * kTileBytes;  // dS^T [128 keys][128 queries], 2 boxes
+    static constexpr int kOffBar = kOffDS + 2 * kBoxBytes;
+    static constexpr int kKVFull = 0;
+    static constexpr int kQFull = 1;    // +s
+    static constexpr int kQEmpty = 3;   // +s
+    static constexpr int kSFull = 5;    // S^T and dP^T written (MMA commit)
+    static constexpr int kPFull = 6;    // P^T in TMEM and dS^T in shared memory (4 warps)
+    static constexpr int kDQFull = 7;   // dQ_t in TMEM; dS^T no longer read (MMA commit)
+    static constexpr int kDQFree = 8;   // dQ_t read out (4 warps)
+    static constexpr int kTeardown = 9;
+    static constexpr int kNumBars = 10;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
+    static constexpr uint32_t kTmemS = 0;
+    static constexpr uint32_t kTmemDP = 128;
+    static constexpr uint32_t kTmemDV = 256;
+    static constexpr uint32_t kTmemDK = 256 + D;
+    static constexpr uint32_t kTmemCols = 512;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+template <bool BF16>
+__device__ __forceinline__ float to_f32(uint16_t x) {
+    if constexpr (BF16) return __uint_as_float(static_cast<uint32_t>(x) << 16);
+    else return __half2float(__ushort_as_half(x));
+}
+
+// ------------------------------------------------------------- preprocess --
+
+// One warp per (head, padded row): D_i = sum_d dO_id O_id, LSE in base 2, and
+// the zeroed dQ accumulator row. Rows past Sq get D = 0 and LSE = +inf.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256)
+    fa_bwd_prep_kernel(const uint16_t *__restrict__ o, const uint16_t *__restrict__ dout,
+                       const float *__restrict__ lse, const BwdParams p) {
+    constexpr int E = D / 32;  // elements per lane
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;
+    if (row >= static_cast<long long>(p.BH) * p.Sq_pad) return;
+    const int bh = static_cast<int>(row / p.Sq_pad);
+    const int r = static_cast<int>(row % p.Sq_pad);
+    const size_t srow = static_cast<size_t>(bh) * p.Sq_pad + r;
+    if (r >= p.Sq) {
+        if (lane == 0) {
+            p.delta[srow] = 0.f;
+            p.lse2[srow] = CUDART_INF_F;
+        }
+        return;
+    }
+    const size_t off = (static_cast<size_t>(bh) * p.Sq + r) * D + lane * E;
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc = fmaf(to_f32<BF16>(o[off + e]), to_f32<BF16>(dout[off + e]), acc);
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+#pragma unroll
+    for (int e = 0; e < E; ++e) p.dq_acc[off + e] = 0.f;
+    if (lane == 0) {
+        p.delta[srow] = acc;
+        p.lse2[srow] = lse[static_cast<size_t>(bh) * p.Sq + r] * 1.4426950408889634f;
+    }
+}
+
+// ------------------------------------------------------------ postprocess --
+
+template <bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float *__restrict__ acc, uint16_t *__restrict__ dq,
+                                                        long long n8, float scale) {
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n8) return;
+    const float4 a = reinterpret_cast<const float4 *>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4 *>(acc)[2 * i + 1];
+    uint4 out;
+    out.x = ptx::pack2<BF16>(a.x * scale, a.y * scale);
+    out.y = ptx::pack2<BF16>(a.z * scale, a.w * scale);
+    out.z = ptx::pack2<BF16>(b.x * scale, b.y * scale);
+    out.w = ptx::pack2<BF16>(b.z * scale, b.w * scale);
+    reinterpret_cast<uint4 *>(dq)[i] = out;
+}
+
+// ------------------------------------------------------------ main kernel --
+
+__device__ __forceinline__ void red_add4(float *dst, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// 128 rows starting at `row0` of head `bh`, all 64-column boxes, into `dst`.
+template <int D>
+__device__ __forceinline__ void load_tile(const CUtensorMap *tm, uint32_t dst, uint32_t bar, int row0, int bh) {
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) ptx::tma_load_3d(dst + c * Shape<D>::kBoxBytes, tm, bar, c * 64, row0, bh);
+}
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const BwdParams p) {
+    using S = Shape<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = ptx::smem_addr(smem);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kOffMisc + 4);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t bars = sbase + S::kOffBar;
+    auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+    auto wait = [&](int i, uint32_t parity) {
+        return __all_sync(0xffffffffu, ptx::bar_wait(bar(i), parity, abort_flag, p.timeout_ns));
+    };
+
+    // work item: key tile kt of head bh; heavy causal tiles (small kt) first
+    const int kt = static_cast<int>(blockIdx.x) / p.BH;
+    const int bh = static_cast<int>(blockIdx.x) % p.BH;
+    const int k0 = kt * kBlock;
+    const int qt0 = CAUSAL ? kt : 0;  // first query tile that sees any of these keys
+    const int n = p.n_qtiles > qt0 ? p.n_qtiles - qt0 : 0;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S::kNumBars; ++i)
+            ptx::bar_init(bar(i), (i == S::kPFull || i == S::kDQFree) ? kBlock / 32 : 1u);
+        *abort_flag = 0;
+        ptx::bar_init_fence();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tm_q);
+        ptx::prefetch_tmap(&tm_k);
+        ptx::prefetch_tmap(&tm_v);
+        ptx::prefetch_tmap(&tm_do);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), S::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && n > 0) {
+        // ---- TMA producer ----
+        const bool leader = ptx::elect_one();
+        if (leader) {
+            ptx::bar_arrive_expect_tx(bar(S::kKVFull), 2 * S::kTileBytes);
+            load_tile<D>(&tm_k, sbase + S::kOffK, bar(S::kKVFull), k0, bh);
+            load_tile<D>(&tm_v, sbase + S::kOffV, bar(S::kKVFull), k0, bh);
+        }
+        int it = 0;
+        for (; it < n; ++it) {
+            const int s = it & 1;
+            if (it >= 2 && !wait(S::kQEmpty + s, ((it >> 1) - 1) & 1)) break;
+            if (leader) {
+                const int q0 = (qt0 + it) * kBlock;
+                ptx::bar_arrive_expect_tx(bar(S::kQFull + s), 2 * S::kTileBytes);
+                load_tile<D>(&tm_q, sbase + S::kOffQ + s * S::kTileBytes, bar(S::kQFull + s), q0, bh);
+                load_tile<D>(&tm_do, sbase + S::kOffDO + s * S::kTileBytes, bar(S::kQFull + s), q0, bh);
+            }
+        }
+        // never leave with copies in flight
+        ptx::bar_wait(bar(S::kKVFull), 0, nullptr, p.timeout_ns);
+        for (int s = 0; s < 2 && s < it; ++s) {
+            const int last = (it - 1) - ((it - 1 - s) % 2);
+            ptx::bar_wait(bar(S::kQFull + s), (last >> 1) & 1, nullptr, p.timeout_ns);
+        }
+    } else if (warp == 1 && n > 0) {
+        // ---- MMA issuer ----
+        const bool leader = ptx::elect_one();
+        constexpr uint32_t kIdS = ptx::idesc_f16(BF16, kBlock, kBlock, false);    // S^T, dP^T
+        constexpr uint32_t kIdKV = ptx::idesc_f16(BF16, kBlock, D, true);         // dV, dK: B MN-major
+        constexpr uint32_t kIdQ = ptx::idesc_f16(BF16, kBlock, D, true, true);    // dQ: A and B MN-major
+        constexpr uint64_t kBox16 = S::kBoxBytes >> 4, kTile16 = S::kTileBytes >> 4, kRows16 = 2048 >> 4;
+        const uint64_t k_kmaj = ptx::smem_desc_sw128(sbase + S::kOffK, 16, 1024);
+        const uint64_t v_kmaj = ptx::smem_desc_sw128(sbase + S::kOffV, 16, 1024);
+        const uint64_t q_kmaj = ptx::smem_desc_sw128(sbase + S::kOffQ, 16, 1024);
+        const uint64_t do_kmaj = ptx::smem_desc_sw128(sbase + S::kOffDO, 16, 1024);
+        const uint64_t q_mn = ptx::smem_desc_sw128(sbase + S::kOffQ, S::kBoxBytes, 1024);
+        const uint64_t do_mn = ptx::smem_desc_sw128(sbase + S::kOffDO, S::kBoxBytes, 1024);
+        const uint64_t k_mn = ptx::smem_desc_sw128(sbase + S::kOffK, S::kBoxBytes, 1024);
+        const uint64_t ds_kmaj = ptx::smem_desc_sw128(sbase + S::kOffDS, 16, 1024);
+        const uint64_t ds_mn = ptx::smem_desc_sw128(sbase + S::kOffDS, S::kBoxBytes, 1024);
+        bool ok = wait(S::kKVFull, 0);
+        for (int it = 0; it < n && ok; ++it) {
+            const int s = it & 1;
+            if (!(ok = wait(S::kQFull + s, (it >> 1) & 1))) break;
+            const uint64_t st = static_cast<uint64_t>(s) * kTile16;
+            // S^T = K Q^T into [0,128): the previous P^T was consumed by the
+            // dV MMA issued before this one.
+            if (leader) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = (kk / 4) * kBox16 + (kk % 4) * 2;
+                    ptx::mma_ss(tmem + S::kTmemS, k_kmaj + off, q_kmaj + st + off, kIdS, kk > 0);
+                }
+            }
+            // dP^T = V dO^T into [128,256), once the last dQ_t there is read
+            if (it > 0 && !(ok = wait(S::kDQFree, (it - 1) & 1))) break;
+            ptx::tc_fence_after();
+            if (leader) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = (kk / 4) * kBox16 + (kk % 4) * 2;
+                    ptx::mma_ss(tmem + S::kTmemDP, v_kmaj + off, do_kmaj + st + off, kIdS, kk > 0);
+                }
+                ptx::mma_commit(bar(S::kSFull));
+            }
+            if (!(ok = wait(S::kPFull, it & 1))) break;
+            ptx::tc_fence_after();
+            if (leader) {
+                // dV += P^T dO: 8 MMAs over the 128 queries, P^T from TMEM
+#pragma unroll
+                for (int kk = 0; kk < kBlock / 16; ++kk)
+                    ptx::mma_ts(tmem + S::kTmemDV, tmem + S::kTmemS + kk * 8, do_mn + st + kk * kRows16, kIdKV,
+                                (it > 0 || kk > 0) ? 1u : 0u);
+                // dK += dS^T Q
+#pragma unroll
+                for (int kk = 0; kk < kBlock / 16; ++kk) {
+                    const uint64_t off = (kk / 4) * kBox16 + (kk % 4) * 2;
+                    ptx::mma_ss(tmem + S::kTmemDK, ds_kmaj + off, q_mn + st + kk * kRows16, kIdKV,
+                                (it > 0 || kk > 0) ? 1u : 0u);
+                }
+                ptx::mma_commit(bar(S::kQEmpty + s));  // Q and dO of this step have all their readers
+                // dQ_t = dS K into [128,256) (dP^T there was consumed by the softmax warps)
+#pragma unroll
+                for (int kk = 0; kk < kBlock / 16; ++kk)
+                    ptx::mma_ss(tmem + S::kTmemDP, ds_mn + kk * kRows16, k_mn + kk * kRows16, kIdQ, kk > 0);
+                ptx::mma_commit(bar(S::kDQFull));
+            }
+        }
+        if (leader) ptx::mma_commit(bar(S::kTeardown));
+        __syncwarp();
+        ptx::bar_wait(bar(S::kTeardown), 0, nullptr, p.timeout_ns);
+    } else if (warp >= 4 && warp < 8) {
+        // ---- key rows: P^T, dS^T; then dK, dV ----
+        const int wq = warp - 4;
+        const int r = wq * 32 + lane;  // key row within the tile
+        const int key = k0 + r;
+        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t ds_row = sbase + S::kOffDS + (r >> 3) * 1024 + (r & 7) * 128;
+        const float *lse2 = p.lse2 + static_cast<size_t>(bh) * p.Sq_pad;
+        const float *delta = p.delta + static_cast<size_t>(bh) * p.Sq_pad;
+        bool ok = true;
+        for (int it = 0; it < n; ++it) {
+            if (!(ok = wait(S::kSFull, it & 1))) break;
+            if (it > 0 && !(ok = wait(S::kDQFull, (it - 1) & 1))) break;  // dS^T buffer free again
+            ptx::tc_fence_after();
+            const int q0 = (qt0 + it) * kBlock;
+#pragma unroll 1
+            for (int c = 0; c < kBlock / 32; ++c) {
+                uint32_t sv[32], dpv[32];
+                ptx::tmem_ld32(tmem + lane_base + S::kTmemS + 32 * c, sv);
+                ptx::tmem_ld32(tmem + lane_base + S::kTmemDP + 32 * c, dpv);
+                float l2[32], dl[32];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const float4 a = __ldg(reinterpret_cast<const float4 *>(lse2 + q0 + 32 * c) + m);
+                    const float4 b = __ldg(reinterpret_cast<const float4 *>(delta + q0 + 32 * c) + m);
+                    l2[4 * m] = a.x, l2[4 * m + 1] = a.y, l2[4 * m + 2] = a.z, l2[4 * m + 3] = a.w;
+                    dl[4 * m] = b.x, dl[4 * m + 1] = b.y, dl[4 * m + 2] = b.z, dl[4 * m + 3] = b.w;
+                }
+                ptx::tmem_ld_wait();
+                ptx::reg_fence(sv);
+                ptx::reg_fence(dpv);
+                const int qc = q0 + 32 * c;
+                const bool need_mask = (CAUSAL && key > qc) || key >= p.Sk;
+                uint32_t pp[16], dd[16];
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    float e[2], g[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        float pv = ptx::ex2(fmaf(__uint_as_float(sv[j + u]), p.scale_log2, -l2[j + u]));
+                        if (need_mask && ((CAUSAL && key > qc + j + u) || key >= p.Sk)) pv = 0.f;
+                        e[u] = pv;
+                        g[u] = pv * (__uint_as_float(dpv[j + u]) - dl[j + u]);
+                    }
+                    pp[j / 2] = ptx::pack2<BF16>(e[0], e[1]);
+                    dd[j / 2] = ptx::pack2<BF16>(g[0], g[1]);
+                }
+                // P^T over S^T columns [16c, 16c+16): those hold queries already read
+                ptx::tmem_st16(tmem + lane_base + S::kTmemS + 16 * c, pp);
+                // dS^T row r, queries [32c, 32c+32): box c/2, 16-byte chunks 4(c%2)..+3, 128-byte swizzle
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const uint32_t chunk = static_cast<uint32_t>(((c & 1) * 4 + m) ^ (r & 7));
+                    st_shared_v4(ds_row + (c >> 1) * S::kBoxBytes + chunk * 16, dd[4 * m], dd[4 * m + 1],
+                                 dd[4 * m + 2], dd[4 * m + 3]);
+                }
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::fence_proxy_async_smem();  // dS^T is read by the tensor core next
+            __syncwarp();
+            if (lane == 0) ptx::bar_arrive(bar(S::kPFull));
+        }
+        // epilogue: dV and scale * dK rows of this key tile
+        if (ok && n > 0) {
+            ok = wait(S::kDQFull, (n - 1) & 1);  // the last MMAs of the loop are done
+            ptx::tc_fence_after();
+        }
+        // The TMEM loads are warp-collective (.sync.aligned): every lane runs
+        // them; only the global stores are limited to keys that exist.
+        if (ok) {
+            const bool row_valid = key < p.Sk;
+            uint16_t *dvr = static_cast<uint16_t *>(p.dv) + (static_cast<size_t>(bh) * p.Sk + key) * D;
+            uint16_t *dkr = static_cast<uint16_t *>(p.dk) + (static_cast<size_t>(bh) * p.Sk + key) * D;
+#pragma unroll 1
+            for (int t = 0; t < 2; ++t) {
+                const float f = t == 0 ? 1.f : p.scale;
+                uint16_t *dst = t == 0 ? dvr : dkr;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    if (n > 0) {
+                        ptx::tmem_ld32(tmem + lane_base + (t == 0 ? S::kTmemDV : S::kTmemDK) + 32 * c, v);
+                        ptx::tmem_ld_wait();
+                        ptx::reg_fence(v);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) v[k] = 0u;
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        pk[k] = ptx::pack2<BF16>(__uint_as_float(v[2 * k]) * f, __uint_as_float(v[2 * k + 1]) * f);
+                    if (row_valid) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                    }
+                }
+            }
+        }
+    } else if (warp >= 8) {
+        // ---- query rows: dQ_t into the fp32 accumulator ----
+        const int wq = warp - 8;
+        const int r = wq * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+        for (int it = 0; it < n; ++it) {
+            if (!wait(S::kDQFull, it & 1)) break;
+            ptx::tc_fence_after();
+            const int query = (qt0 + it) * kBlock + r;
+            float *dst = p.dq_acc + (static_cast<size_t>(bh) * p.Sq + query) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                ptx::tmem_ld32(tmem + lane_base + S::kTmemDP + 32 * c, v);
+                ptx::tmem_ld_wait();
+                ptx::reg_fence(v);
+                if (query < p.Sq) {
+#pragma unroll
+                    for (int m = 0; m < 8; ++m)
+                        red_add4(dst + 32 * c + 4 * m, __uint_as_float(v[4 * m]), __uint_as_float(v[4 * m + 1]),
+                                 __uint_as_float(v[4 * m + 2]), __uint_as_float(v[4 * m + 3]));
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::bar_arrive(bar(S::kDQFree));
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, S::kTmemCols);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicExch(p.err, kDeviceErrTimeout);
+}
+
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_t(const CUtensorMap *maps, const void *o, const void *dout, const float *lse, void *dq,
+                     const BwdParams &p, cudaStream_t st) {
+    const long long rows = static_cast<long long>(p.BH) * p.Sq_pad;
+    fa_bwd_prep_kernel<D, BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+        static_cast<const uint16_t *>(o), static_cast<const uint16_t *>(dout), lse, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    auto kern = fa_bwd_kernel<D, BF16, CAUSAL>;
+    constexpr int kSmem = Shape<D>::kSmemBytes;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    kern<<<static_cast<unsigned>(p.BH * p.n_ktiles), kThreads, kSmem, st>>>(maps[0], maps[1], maps[2], maps[3], p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long n8 = static_cast<long long>(p.BH) * p.Sq * D / 8;
+    fa_bwd_dq_kernel<BF16><<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, st>>>(
+        p.dq_acc, static_cast<uint16_t *>(dq), n8, p.scale);
+    return cudaGetLastError();
+}
+
+}  // namespace bwd
+
+cudaError_t launch_bwd(int D, bool bf16, bool causal, const CUtensorMap *maps, const void *o, const void *dout,
+                       const float *lse, void *dq, const BwdParams &p, cudaStream_t stream) {
+#define FA_BWD(DD, BB, CC) \
+    if (D == DD && bf16 == BB && causal == CC) return bwd::launch_t<DD, BB, CC>(maps, o, dout, lse, dq, p, stream);
+    FA_BWD(64, false, false) FA_BWD(64, false, true) FA_BWD(64, true, false) FA_BWD(64, true, true)
+    FA_BWD(128, false, false) FA_BWD(128, false, true) FA_BWD(128, true, false) FA_BWD(128, true, true)
+#undef FA_BWD
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

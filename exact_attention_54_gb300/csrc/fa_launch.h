@@ -57,6 +57,24 @@ struct DecodeParams {
     int *counters;               // fused: [B*H] finished partitions per head, zero between calls
 };
 
+// Parameters of the backward pass (dense [B,H,S,D] layout).
+struct BwdParams {
+    float *lse2;           // [B*H][Sq_pad] forward LSE * log2(e); +inf past Sq
+    float *delta;          // [B*H][Sq_pad] D_i = sum_d dO_id O_id; 0 past Sq
+    float *dq_acc;         // [B*H][Sq][D] fp32 accumulator of dS K
+    void *dk, *dv;         // [B*H][Sk][D] outputs (input dtype)
+    int BH, Sq, Sk;
+    int Sq_pad;            // Sq rounded up to whole 128-row tiles
+    int n_qtiles, n_ktiles;
+    float scale, scale_log2;
+    int *err;              // device error word
+    unsigned long long timeout_ns;
+};
+
+// maps: {Q, K, V, dO}; lse [B*H][Sq]; dq output (input dtype).
+cudaError_t launch_bwd(int D, bool bf16, bool causal, const CUtensorMap *maps, const void *o, const void *dout,
+                       const float *lse, void *dq, const BwdParams &p, cudaStream_t stream);
+
 // maps: {Q, K, V} tensor maps (see fa_api.cu for their geometry).
 cudaError_t launch_fwd_dense(int D, bool bf16, bool causal, const CUtensorMap *maps,
                              const FwdParams &p, int grid, cudaStream_t stream);

@@ -5,6 +5,10 @@
 //                        swizzle) + tcgen05.mma with two K-major smem operands
 //   fa_selftest_pv       C[128xD] = P[128x128] V[128xD]: P written to TMEM
 //                        with tcgen05.st, V MN-major from smem (TS form)
+//   fa_selftest_tn       C[128xD] = X^T Y for X [128x128], Y [128xD]: X is loaded
+//                        like any 128-row tile and read by the MMA as an
+//                        MN-major A operand (the backward pass's dQ = dS K
+//                        reads dS^T this way), Y as an MN-major B operand
 //   fa_selftest_watchdog a bounded wait on a barrier nobody arrives at; the
 //                        kernel must give up, release TMEM and report it
 // Each kernel writes 0 (done) or 1 (a wait timed out) to *status.
@@ -183,6 +187,71 @@ __global__ void __launch_bounds__(128, 1)
     if (threadIdx.x == 0) *status = *abort_flag ? 1 : 0;
 }
 
+// C = X^T Y: 8 MMAs of K = 16 (rows of X and Y), both operands MN-major.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(128, 1)
+    st_tn_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap ty, float *c, int *status,
+                 unsigned long long timeout_ns) {
+    constexpr int kBox = 128 * 128;
+    constexpr int kOffX = 0, kOffY = 2 * kBox, kOffBar = kOffY + (D / 64) * kBox;
+    extern __shared__ uint8_t raw[];
+    uint8_t *smem = align1024(raw);
+    const uint32_t sb = ptx::smem_addr(smem);
+    const uint32_t bar_load = sb + kOffBar, bar_mma = bar_load + 8;
+    uint32_t *slot = reinterpret_cast<uint32_t *>(smem + kOffBar + 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffBar + 20);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        ptx::bar_init(bar_load, 1);
+        ptx::bar_init(bar_mma, 1);
+        *abort_flag = 0;
+        ptx::bar_init_fence();
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(ptx::smem_addr(slot), 128);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *slot;
+    if (threadIdx.x == 0) {
+        ptx::bar_arrive_expect_tx(bar_load, (2 + D / 64) * kBox);
+        for (int b = 0; b < 2; ++b) ptx::tma_load_3d(sb + kOffX + b * kBox, &tx, bar_load, b * 64, 0, 0);
+        for (int b = 0; b < D / 64; ++b) ptx::tma_load_3d(sb + kOffY + b * kBox, &ty, bar_load, b * 64, 0, 0);
+        if (ptx::bar_wait(bar_load, 0, abort_flag, timeout_ns)) {
+            constexpr uint32_t idesc = ptx::idesc_f16(BF16, 128, D, true, true);
+            for (int kk = 0; kk < 8; ++kk)
+                ptx::mma_ss(tmem, ptx::smem_desc_sw128(sb + kOffX + kk * 2048, kBox, 1024),
+                            ptx::smem_desc_sw128(sb + kOffY + kk * 2048, kBox, 1024), idesc, kk > 0);
+            ptx::mma_commit(bar_mma);
+            ptx::bar_wait(bar_mma, 0, nullptr, timeout_ns);
+        } else {
+            ptx::bar_wait(bar_load, 0, nullptr, timeout_ns);
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (!*abort_flag) {
+        const int row = warp * 32 + lane;
+        for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t r[32];
+            ptx::tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + ch * 32, r);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence(r);
+            for (int i = 0; i < 32; ++i) c[row * D + ch * 32 + i] = __uint_as_float(r[i]);
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 128);
+    }
+    if (threadIdx.x == 0) *status = *abort_flag ? 1 : 0;
+}
+
 // Waits on a barrier that never completes, while holding TMEM, and must come
 // back on its own after timeout_ns with the TMEM released.
 __global__ void __launch_bounds__(128, 1) st_watchdog_kernel(int *status, unsigned long long timeout_ns) {
@@ -227,6 +296,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// A [rows, D] row-major 16-bit matrix as a 3-D map {D, rows, 1} with 64 x rows x 1 boxes.
+bool encode_rows(CUtensorMap *m, const void *base, int rows, int D, bool bf16) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows), 1};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(D) * 2 * rows};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base),
+              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A [128, D] row-major 16-bit matrix as a 3-D map {D, 128, 1} with 64x128x1 boxes.
 bool encode_128xD(CUtensorMap *m, const void *base, int D, bool bf16) {
     auto fn = encode_fn();
@@ -260,6 +342,17 @@ int run_pv(const void *p, const void *v, float *c, int *status, unsigned long lo
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
+template <int D, bool BF16>
+int run_tn(const void *x, const void *y, float *c, int *status, unsigned long long t, cudaStream_t st) {
+    CUtensorMap mx, my;
+    if (!encode_rows(&mx, x, 128, 128, BF16) || !encode_rows(&my, y, 128, D, BF16)) return -2;
+    auto k = st_tn_kernel<D, BF16>;
+    constexpr int kSmem = (2 + D / 64) * 128 * 128 + 64 + 1024;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess) return -3;
+    k<<<1, 128, kSmem, st>>>(mx, my, c, status, t);
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
 }  // namespace
 
 extern "C" {
@@ -277,6 +370,15 @@ __attribute__((visibility("default"))) int fa_selftest_pv(const void *p, const v
     auto st = static_cast<cudaStream_t>(stream);
     if (D == 64) return bf16 ? run_pv<64, true>(p, v, c, status, timeout_ns, st) : run_pv<64, false>(p, v, c, status, timeout_ns, st);
     if (D == 128) return bf16 ? run_pv<128, true>(p, v, c, status, timeout_ns, st) : run_pv<128, false>(p, v, c, status, timeout_ns, st);
+    return -1;
+}
+
+// x [128,128], y [128,D] row-major 16-bit; c [128,D] fp32 = x^T y. D: 64 or 128.
+__attribute__((visibility("default"))) int fa_selftest_tn(const void *x, const void *y, float *c, int D, int bf16,
+                                                          int *status, unsigned long long timeout_ns, void *stream) {
+    auto st = static_cast<cudaStream_t>(stream);
+    if (D == 64) return bf16 ? run_tn<64, true>(x, y, c, status, timeout_ns, st) : run_tn<64, false>(x, y, c, status, timeout_ns, st);
+    if (D == 128) return bf16 ? run_tn<128, true>(x, y, c, status, timeout_ns, st) : run_tn<128, false>(x, y, c, status, timeout_ns, st);
     return -1;
 }
 

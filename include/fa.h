@@ -8,6 +8,7 @@
  *   fa_splitkv_merge   split-KV decoding, phase 2: log-sum-exp merge.
  *   fa_decode_splitkv_fused, fa_decode_paged_splitkv_fused
  *                      both phases in one launch (last partition merges).
+ *   fa_bwd             backward pass: dQ, dK, dV from dO and the forward LSE.
  *
  * Common rules
  *   - Every tensor pointer is a DEVICE pointer owned by the caller. The library
@@ -34,6 +35,7 @@
 #ifndef FA_H
 #define FA_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)
@@ -58,7 +60,8 @@ typedef enum {
     FA_ERR_CUDA = -8,           /* the CUDA runtime reported an error (launch, tensor map) */
     FA_ERR_DEVICE_TIMEOUT = -9, /* a kernel gave up waiting on an on-chip barrier */
     FA_ERR_SCRATCH = -10,       /* fa_decode_noalloc: problem larger than its built-in scratch */
-    FA_ERR_DEVICE_INDEX = -11   /* a kernel met an out-of-range block-table entry */
+    FA_ERR_DEVICE_INDEX = -11,  /* a kernel met an out-of-range block-table entry */
+    FA_ERR_WORKSPACE = -12      /* caller workspace smaller than required */
 } fa_status_t;
 
 typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype_t;
@@ -229,6 +232,42 @@ FA_API fa_status_t fa_decode_paged_splitkv_fused(const void *q, const void *k_ca
                                                  int32_t *counters, int B, int H, int D, int num_blocks,
                                                  int block_size, int max_blocks_per_seq, int num_splits,
                                                  float scale, fa_dtype_t dtype, void *stream);
+
+/*
+ * fa_bwd_workspace_bytes - bytes of fp32 workspace fa_bwd needs:
+ * 4 * (B*H*Sq*D + 2*B*H*ceil(Sq/128)*128); 0 for an invalid shape.
+ */
+FA_API size_t fa_bwd_workspace_bytes(int B, int H, int Sq, int D);
+
+/*
+ * fa_bwd - exact attention backward pass.
+ *
+ * Defined by "Adaptive High-Performance Attention Kernels in CUDA" (Advanced
+ * Production Features 2, Custom CUDA Backward Pass): S = scale Q K^T and
+ * P = exp(S - LSE) are recomputed on chip from the forward's LSE (P is never
+ * stored), D_i = sum_k dO_ik O_ik, dS = P (dP - D_i) with dP = dO V^T; then
+ * dV = P^T dO, dK = scale dS^T Q, dQ = scale dS K (chain rule of the same
+ * definition), with the causal rule of fa_fwd.
+ *
+ *   q, o, dout  [B,H,Sq,D]  fp16/bf16   k, v [B,H,Sk,D]  same dtype
+ *   lse         [B,H,Sq] fp32, as written by fa_fwd for these q, k, v
+ *   dq [B,H,Sq,D], dk and dv [B,H,Sk,D]: outputs in the input dtype
+ *   workspace   caller-owned device memory of at least
+ *               fa_bwd_workspace_bytes(B, H, Sq, D) bytes, 16-byte aligned
+ *               (fp32 dQ accumulator and per-row statistics); its contents on
+ *               entry do not matter. Calls sharing a workspace must not
+ *               overlap on the GPU.
+ *   D           64 or 128.
+ * Three launches on `stream`. dQ sums contributions of all key tiles with
+ * fp32 atomic additions, so its rounding can differ between runs; dK and dV
+ * are deterministic.
+ * Errors: FA_ERR_NULL, FA_ERR_SHAPE, FA_ERR_HEADDIM, FA_ERR_DTYPE,
+ * FA_ERR_ALIGN, FA_ERR_SCALE, FA_ERR_WORKSPACE, FA_ERR_CUDA.
+ */
+FA_API fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                          const float *lse, void *dq, void *dk, void *dv, float *workspace,
+                          size_t workspace_bytes, int B, int H, int Sq, int Sk, int D, int causal,
+                          float scale, fa_dtype_t dtype, void *stream);
 
 /*
  * fa_check_device_error - synchronise `stream`, then read and clear the

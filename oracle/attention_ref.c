@@ -286,17 +286,18 @@ int oracle_attention_bwd_head(const double *q, const double *k, const double *v,
             for (int j = 0; j < Sk; ++j) acc += dS[(size_t)i * Sk + j] * k[(size_t)j * D + d];
             dq[(size_t)i * D + d] = scale * acc;
         }
-    /* dK_j = scale * sum_i dS_ij q_i, dV_j = sum_i P_ij dO_i */
-    for (int j = 0; j < Sk; ++j)
-        for (int d = 0; d < D; ++d) {
-            double ak = 0.0, av = 0.0;
-            for (int i = 0; i < Sq; ++i) {
-                ak += dS[(size_t)i * Sk + j] * q[(size_t)i * D + d];
-                av += P[(size_t)i * Sk + j] * dout[(size_t)i * D + d];
+    /* dK_j = scale * sum_i dS_ij q_i, dV_j = sum_i P_ij dO_i (summed over i
+     * in the outer loop so that P and dS are read row by row) */
+    for (size_t x = 0; x < (size_t)Sk * D; ++x) { dk[x] = 0.0; dv[x] = 0.0; }
+    for (int i = 0; i < Sq; ++i)
+        for (int j = 0; j < Sk; ++j) {
+            const double ds_ij = dS[(size_t)i * Sk + j], p_ij = P[(size_t)i * Sk + j];
+            for (int d = 0; d < D; ++d) {
+                dk[(size_t)j * D + d] += ds_ij * q[(size_t)i * D + d];
+                dv[(size_t)j * D + d] += p_ij * dout[(size_t)i * D + d];
             }
-            dk[(size_t)j * D + d] = scale * ak;
-            dv[(size_t)j * D + d] = av;
         }
+    for (size_t x = 0; x < (size_t)Sk * D; ++x) dk[x] *= scale;
     free(P);
     free(dS);
     free(o);

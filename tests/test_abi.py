@@ -46,7 +46,7 @@ def test_only_the_abi_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    for code in range(-11, 1):
+    for code in range(-12, 1):
         s = fa.fa_status_string(code)
         assert s and s != "unknown status"
     assert fa.fa_status_string(-1234) == "unknown status"
@@ -171,6 +171,27 @@ def test_paged_fused_validation(lib):
     assert _paged_fused(lib, cnt=A + 1) == ALIGN
 
 
+def _bwd(lib, q=A, k=A, v=A, o=A, do=A, lse=A, dq=A, dk=A, dv=A, ws=A, wsb=1 << 30, B=1, H=2, Sq=200, Sk=300,
+         D=128, causal=1, scale=0.1, dtype=1):
+    return lib.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, wsb, B, H, Sq, Sk, D, causal, scale, dtype, None)
+
+
+def test_bwd_validation(lib):
+    for kw in ("q", "o", "do", "lse", "dq", "dk", "dv", "ws"):
+        assert _bwd(lib, **{kw: None}) == NULL, kw
+    assert _bwd(lib, dtype=3) == DTYPE
+    assert _bwd(lib, D=256) == HEADDIM
+    for kw in ({"B": 0}, {"H": 0}, {"Sq": 0}, {"Sk": 0}):
+        assert _bwd(lib, **kw) == SHAPE, kw
+    assert _bwd(lib, scale=0.0) == SCALE
+    assert _bwd(lib, dq=MIS) == ALIGN
+    assert _bwd(lib, ws=MIS) == ALIGN
+    need = lib.fa_bwd_workspace_bytes(1, 2, 200, 128)
+    assert need == 4 * (2 * 200 * 128 + 2 * 2 * 256)
+    assert _bwd(lib, wsb=need - 4) == -12
+    assert lib.fa_bwd_workspace_bytes(1, 2, 200, 96) == 0
+
+
 def test_merge_validation(lib):
     m = lib.fa_splitkv_merge
     assert m(None, A, A, A, A, 2, 2, 128, 8, 1, None) == NULL
@@ -188,5 +209,5 @@ def test_binding_fails_loudly_without_library(tmp_path):
 
 def test_selftest_library_exports(lib):
     st = ctypes.CDLL(fabuild.SELFTEST_LIB)
-    for n in ("fa_selftest_qk", "fa_selftest_pv", "fa_selftest_watchdog"):
+    for n in ("fa_selftest_qk", "fa_selftest_pv", "fa_selftest_tn", "fa_selftest_watchdog"):
         assert hasattr(st, n)

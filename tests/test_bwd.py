@@ -1,0 +1,111 @@
+"""Backward pass (fa_bwd) against the fp64 oracle's gradients on the same
+seeded inputs, with the forward's O and LSE from fa_fwd.
+
+Tolerance: the kernel rounds P and dS to 16 bits before their products and
+accumulates in fp32, so an element of dQ, dK or dV carries a relative error
+of a few 2^-9 of the magnitudes that meet in its sum; the check is
+max |g - ref| <= 2e-2 * max(1, max |ref|) per tensor, plus
+||g - ref|| <= 1e-2 * max(||ref||, sqrt(n)). Bookkeeping is exact: keys no query can see get
+dK = dV = 0 bit for bit, and dK, dV are bitwise repeatable."""
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_54_gb300 as fa
+import oracle
+from exact_attention_54_gb300 import inputs
+from gpu_helpers import dev
+
+pytestmark = pytest.mark.gpu
+
+GRAD_TOL = 2e-2
+FRO_TOL = 1e-2
+
+
+def grads(q, k, v, do, causal, scale):
+    qd, kd, vd, dod = dev(q, k, v, do)
+    o, lse = fa.flash_attention(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = fa.flash_attention_bwd(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    return dq.cpu(), dk.cpu(), dv.cpu()
+
+
+def assert_grad_close(got, ref, what):
+    g = got.double().numpy() if hasattr(got, "numpy") else np.asarray(got, np.float64)
+    r = np.asarray(ref, np.float64)
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite values"
+    err = float(np.max(np.abs(g - r)))
+    bound = GRAD_TOL * max(1.0, float(np.max(np.abs(r))))
+    # Frobenius error relative to the reference, floored (like the max bound)
+    # at an O(1) scale per element: an exactly zero reference (one key) only
+    # meets rounding noise
+    fro = float(np.linalg.norm(g - r) / max(np.linalg.norm(r), np.sqrt(r.size)))
+    assert err <= bound and fro <= FRO_TOL, f"{what}: max err {err:.3e} (bound {bound:.3e}), rel fro {fro:.3e}"
+
+
+def check(B, H, Sq, Sk, D, dtype, causal, seed, scale=None):
+    q, k, v = inputs.make_dense(B, H, Sq, Sk, D, dtype, seed=seed)
+    do = inputs.make_dense(B, H, Sq, Sq, D, dtype, seed=seed + 1)[0]
+    scale = 1.0 / D ** 0.5 if scale is None else scale
+    dq, dk, dv = grads(q, k, v, do, causal, scale)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, causal, scale)
+    what = f"{(B, H, Sq, Sk, D, dtype, causal)}"
+    assert_grad_close(dq, rq, "dq " + what)
+    assert_grad_close(dk, rk, "dk " + what)
+    assert_grad_close(dv, rv, "dv " + what)
+    return dq, dk, dv
+
+
+SHAPES = [
+    # B, H, Sq, Sk, D, dtype, causal
+    (1, 1, 1, 1, 64, torch.float16, False),
+    (1, 1, 128, 128, 64, torch.float16, False),
+    (1, 2, 200, 200, 128, torch.bfloat16, True),
+    (2, 2, 300, 77, 64, torch.bfloat16, False),
+    (1, 2, 77, 300, 128, torch.float16, False),
+    (1, 2, 300, 77, 128, torch.bfloat16, True),    # Sq > Sk: late rows see every key
+    (1, 2, 77, 300, 64, torch.float16, True),      # Sq < Sk: keys past the last query get no gradient
+    (2, 2, 640, 640, 128, torch.bfloat16, True),
+    (1, 3, 384, 512, 64, torch.float16, False),
+]
+
+
+@pytest.mark.parametrize("B,H,Sq,Sk,D,dtype,causal", SHAPES)
+def test_bwd_matches_oracle(B, H, Sq, Sk, D, dtype, causal):
+    check(B, H, Sq, Sk, D, dtype, causal, seed=Sq * 3 + Sk + D)
+
+
+def test_bwd_non_default_scale():
+    check(1, 2, 256, 256, 128, torch.bfloat16, True, seed=9, scale=0.3)
+
+
+def test_unreachable_keys_get_exact_zero_and_dk_dv_repeat_bitwise():
+    """Causal, Sq = 200 < Sk = 520: keys 200.. are above every query's
+    diagonal (and keys 256.. form whole tiles no query visits)."""
+    q, k, v = inputs.make_dense(1, 2, 200, 520, 64, torch.bfloat16, seed=61)
+    do = inputs.make_dense(1, 2, 200, 200, 64, torch.bfloat16, seed=62)[0]
+    dq1, dk1, dv1 = grads(q, k, v, do, True, 0.125)
+    assert torch.count_nonzero(dk1[:, :, 200:]) == 0 and torch.count_nonzero(dv1[:, :, 200:]) == 0
+    _, dk2, dv2 = grads(q, k, v, do, True, 0.125)
+    assert torch.equal(dk1.view(torch.int16), dk2.view(torch.int16))
+    assert torch.equal(dv1.view(torch.int16), dv2.view(torch.int16))
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, True, 0.125)
+    assert_grad_close(dq1, rq, "dq")
+    assert_grad_close(dk1[:, :, :200], rk[:, :, :200], "dk")
+
+
+def test_bwd_llama_prefill_full_size_two_heads():
+    """The LLaMA-7B prefill shape (1,32,4096,4096,128, causal, bf16) through
+    the full kernel; two heads compared against the oracle (about a minute of
+    fp64 CPU work per head)."""
+    w = inputs.WORKLOADS["llama_prefill"]
+    q, k, v = inputs.make_workload(w)
+    do = inputs.make_dense(w.B, w.H, w.Sq, w.Sq, w.D, w.dtype, seed=w.seed + 100)[0]
+    dq, dk, dv = grads(q, k, v, do, True, w.scale)
+    heads = [0, 17]
+    rq, rk, rv = oracle.attention_bwd(q[:, heads], k[:, heads], v[:, heads], do[:, heads], True, w.scale)
+    assert_grad_close(dq[:, heads], rq, "dq llama")
+    assert_grad_close(dk[:, heads], rk, "dk llama")
+    assert_grad_close(dv[:, heads], rv, "dv llama")

@@ -43,10 +43,12 @@ MUTANTS = [
     ("bwd dQ unscaled", "dq[(size_t)i * D + d] = scale * acc;", "dq[(size_t)i * D + d] = acc;"),
     ("bwd dQ against V", "acc += dS[(size_t)i * Sk + j] * k[(size_t)j * D + d];",
      "acc += dS[(size_t)i * Sk + j] * v[(size_t)j * D + d];"),
-    ("bwd dK from P", "ak += dS[(size_t)i * Sk + j] * q[(size_t)i * D + d];",
-     "ak += P[(size_t)i * Sk + j] * q[(size_t)i * D + d];"),
-    ("bwd dV from dS", "av += P[(size_t)i * Sk + j] * dout[(size_t)i * D + d];",
-     "av += dS[(size_t)i * Sk + j] * dout[(size_t)i * D + d];"),
+    ("bwd dK from P", "dk[(size_t)j * D + d] += ds_ij * q[(size_t)i * D + d];",
+     "dk[(size_t)j * D + d] += p_ij * q[(size_t)i * D + d];"),
+    ("bwd dV from dS", "dv[(size_t)j * D + d] += p_ij * dout[(size_t)i * D + d];",
+     "dv[(size_t)j * D + d] += ds_ij * dout[(size_t)i * D + d];"),
+    ("bwd dK unscaled", "for (size_t x = 0; x < (size_t)Sk * D; ++x) dk[x] *= scale;",
+     "for (size_t x = 0; x < (size_t)Sk * D; ++x) dk[x] *= 1.0;"),
     ("bwd mask direction", "Pi[j] = (causal && j > i) ? -INFINITY : scale * qk;",
      "Pi[j] = (causal && j < i) ? -INFINITY : scale * qk;"),
     ("bwd softmax unnormalised", "for (int j = 0; j < Sk; ++j) Pi[j] /= l;", "for (int j = 0; j < Sk; ++j) Pi[j] /= 1.0;"),

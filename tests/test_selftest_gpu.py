@@ -19,6 +19,7 @@ def st():
     vp, i, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_ulonglong
     lib.fa_selftest_qk.argtypes = [vp, vp, vp, i, i, vp, u64, vp]
     lib.fa_selftest_pv.argtypes = [vp, vp, vp, i, i, vp, u64, vp]
+    lib.fa_selftest_tn.argtypes = [vp, vp, vp, i, i, vp, u64, vp]
     lib.fa_selftest_watchdog.argtypes = [vp, u64, vp]
     return lib
 
@@ -72,6 +73,26 @@ def test_pv_mma(st, D, dtype):
     assert rc == 0 and int(status) == 0
     err = float((c - p.float() @ v.float()).abs().max())
     assert err < 1e-3, _diagnose_pv(c, p, v)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_transposed_a_mma(st, D, dtype):
+    """C = X^T Y with X read as an MN-major A operand (the layout the backward
+    pass uses for dQ = dS K with dS^T in shared memory)."""
+    g = torch.Generator().manual_seed(200 + D)
+    x = torch.randn(128, 128, generator=g).to(dtype).cuda()
+    y = torch.randn(128, D, generator=g).to(dtype).cuda()
+    c = torch.full((128, D), float("nan"), device="cuda")
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    rc = st.fa_selftest_tn(x.data_ptr(), y.data_ptr(), c.data_ptr(), D, int(dtype == torch.bfloat16),
+                           status.data_ptr(), 1_000_000_000, _stream())
+    torch.cuda.synchronize()
+    assert rc == 0 and int(status) == 0
+    ref = x.float().T @ y.float()
+    err = float((c - ref).abs().max())
+    hyps = {"X^T Y": ref, "X Y": x.float() @ y.float()}
+    assert err < 1e-3, {k: float((c - v).abs().max()) for k, v in hyps.items()}
 
 
 def test_watchdog_gives_up_and_gpu_stays_usable(st):

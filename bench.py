@@ -58,7 +58,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end loop (profiling runs)")
     ap.add_argument("--parts", default="prefill,decode",
-                    help="comma list of the path parts to run (profiling runs may isolate one)")
+                    help="comma list of the path parts to run (profiling runs may isolate one: prefill, decode, "
+                         "backward, d256)")
     return ap.parse_args(argv)
 
 
@@ -334,6 +335,16 @@ def run_gpu(args, rank, world, local):
 
     parts = set(args.parts.split(","))
     run_pf, run_dc = "prefill" in parts, "decode" in parts
+    if parts & {"backward", "d256"} and not (run_pf or run_dc):
+        # profiling run of the backward pass or of the D = 256 forward alone
+        rec = {"part": args.parts, "steps": args.steps}
+        if "backward" in parts:
+            rec["backward"] = run_bwd(args, fa, torch, stream, dev, flush, world, (q, k, v), o, lse, wp)
+        if "d256" in parts:
+            rec["d256_prefill"] = run_d256(args, fa, torch, stream, dev, flush, world)
+        if rank == 0:
+            print(json.dumps(rec), flush=True)
+        return None
 
     def step(evs=None):
         flush.fill_(float(1.0))

@@ -23,7 +23,8 @@
 //                         dK  += dS^T Q    (dS^T K-major, Q MN-major)
 //                         dQ_t = dS K      (dS^T read as an MN-major A operand)
 //                       and the query-row warps add dQ_t into the fp32
-//                       accumulator with vector reductions. dK and dV stay in
+//                       accumulator with vector reductions (dQ_t is issued
+//                       first, so they overlap dV and dK). dK and dV stay in
 //                       TMEM for the whole loop and are written once.
 //   fa_bwd_dq_kernel    dQ = scale * accumulator, in the input dtype.
 //
@@ -66,10 +67,11 @@ struct Shape {
     static constexpr int kQEmpty = 3;   // +s
     static constexpr int kSFull = 5;    // S^T and dP^T written (MMA commit)
     static constexpr int kPFull = 6;    // P^T in TMEM and dS^T in shared memory (4 warps)
-    static constexpr int kDQFull = 7;   // dQ_t in TMEM; dS^T no longer read (MMA commit)
+    static constexpr int kDQFull = 7;   // dQ_t in TMEM (MMA commit)
     static constexpr int kDQFree = 8;   // dQ_t read out (4 warps)
-    static constexpr int kTeardown = 9;
-    static constexpr int kNumBars = 10;
+    static constexpr int kDSFree = 9;   // dS^T no longer read; dK and dV of the step done (MMA commit)
+    static constexpr int kTeardown = 10;
+    static constexpr int kNumBars = 11;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
     static constexpr uint32_t kTmemS = 0;
@@ -272,6 +274,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = wait(S::kPFull, it & 1))) break;
             ptx::tc_fence_after();
             if (leader) {
+                // dQ_t = dS K into [128,256) first (dP^T there was consumed by
+                // the key-row warps), so that its reduction overlaps dV and dK
+#pragma unroll
+                for (int kk = 0; kk < kBlock / 16; ++kk)
+                    ptx::mma_ss(tmem + S::kTmemDP, ds_mn + kk * kRows16, k_mn + kk * kRows16, kIdQ, kk > 0);
+                ptx::mma_commit(bar(S::kDQFull));
                 // dV += P^T dO: 8 MMAs over the 128 queries, P^T from TMEM
 #pragma unroll
                 for (int kk = 0; kk < kBlock / 16; ++kk)
@@ -285,11 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 (it > 0 || kk > 0) ? 1u : 0u);
                 }
                 ptx::mma_commit(bar(S::kQEmpty + s));  // Q and dO of this step have all their readers
-                // dQ_t = dS K into [128,256) (dP^T there was consumed by the softmax warps)
-#pragma unroll
-                for (int kk = 0; kk < kBlock / 16; ++kk)
-                    ptx::mma_ss(tmem + S::kTmemDP, ds_mn + kk * kRows16, k_mn + kk * kRows16, kIdQ, kk > 0);
-                ptx::mma_commit(bar(S::kDQFull));
+                ptx::mma_commit(bar(S::kDSFree));
             }
         }
         if (leader) ptx::mma_commit(bar(S::kTeardown));
@@ -306,23 +310,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float *delta = p.delta + static_cast<size_t>(bh) * p.Sq_pad;
         bool ok = true;
         for (int it = 0; it < n; ++it) {
-            if (!(ok = wait(S::kSFull, it & 1))) break;
-            if (it > 0 && !(ok = wait(S::kDQFull, (it - 1) & 1))) break;  // dS^T buffer free again
-            ptx::tc_fence_after();
+            // the query tile's 128 LSE and D values, 4 per lane, fetched
+            // (coalesced) before the wait and handed out with shuffles
             const int q0 = (qt0 + it) * kBlock;
+            const float4 lse4 = __ldg(reinterpret_cast<const float4 *>(lse2 + q0) + lane);
+            const float4 del4 = __ldg(reinterpret_cast<const float4 *>(delta + q0) + lane);
+            if (!(ok = wait(S::kSFull, it & 1))) break;
+            if (it > 0 && !(ok = wait(S::kDSFree, (it - 1) & 1))) break;  // dS^T buffer free again
+            ptx::tc_fence_after();
 #pragma unroll 1
             for (int c = 0; c < kBlock / 32; ++c) {
                 uint32_t sv[32], dpv[32];
                 ptx::tmem_ld32(tmem + lane_base + S::kTmemS + 32 * c, sv);
                 ptx::tmem_ld32(tmem + lane_base + S::kTmemDP + 32 * c, dpv);
-                float l2[32], dl[32];
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const float4 a = __ldg(reinterpret_cast<const float4 *>(lse2 + q0 + 32 * c) + m);
-                    const float4 b = __ldg(reinterpret_cast<const float4 *>(delta + q0 + 32 * c) + m);
-                    l2[4 * m] = a.x, l2[4 * m + 1] = a.y, l2[4 * m + 2] = a.z, l2[4 * m + 3] = a.w;
-                    dl[4 * m] = b.x, dl[4 * m + 1] = b.y, dl[4 * m + 2] = b.z, dl[4 * m + 3] = b.w;
-                }
                 ptx::tmem_ld_wait();
                 ptx::reg_fence(sv);
                 ptx::reg_fence(dpv);
@@ -334,10 +334,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float e[2], g[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        float pv = ptx::ex2(fmaf(__uint_as_float(sv[j + u]), p.scale_log2, -l2[j + u]));
+                        // query 32c + j + u lives in lane 8c + (j + u) / 4, component (j + u) % 4
+                        const int src = 8 * c + (j + u) / 4;
+                        const int comp = (j + u) % 4;
+                        const float l2 = __shfl_sync(0xffffffffu, comp == 0 ? lse4.x : comp == 1 ? lse4.y
+                                                                 : comp == 2 ? lse4.z : lse4.w, src);
+                        const float dl = __shfl_sync(0xffffffffu, comp == 0 ? del4.x : comp == 1 ? del4.y
+                                                                 : comp == 2 ? del4.z : del4.w, src);
+                        float pv = ptx::ex2(fmaf(__uint_as_float(sv[j + u]), p.scale_log2, -l2));
                         if (need_mask && ((CAUSAL && key > qc + j + u) || key >= p.Sk)) pv = 0.f;
                         e[u] = pv;
-                        g[u] = pv * (__uint_as_float(dpv[j + u]) - dl[j + u]);
+                        g[u] = pv * (__uint_as_float(dpv[j + u]) - dl);
                     }
                     pp[j / 2] = ptx::pack2<BF16>(e[0], e[1]);
                     dd[j / 2] = ptx::pack2<BF16>(g[0], g[1]);
@@ -360,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // epilogue: dV and scale * dK rows of this key tile
         if (ok && n > 0) {
-            ok = wait(S::kDQFull, (n - 1) & 1);  // the last MMAs of the loop are done
+            ok = wait(S::kDSFree, (n - 1) & 1);  // the last dV and dK of the loop are done
             ptx::tc_fence_after();
         }
         // The TMEM loads are warp-collective (.sync.aligned): every lane runs

@@ -22,16 +22,18 @@
 //                         dV  += P^T dO    (P^T from TMEM, dO MN-major)
 //                         dK  += dS^T Q    (dS^T K-major, Q MN-major)
 //                         dQ_t = dS K      (dS^T read as an MN-major A operand)
-//                       and the query-row warps add dQ_t into the fp32
-//                       accumulator with vector reductions (dQ_t is issued
-//                       first, so they overlap dV and dK). dK and dV stay in
+//                       dQ_t is issued first; the query-row warps move it to
+//                       registers (releasing its TMEM columns), then into the
+//                       step's Q/dO stage once dV and dK are done with it, and
+//                       warp 3 adds the staged tile to the fp32 accumulator
+//                       with TMA bulk tensor reductions. dK and dV stay in
 //                       TMEM for the whole loop and are written once.
 //   fa_bwd_dq_kernel    dQ = scale * accumulator, in the input dtype.
 //
 // Roles of fa_bwd_kernel (384 threads): warp 0 TMA producer (K, V once; Q and
-// dO double-buffered), warp 1 MMA issuer and TMEM owner, warps 4..7 one key
-// row per thread (P^T, dS^T, then the dK/dV epilogue), warps 8..11 one query
-// row per thread (dQ reduction). TMEM columns: S^T [0,128), dP^T and then dQ_t
+// dO double-buffered), warp 1 MMA issuer and TMEM owner, warp 3 bulk
+// reductions of dQ_t, warps 4..7 one key row per thread (P^T, dS^T, then the
+// dK/dV epilogue), warps 8..11 one query row per thread (dQ_t staging). TMEM columns: S^T [0,128), dP^T and then dQ_t
 // [128,256), dV [256, 256+D), dK [256+D, 256+2D).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -70,8 +72,10 @@ struct Shape {
     static constexpr int kDQFull = 7;   // dQ_t in TMEM (MMA commit)
     static constexpr int kDQFree = 8;   // dQ_t read out (4 warps)
     static constexpr int kDSFree = 9;   // dS^T no longer read; dK and dV of the step done (MMA commit)
-    static constexpr int kTeardown = 10;
-    static constexpr int kNumBars = 11;
+    static constexpr int kStageReady = 10;  // dQ_t staged in the step's Q/dO buffers (4 warps)
+    static constexpr int kStageFree = 11;   // +s: the bulk reduction has read stage s (1 thread)
+    static constexpr int kTeardown = 13;
+    static constexpr int kNumBars = 14;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
     static constexpr uint32_t kTmemS = 0;
@@ -163,7 +167,7 @@ template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     using S = Shape<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -186,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S::kNumBars; ++i)
-            ptx::bar_init(bar(i), (i == S::kPFull || i == S::kDQFree) ? kBlock / 32 : 1u);
+            ptx::bar_init(bar(i), (i == S::kPFull || i == S::kDQFree || i == S::kStageReady) ? kBlock / 32 : 1u);
         *abort_flag = 0;
         ptx::bar_init_fence();
     }
@@ -195,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
         ptx::prefetch_tmap(&tm_do);
+        ptx::prefetch_tmap(&tm_dq);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), S::kTmemCols);
@@ -216,7 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int it = 0;
         for (; it < n; ++it) {
             const int s = it & 1;
-            if (it >= 2 && !wait(S::kQEmpty + s, ((it >> 1) - 1) & 1)) break;
+            // stage s is free once the bulk reduction of step it-2 has read it
+            if (it >= 2 && !wait(S::kStageFree + s, ((it >> 1) - 1) & 1)) break;
             if (leader) {
                 const int q0 = (qt0 + it) * kBlock;
                 ptx::bar_arrive_expect_tx(bar(S::kQFull + s), 2 * S::kTileBytes);
@@ -406,31 +412,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 8) {
         // ---- query rows: dQ_t into the fp32 accumulator ----
+        // The row goes to registers (freeing the TMEM columns for the next
+        // dP^T at once), then, when dV and dK of the step are done, into the
+        // step's own Q/dO stage as four 128-byte-swizzled boxes of 32 fp32
+        // columns, which warp 3 adds to the accumulator with bulk reductions.
         const int wq = warp - 8;
         const int r = wq * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t row_off = (r >> 3) * 1024 + (r & 7) * 128;
         for (int it = 0; it < n; ++it) {
+            const int s = it & 1;
             if (!wait(S::kDQFull, it & 1)) break;
             ptx::tc_fence_after();
-            const int query = (qt0 + it) * kBlock + r;
-            float *dst = p.dq_acc + (static_cast<size_t>(bh) * p.Sq + query) * D;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                ptx::tmem_ld32(tmem + lane_base + S::kTmemDP + 32 * c, v);
-                ptx::tmem_ld_wait();
-                ptx::reg_fence(v);
-                if (query < p.Sq) {
+            uint32_t v[D / 32][32];
 #pragma unroll
-                    for (int m = 0; m < 8; ++m)
-                        red_add4(dst + 32 * c + 4 * m, __uint_as_float(v[4 * m]), __uint_as_float(v[4 * m + 1]),
-                                 __uint_as_float(v[4 * m + 2]), __uint_as_float(v[4 * m + 3]));
-                }
-            }
+            for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(tmem + lane_base + S::kTmemDP + 32 * c, v[c]);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) ptx::reg_fence(v[c]);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::bar_arrive(bar(S::kDQFree));
+            if (!wait(S::kQEmpty + s, (it >> 1) & 1)) break;  // Q and dO of this step have all their readers
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                // boxes [0, D/64) in the Q stage, the rest in the dO stage
+                const uint32_t box = sbase + (c < D / 64 ? S::kOffQ + s * S::kTileBytes + c * S::kBoxBytes
+                                                         : S::kOffDO + s * S::kTileBytes + (c - D / 64) * S::kBoxBytes);
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    st_shared_v4(box + row_off + ((m ^ (r & 7)) * 16), v[c][4 * m], v[c][4 * m + 1], v[c][4 * m + 2],
+                                 v[c][4 * m + 3]);
+            }
+            ptx::fence_proxy_async_smem();  // the bulk reduction reads the stage next
+            __syncwarp();
+            if (lane == 0) ptx::bar_arrive(bar(S::kStageReady));
         }
+    } else if (warp == 3 && n > 0) {
+        // ---- bulk reductions of the staged dQ_t into the accumulator ----
+        const bool leader = ptx::elect_one();
+        for (int it = 0; it < n; ++it) {
+            const int s = it & 1;
+            if (!wait(S::kStageReady, it & 1)) break;
+            if (leader) {
+                const int q0 = (qt0 + it) * kBlock;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    const uint32_t box = sbase + (c < D / 64 ? S::kOffQ + s * S::kTileBytes + c * S::kBoxBytes
+                                                             : S::kOffDO + s * S::kTileBytes + (c - D / 64) * S::kBoxBytes);
+                    ptx::tma_reduce_add_3d(&tm_dq, box, 32 * c, q0, bh);  // rows past Sq are clipped
+                }
+                ptx::bulk_commit();
+                ptx::bulk_wait_read_all();  // the stage may be refilled now
+                ptx::bar_arrive(bar(S::kStageFree + s));
+            }
+            __syncwarp();
+        }
+        if (leader) ptx::bulk_wait_all();  // the reductions themselves are complete
+        __syncwarp();
     }
 
     ptx::tc_fence_before();
@@ -455,7 +494,8 @@ cudaError_t launch_t(const CUtensorMap *maps, const void *o, const void *dout, c
     constexpr int kSmem = Shape<D>::kSmemBytes;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(p.BH * p.n_ktiles), kThreads, kSmem, st>>>(maps[0], maps[1], maps[2], maps[3], p);
+    kern<<<static_cast<unsigned>(p.BH * p.n_ktiles), kThreads, kSmem, st>>>(maps[0], maps[1], maps[2], maps[3],
+                                                                             maps[4], p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long n8 = static_cast<long long>(p.BH) * p.Sq * D / 8;

@@ -71,7 +71,7 @@ struct BwdParams {
     unsigned long long timeout_ns;
 };
 
-// maps: {Q, K, V, dO}; lse [B*H][Sq]; dq output (input dtype).
+// maps: {Q, K, V, dO, dQ accumulator (fp32)}; lse [B*H][Sq]; dq output (input dtype).
 cudaError_t launch_bwd(int D, bool bf16, bool causal, const CUtensorMap *maps, const void *o, const void *dout,
                        const float *lse, void *dq, const BwdParams &p, cudaStream_t stream);
 

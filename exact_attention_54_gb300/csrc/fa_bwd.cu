@@ -32,8 +32,11 @@
 //
 // Roles of fa_bwd_kernel (384 threads): warp 0 TMA producer (K, V once; Q and
 // dO double-buffered), warp 1 MMA issuer and TMEM owner, warp 3 bulk
-// reductions of dQ_t, warps 4..7 one key row per thread (P^T, dS^T, then the
-// dK/dV epilogue), warps 8..11 one query row per thread (dQ_t staging). TMEM columns: S^T [0,128), dP^T and then dQ_t
+// reductions of dQ_t, warps 4..11 two warpgroups that split every step by
+// halves: warpgroup h computes P^T and dS^T for queries [64h, 64h+64) of each
+// key row, then stages dQ_t columns [h D/2, (h+1) D/2) of each query row, and
+// writes that column half of dK and dV at the end. P^T of half h sits in S^T
+// columns [64h, 64h+32). TMEM columns: S^T [0,128), dP^T and then dQ_t
 // [128,256), dV [256, 256+D), dK [256+D, 256+2D).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -63,21 +66,30 @@ struct Shape {
     static constexpr int kOffQ = kOffV + kTileBytes;    // + s * tile, s = 0, 1
     static constexpr int kOffDO = kOffQ + 2 * kTileBytes;
     static constexpr int kOffDS = kOffDO + 2 * kTileBytes;  // dS^T [128 keys][128 queries], 2 boxes
-    static constexpr int kOffBar = kOffDS + 2 * kBoxBytes;
+    static constexpr int kTilesBytes = kOffDS + 2 * kBoxBytes;
+    // The small region (barriers, TMEM base, abort flag, the step's base-2 LSE
+    // and D values) sits at the start of the allocation, in front of the
+    // 1024-aligned tiles, so it reuses the alignment slack.
+    static constexpr int kOffBar = 0;
     static constexpr int kKVFull = 0;
     static constexpr int kQFull = 1;    // +s
     static constexpr int kQEmpty = 3;   // +s
     static constexpr int kSFull = 5;    // S^T and dP^T written (MMA commit)
-    static constexpr int kPFull = 6;    // P^T in TMEM and dS^T in shared memory (4 warps)
+    static constexpr int kPFull = 6;    // P^T in TMEM and dS^T in shared memory (8 warps)
     static constexpr int kDQFull = 7;   // dQ_t in TMEM (MMA commit)
-    static constexpr int kDQFree = 8;   // dQ_t read out (4 warps)
+    static constexpr int kDQFree = 8;   // dQ_t read out (8 warps)
     static constexpr int kDSFree = 9;   // dS^T no longer read; dK and dV of the step done (MMA commit)
-    static constexpr int kStageReady = 10;  // dQ_t staged in the step's Q/dO buffers (4 warps)
+    static constexpr int kStageReady = 10;  // dQ_t staged in the step's Q/dO buffers (8 warps)
     static constexpr int kStageFree = 11;   // +s: the bulk reduction has read stage s (1 thread)
-    static constexpr int kTeardown = 13;
-    static constexpr int kNumBars = 14;
+    static constexpr int kLFull = 13;       // the step's LSE and D values are in shared memory (bulk copy)
+    static constexpr int kTeardown = 14;
+    static constexpr int kNumBars = 15;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
+    static constexpr int kOffRows = 256;                     // float lse2[128], delta[128]
+    static constexpr int kSmallBytes = kOffRows + 2 * 128 * 4;
+    static_assert(kOffMisc + 16 <= kOffRows, "small region layout");
+    // small region + worst-case padding to the next 1024-byte boundary + tiles
+    static constexpr int kSmemBytes = kSmallBytes + 1024 + kTilesBytes;
     static constexpr uint32_t kTmemS = 0;
     static constexpr uint32_t kTmemDP = 128;
     static constexpr uint32_t kTmemDV = 256;
@@ -169,13 +181,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     using S = Shape<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t sbase = ptx::smem_addr(smem);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kOffMisc);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kOffMisc + 4);
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + S::kSmallBytes + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = ptx::smem_addr(smem);     // 1024-aligned tiles
+    const uint32_t ssmall = ptx::smem_addr(smem_raw);  // barriers, misc, row values
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem_raw + S::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_raw + S::kOffMisc + 4);
+    const float *rows_lse = reinterpret_cast<const float *>(smem_raw + S::kOffRows);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const uint32_t bars = sbase + S::kOffBar;
+    const uint32_t bars = ssmall + S::kOffBar;
     auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
     auto wait = [&](int i, uint32_t parity) {
         return __all_sync(0xffffffffu, ptx::bar_wait(bar(i), parity, abort_flag, p.timeout_ns));
@@ -190,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S::kNumBars; ++i)
-            ptx::bar_init(bar(i), (i == S::kPFull || i == S::kDQFree || i == S::kStageReady) ? kBlock / 32 : 1u);
+            ptx::bar_init(bar(i), (i == S::kPFull || i == S::kDQFree || i == S::kStageReady) ? 2 * kBlock / 32 : 1u);
         *abort_flag = 0;
         ptx::bar_init_fence();
     }
@@ -218,22 +233,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             load_tile<D>(&tm_k, sbase + S::kOffK, bar(S::kKVFull), k0, bh);
             load_tile<D>(&tm_v, sbase + S::kOffV, bar(S::kKVFull), k0, bh);
         }
-        int it = 0;
-        for (; it < n; ++it) {
+        int nq = 0, nl = 0;  // Q/dO steps and row-value steps loaded
+        for (int it = 0; it < n; ++it) {
             const int s = it & 1;
             // stage s is free once the bulk reduction of step it-2 has read it
             if (it >= 2 && !wait(S::kStageFree + s, ((it >> 1) - 1) & 1)) break;
+            const int q0 = (qt0 + it) * kBlock;
             if (leader) {
-                const int q0 = (qt0 + it) * kBlock;
                 ptx::bar_arrive_expect_tx(bar(S::kQFull + s), 2 * S::kTileBytes);
                 load_tile<D>(&tm_q, sbase + S::kOffQ + s * S::kTileBytes, bar(S::kQFull + s), q0, bh);
                 load_tile<D>(&tm_do, sbase + S::kOffDO + s * S::kTileBytes, bar(S::kQFull + s), q0, bh);
             }
+            ++nq;
+            // the single row-value buffer is free once every compute warp has
+            // finished the previous step's P^T and dS^T (P_FULL)
+            if (it >= 1 && !wait(S::kPFull, (it - 1) & 1)) break;
+            if (leader) {
+                const size_t ro = static_cast<size_t>(bh) * p.Sq_pad + q0;
+                ptx::bar_arrive_expect_tx(bar(S::kLFull), 2 * 128 * 4);
+                ptx::bulk_load(ssmall + S::kOffRows, p.lse2 + ro, 128 * 4, bar(S::kLFull));
+                ptx::bulk_load(ssmall + S::kOffRows + 128 * 4, p.delta + ro, 128 * 4, bar(S::kLFull));
+            }
+            ++nl;
         }
         // never leave with copies in flight
         ptx::bar_wait(bar(S::kKVFull), 0, nullptr, p.timeout_ns);
-        for (int s = 0; s < 2 && s < it; ++s) {
-            const int last = (it - 1) - ((it - 1 - s) % 2);
+        if (nl > 0) ptx::bar_wait(bar(S::kLFull), (nl - 1) & 1, nullptr, p.timeout_ns);
+        for (int s = 0; s < 2 && s < nq; ++s) {
+            const int last = (nq - 1) - ((nq - 1 - s) % 2);
             ptx::bar_wait(bar(S::kQFull + s), (last >> 1) & 1, nullptr, p.timeout_ns);
         }
     } else if (warp == 1 && n > 0) {
@@ -287,10 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_ss(tmem + S::kTmemDP, ds_mn + kk * kRows16, k_mn + kk * kRows16, kIdQ, kk > 0);
                 ptx::mma_commit(bar(S::kDQFull));
                 // dV += P^T dO: 8 MMAs over the 128 queries, P^T from TMEM
+                // (queries [0,64) in columns [0,32), [64,128) in [64,96))
 #pragma unroll
                 for (int kk = 0; kk < kBlock / 16; ++kk)
-                    ptx::mma_ts(tmem + S::kTmemDV, tmem + S::kTmemS + kk * 8, do_mn + st + kk * kRows16, kIdKV,
-                                (it > 0 || kk > 0) ? 1u : 0u);
+                    ptx::mma_ts(tmem + S::kTmemDV, tmem + S::kTmemS + kk * 8 + (kk >= 4 ? 32 : 0),
+                                do_mn + st + kk * kRows16, kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
                 // dK += dS^T Q
 #pragma unroll
                 for (int kk = 0; kk < kBlock / 16; ++kk) {
@@ -305,27 +333,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) ptx::mma_commit(bar(S::kTeardown));
         __syncwarp();
         ptx::bar_wait(bar(S::kTeardown), 0, nullptr, p.timeout_ns);
-    } else if (warp >= 4 && warp < 8) {
-        // ---- key rows: P^T, dS^T; then dK, dV ----
-        const int wq = warp - 4;
-        const int r = wq * 32 + lane;  // key row within the tile
+    } else if (warp >= 4) {
+        // ---- compute warps: warpgroup h = 0, 1 owns queries [64h, 64h+64)
+        // of every key row (P^T, dS^T), then dQ_t columns [h D/2, (h+1) D/2)
+        // of every query row (to registers, releasing the TMEM columns, then
+        // staged into the step's Q/dO buffers for warp 3's bulk reductions),
+        // and at the end columns [h D/2, (h+1) D/2) of dK and dV. ----
+        const int wq = warp % 4;       // TMEM lane quarter
+        const int h = (warp - 4) / 4;
+        const int r = wq * 32 + lane;  // key row (P^T, dS^T, epilogue) or query row (dQ_t)
         const int key = k0 + r;
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t ds_row = sbase + S::kOffDS + (r >> 3) * 1024 + (r & 7) * 128;
-        const float *lse2 = p.lse2 + static_cast<size_t>(bh) * p.Sq_pad;
-        const float *delta = p.delta + static_cast<size_t>(bh) * p.Sq_pad;
+        const uint32_t row_off = (r >> 3) * 1024 + (r & 7) * 128;
         bool ok = true;
         for (int it = 0; it < n; ++it) {
-            // the query tile's 128 LSE and D values, 4 per lane, fetched
-            // (coalesced) before the wait and handed out with shuffles
+            const int s = it & 1;
             const int q0 = (qt0 + it) * kBlock;
-            const float4 lse4 = __ldg(reinterpret_cast<const float4 *>(lse2 + q0) + lane);
-            const float4 del4 = __ldg(reinterpret_cast<const float4 *>(delta + q0) + lane);
             if (!(ok = wait(S::kSFull, it & 1))) break;
+            if (!(ok = wait(S::kLFull, it & 1))) break;  // the step's LSE and D values (broadcast reads)
             if (it > 0 && !(ok = wait(S::kDSFree, (it - 1) & 1))) break;  // dS^T buffer free again
             ptx::tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < kBlock / 32; ++c) {
+            for (int cl = 0; cl < 2; ++cl) {
+                const int c = 2 * h + cl;  // 32-query chunk of the tile
                 uint32_t sv[32], dpv[32];
                 ptx::tmem_ld32(tmem + lane_base + S::kTmemS + 32 * c, sv);
                 ptx::tmem_ld32(tmem + lane_base + S::kTmemDP + 32 * c, dpv);
@@ -335,28 +366,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int qc = q0 + 32 * c;
                 const bool need_mask = (CAUSAL && key > qc) || key >= p.Sk;
                 uint32_t pp[16], dd[16];
+                const float4 *lq = reinterpret_cast<const float4 *>(rows_lse + 32 * c);
+                const float4 *dq4 = reinterpret_cast<const float4 *>(rows_lse + 128 + 32 * c);
 #pragma unroll
                 for (int j = 0; j < 32; j += 2) {
-                    float e[2], g[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        // query 32c + j + u lives in lane 8c + (j + u) / 4, component (j + u) % 4
-                        const int src = 8 * c + (j + u) / 4;
-                        const int comp = (j + u) % 4;
-                        const float l2 = __shfl_sync(0xffffffffu, comp == 0 ? lse4.x : comp == 1 ? lse4.y
-                                                                 : comp == 2 ? lse4.z : lse4.w, src);
-                        const float dl = __shfl_sync(0xffffffffu, comp == 0 ? del4.x : comp == 1 ? del4.y
-                                                                 : comp == 2 ? del4.z : del4.w, src);
-                        float pv = ptx::ex2(fmaf(__uint_as_float(sv[j + u]), p.scale_log2, -l2));
-                        if (need_mask && ((CAUSAL && key > qc + j + u) || key >= p.Sk)) pv = 0.f;
-                        e[u] = pv;
-                        g[u] = pv * (__uint_as_float(dpv[j + u]) - dl);
+                    // queries 32c + j, +1 of the tile (every lane reads the same address)
+                    const float4 lv = lq[j / 4], dv4 = dq4[j / 4];
+                    const float l0 = (j % 4 == 0) ? lv.x : lv.z, l1 = (j % 4 == 0) ? lv.y : lv.w;
+                    const float d0 = (j % 4 == 0) ? dv4.x : dv4.z, d1 = (j % 4 == 0) ? dv4.y : dv4.w;
+                    float e0 = ptx::ex2(fmaf(__uint_as_float(sv[j]), p.scale_log2, -l0));
+                    float e1 = ptx::ex2(fmaf(__uint_as_float(sv[j + 1]), p.scale_log2, -l1));
+                    if (need_mask) {
+                        if ((CAUSAL && key > qc + j) || key >= p.Sk) e0 = 0.f;
+                        if ((CAUSAL && key > qc + j + 1) || key >= p.Sk) e1 = 0.f;
                     }
-                    pp[j / 2] = ptx::pack2<BF16>(e[0], e[1]);
-                    dd[j / 2] = ptx::pack2<BF16>(g[0], g[1]);
+                    pp[j / 2] = ptx::pack2<BF16>(e0, e1);
+                    dd[j / 2] = ptx::pack2<BF16>(e0 * (__uint_as_float(dpv[j]) - d0),
+                                                 e1 * (__uint_as_float(dpv[j + 1]) - d1));
                 }
-                // P^T over S^T columns [16c, 16c+16): those hold queries already read
-                ptx::tmem_st16(tmem + lane_base + S::kTmemS + 16 * c, pp);
+                // P^T for queries [32c, 32c+32) goes to columns 64h + 16 cl: inside
+                // this half's own S^T columns, which it has already read
+                ptx::tmem_st16(tmem + lane_base + S::kTmemS + 64 * h + 16 * cl, pp);
                 // dS^T row r, queries [32c, 32c+32): box c/2, 16-byte chunks 4(c%2)..+3, 128-byte swizzle
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
@@ -370,75 +400,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::fence_proxy_async_smem();  // dS^T is read by the tensor core next
             __syncwarp();
             if (lane == 0) ptx::bar_arrive(bar(S::kPFull));
-        }
-        // epilogue: dV and scale * dK rows of this key tile
-        if (ok && n > 0) {
-            ok = wait(S::kDSFree, (n - 1) & 1);  // the last dV and dK of the loop are done
+
+            // dQ_t, this half's columns of query row r
+            if (!(ok = wait(S::kDQFull, it & 1))) break;
             ptx::tc_fence_after();
-        }
-        // The TMEM loads are warp-collective (.sync.aligned): every lane runs
-        // them; only the global stores are limited to keys that exist.
-        if (ok) {
-            const bool row_valid = key < p.Sk;
-            uint16_t *dvr = static_cast<uint16_t *>(p.dv) + (static_cast<size_t>(bh) * p.Sk + key) * D;
-            uint16_t *dkr = static_cast<uint16_t *>(p.dk) + (static_cast<size_t>(bh) * p.Sk + key) * D;
-#pragma unroll 1
-            for (int t = 0; t < 2; ++t) {
-                const float f = t == 0 ? 1.f : p.scale;
-                uint16_t *dst = t == 0 ? dvr : dkr;
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t v[32];
-                    if (n > 0) {
-                        ptx::tmem_ld32(tmem + lane_base + (t == 0 ? S::kTmemDV : S::kTmemDK) + 32 * c, v);
-                        ptx::tmem_ld_wait();
-                        ptx::reg_fence(v);
-                    } else {
+            uint32_t v[D / 64][32];
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) v[k] = 0u;
-                    }
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        pk[k] = ptx::pack2<BF16>(__uint_as_float(v[2 * k]) * f, __uint_as_float(v[2 * k + 1]) * f);
-                    if (row_valid) {
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-                    }
-                }
-            }
-        }
-    } else if (warp >= 8) {
-        // ---- query rows: dQ_t into the fp32 accumulator ----
-        // The row goes to registers (freeing the TMEM columns for the next
-        // dP^T at once), then, when dV and dK of the step are done, into the
-        // step's own Q/dO stage as four 128-byte-swizzled boxes of 32 fp32
-        // columns, which warp 3 adds to the accumulator with bulk reductions.
-        const int wq = warp - 8;
-        const int r = wq * 32 + lane;
-        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-        const uint32_t row_off = (r >> 3) * 1024 + (r & 7) * 128;
-        for (int it = 0; it < n; ++it) {
-            const int s = it & 1;
-            if (!wait(S::kDQFull, it & 1)) break;
-            ptx::tc_fence_after();
-            uint32_t v[D / 32][32];
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(tmem + lane_base + S::kTmemDP + 32 * c, v[c]);
+            for (int c = 0; c < D / 64; ++c)
+                ptx::tmem_ld32(tmem + lane_base + S::kTmemDP + h * (D / 2) + 32 * c, v[c]);
             ptx::tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) ptx::reg_fence(v[c]);
+            for (int c = 0; c < D / 64; ++c) ptx::reg_fence(v[c]);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::bar_arrive(bar(S::kDQFree));
-            if (!wait(S::kQEmpty + s, (it >> 1) & 1)) break;  // Q and dO of this step have all their readers
+            if (!(ok = wait(S::kQEmpty + s, (it >> 1) & 1))) break;  // Q and dO of this step have all their readers
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 64; ++c) {
+                const int box_i = h * (D / 64) + c;  // 32-column box of the dQ_t tile
                 // boxes [0, D/64) in the Q stage, the rest in the dO stage
-                const uint32_t box = sbase + (c < D / 64 ? S::kOffQ + s * S::kTileBytes + c * S::kBoxBytes
-                                                         : S::kOffDO + s * S::kTileBytes + (c - D / 64) * S::kBoxBytes);
+                const uint32_t box =
+                    sbase + (box_i < D / 64 ? S::kOffQ + s * S::kTileBytes + box_i * S::kBoxBytes
+                                            : S::kOffDO + s * S::kTileBytes + (box_i - D / 64) * S::kBoxBytes);
 #pragma unroll
                 for (int m = 0; m < 8; ++m)
                     st_shared_v4(box + row_off + ((m ^ (r & 7)) * 16), v[c][4 * m], v[c][4 * m + 1], v[c][4 * m + 2],
@@ -447,6 +430,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::fence_proxy_async_smem();  // the bulk reduction reads the stage next
             __syncwarp();
             if (lane == 0) ptx::bar_arrive(bar(S::kStageReady));
+        }
+        // epilogue: columns [h D/2, (h+1) D/2) of dV and scale * dK for this key row
+        if (ok && n > 0) {
+            ok = wait(S::kDSFree, (n - 1) & 1);  // the last dV and dK of the loop are done
+            ptx::tc_fence_after();
+        }
+        // The TMEM loads are warp-collective (.sync.aligned): every lane runs
+        // them; only the global stores are limited to keys that exist.
+        if (ok) {
+            const bool row_valid = key < p.Sk;
+            const size_t row_g = (static_cast<size_t>(bh) * p.Sk + key) * D + h * (D / 2);
+#pragma unroll 1
+            for (int t = 0; t < 2; ++t) {
+                const float f = t == 0 ? 1.f : p.scale;
+                uint16_t *dst = static_cast<uint16_t *>(t == 0 ? p.dv : p.dk) + row_g;
+#pragma unroll 1
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t w[32];
+                    if (n > 0) {
+                        ptx::tmem_ld32(tmem + lane_base + (t == 0 ? S::kTmemDV : S::kTmemDK) + h * (D / 2) + 32 * c,
+                                       w);
+                        ptx::tmem_ld_wait();
+                        ptx::reg_fence(w);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) w[k] = 0u;
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        pk[k] = ptx::pack2<BF16>(__uint_as_float(w[2 * k]) * f, __uint_as_float(w[2 * k + 1]) * f);
+                    if (row_valid) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                    }
+                }
+            }
         }
     } else if (warp == 3 && n > 0) {
         // ---- bulk reductions of the staged dQ_t into the accumulator ----

@@ -43,8 +43,16 @@ METRIC = "attn fwd TFLOPS & % bf16 tensor peak; split-KV decode HBM GB/s & % pea
 PREFILL = "llama_prefill"
 DECODE = "decode"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["exact_attention_54_gb300/csrc/fa_fwd_kernel.cuh", "exact_attention_54_gb300/csrc/sm103_ptx.cuh",
-                  "exact_attention_54_gb300/csrc/fa_decode.cu"]
+# The sources each captured kernel is compiled from: a committed DRAM-traffic
+# figure is reported only while these still hash to the captured ones.
+_CSRC = "exact_attention_54_gb300/csrc/"
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": [_CSRC + "fa_fwd_kernel.cuh", _CSRC + "sm103_ptx.cuh", _CSRC + "fa_launch.h"],
+    "fa_decode_split_kernel_fused": [_CSRC + "fa_decode.cu", _CSRC + "fa_launch.h"],
+    "fa_splitkv_merge_kernel": [_CSRC + "fa_decode.cu", _CSRC + "fa_launch.h"],
+    "fa_fwd_d256_kernel": [_CSRC + "fa_fwd_d256.cuh", _CSRC + "sm103_ptx.cuh", _CSRC + "fa_launch.h"],
+    "fa_bwd_kernel": [_CSRC + "fa_bwd.cu", _CSRC + "sm103_ptx.cuh", _CSRC + "fa_launch.h"],
+}
 
 
 def parse_args(argv=None):
@@ -81,25 +89,27 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def committed_traffic():
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    """Per-launch DRAM bytes from the committed ncu captures, for each kernel
+    whose sources still hash to the captured ones (others are left out)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return {}
     with open(path) as f:
         t = json.load(f)
-    if t.get("kernel_source_hash") != kernel_source_hash():
-        return {}
-    return t.get("per_launch_bytes", {})
+    out = {}
+    for name, rec in t.get("kernels", {}).items():
+        if name in KERNEL_SOURCES and rec.get("hash") == kernel_source_hash(name):
+            out[name] = rec.get("bytes")
+    return out
 
 
 def aggregate_max(values, world):
@@ -480,7 +490,6 @@ def run_two_launch(args, fa, torch, stream, flush, world, dec, ws, o, lse, wd):
     gbs = world * nbytes / ((sp + mg) * 1e-3) / 1e9
     return {"value": gbs, "unit": "GB/s", "split_ms": sp, "merge_ms": mg, "steps": n,
             "frac_of_hbm": gbs / peaks["hbm_gbs"], "split_only_gbs": world * nbytes / (sp * 1e-3) / 1e9,
-            "traffic_split": committed_traffic().get("fa_decode_split_kernel"),
             "traffic_merge": committed_traffic().get("fa_splitkv_merge_kernel")}
 
 
@@ -518,7 +527,8 @@ def run_bwd(args, fa, torch, stream, dev, flush, world, qkv, o, lse, wp):
     peaks, _ = load_peaks()
     tf = world * flops / (ms * 1e-3) / 1e12
     return {"workload": wp.name, "value": tf, "unit": "TFLOPS", "ms_per_call": ms, "steps": n,
-            "launches_per_call": 3, "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "per_call_flops": flops}
+            "launches_per_call": 3, "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "per_call_flops": flops,
+            "traffic_main_kernel": committed_traffic().get("fa_bwd_kernel")}
 
 
 def run_d256(args, fa, torch, stream, dev, flush, world):
@@ -553,7 +563,7 @@ def run_d256(args, fa, torch, stream, dev, flush, world):
     tf = world * flops / (ms * 1e-3) / 1e12
     return {"workload": w.name, "value": tf, "unit": "TFLOPS", "ms_per_launch": ms, "steps": n,
             "kernel": "fa_fwd_d256_kernel<fp16,non-causal,dense>", "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
-            "per_launch_flops": flops}
+            "per_launch_flops": flops, "traffic": committed_traffic().get("fa_fwd_d256_kernel")}
 
 
 def run_paged(args, fa, torch, stream, dev, flush, world):

@@ -189,9 +189,26 @@ __global__ void __launch_bounds__(kDecodeThreads)
     // address of row `key` of this head (dense), or nullptr offset semantics for a bad page (paged)
     const int b = bh / p.H, h = bh % p.H;
     const int *bt = PAGED ? p.block_table + static_cast<size_t>(b) * p.max_blocks : nullptr;
+    // Paged: the partition's slice of the block table is staged in shared
+    // memory once, so no key waits for a dependent table load before its K
+    // and V loads; a slice longer than the buffer is read from global memory.
+    constexpr int kTableSlots = PAGED ? 512 : 1;
+    __shared__ int sm_table[kTableSlots];
+    int blk_lo = 0;
+    bool staged = false;
+    if constexpr (PAGED) {
+        if (k_lo < k_hi) {
+            blk_lo = k_lo >> p.log2_bs;
+            const int n_ent = ((k_hi - 1) >> p.log2_bs) - blk_lo + 1;
+            staged = n_ent <= kTableSlots;  // uniform across the CTA
+            if (staged)
+                for (int i = threadIdx.x; i < n_ent; i += kDecodeThreads) sm_table[i] = bt[blk_lo + i];
+        }
+        __syncthreads();
+    }
     auto row_offset = [&](int key, bool &ok) -> size_t {
         if constexpr (PAGED) {
-            const int blk = bt[key >> p.log2_bs];
+            const int blk = staged ? sm_table[(key >> p.log2_bs) - blk_lo] : bt[key >> p.log2_bs];
             ok = static_cast<unsigned>(blk) < static_cast<unsigned>(p.num_blocks);
             const int blk_safe = ok ? blk : 0;
             return ((static_cast<size_t>(blk_safe) * p.H + h) << p.log2_bs | (key & ((1 << p.log2_bs) - 1))) * D;

@@ -66,8 +66,9 @@ struct FwdShape {
     static constexpr int kVFull = kKEmpty + kKStages;
     static constexpr int kVEmpty = kVFull + kVStages;
     static constexpr int kSFull = kVEmpty + kVStages;    // +t
-    static constexpr int kPFull = kSFull + 2;            // +t
-    static constexpr int kODone = kPFull + 2;            // +t
+    static constexpr int kPFull = kSFull + 2;            // +t: P keys [0,64) written, O corrected
+    static constexpr int kPFull2 = kPFull + 2;           // +t: P keys [64,128) written
+    static constexpr int kODone = kPFull2 + 2;           // +t
     static constexpr int kNumBars = kODone + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
@@ -293,13 +294,16 @@ __device__ void fwd_mma(const FwdParams &p, uint32_t sbase, uint32_t tmem, volat
     };
     // O_t (+)= P_t V: 128/16 MMAs of K=16; P_t from TMEM (two 16-bit values per
     // column), V MN-major: 64-column boxes 16 KB apart, 8-key atoms 1 KB apart.
-    auto issue_pv = [&](int t, uint32_t stage, bool accumulate) {
+    // half 0: keys [0,64), half 1: keys [64,128) (each published separately)
+    auto issue_pv = [&](int t, uint32_t stage, bool accumulate, int half) {
         const uint64_t vd = dv0 + static_cast<uint64_t>(stage) * kTile16;
         const uint32_t dst = tmem + S::kTmemO + t * D;
         const uint32_t pa = tmem + S::kTmemS + t * 128;
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk)
+        for (int k4 = 0; k4 < kBlockN / 32; ++k4) {
+            const int kk = half * (kBlockN / 32) + k4;
             ptx::mma_ts(dst, pa + kk * 8, vd + kk * (2048 >> 4), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+        }
     };
 
     uint32_t it = 0, wi = 0;   // K/V tiles consumed, work items consumed
@@ -342,8 +346,13 @@ __device__ void fwd_mma(const FwdParams &p, uint32_t sbase, uint32_t tmem, volat
                     v_ready = true;
                 }
                 ptx::tc_fence_after();
+                if (leader) issue_pv(t, vs, j > 0, 0);
+                // the second half of P V once the softmax has published keys [64,128)
+                if (!(ok = ptx::warp_all(ptx::bar_wait(bar(S::kPFull2 + t), cnt[t] & 1, abort_flag, p.timeout_ns))))
+                    break;
+                ptx::tc_fence_after();
                 if (leader) {
-                    issue_pv(t, vs, j > 0);
+                    issue_pv(t, vs, true, 1);
                     // the epilogue needs the last product; earlier ones are covered by S_FULL
                     if (j + 1 == wk.n_kv[t]) ptx::mma_commit(bar(S::kODone + t));
                 }
@@ -462,6 +471,8 @@ __device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, i
             const uint64_t scale2 = ptx::pk2(scale_log2, scale_log2);
             const uint64_t negm2 = ptx::pk2(-m_sub, -m_sub);
             uint64_t sum2[2] = {ptx::pk2(0.f, 0.f), ptx::pk2(0.f, 0.f)};
+            // Each half is published on its own barrier, so the tensor core
+            // starts P V on keys [0,64) while keys [64,128) are exponentiated.
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t pk[32];
@@ -478,6 +489,26 @@ __device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, i
                     pk[i] = ptx::pack2<BF16>(e0, e1);
                 }
                 ptx::tmem_st32(tS + 32 * h, pk);
+                // O *= alpha before the first half's P V accumulates into it
+                // (only when a row of this warp moved its maximum). The previous
+                // P V has landed: Q K^T j was issued after it, and S_FULL tracks
+                // every MMA issued before that Q K^T.
+                if (h == 0 && j > 0 && __any_sync(kFull, need)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32(tO + c * 32, o);
+                        ptx::tmem_ld_wait();
+                        ptx::reg_fence(o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        ptx::tmem_st32(tO + c * 32, o);
+                    }
+                }
+                ptx::tmem_st_wait();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::bar_arrive(bar((h == 0 ? S::kPFull : S::kPFull2) + t));
             }
             {
                 float a0, a1, b0, b1;
@@ -485,26 +516,6 @@ __device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, i
                 ptx::upk2(sum2[1], b0, b1);
                 l += (a0 + a1) + (b0 + b1);
             }
-
-            // O *= alpha (only when a row of this warp moved its maximum). The
-            // previous P V has landed: Q K^T j was issued after it, and S_FULL
-            // tracks every MMA issued before that Q K^T.
-            if (j > 0 && __any_sync(kFull, need)) {
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    ptx::tmem_ld32(tO + c * 32, o);
-                    ptx::tmem_ld_wait();
-                    ptx::reg_fence(o);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    ptx::tmem_st32(tO + c * 32, o);
-                }
-            }
-            ptx::tmem_st_wait();
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::bar_arrive(bar(S::kPFull + t));
             ++cnt;
         }
         if (!ok) break;
@@ -572,7 +583,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (threadIdx.x == 0) {
         const uint32_t bars = sbase + S::kOffBar;
         for (int i = 0; i < S::kNumBars; ++i) {
-            const bool p_full = (i == S::kPFull || i == S::kPFull + 1);
+            const bool p_full = i >= S::kPFull && i < S::kODone;  // P_FULL and P_FULL2
             ptx::bar_init(bars + 8u * i, p_full ? kBlockM / 32 : 1u);  // one arrival per softmax warp
         }
         *abort_flag = 0;

@@ -22,7 +22,8 @@
 //                         dV  += P^T dO    (P^T from TMEM, dO MN-major)
 //                         dK  += dS^T Q    (dS^T K-major, Q MN-major)
 //                         dQ_t = dS K      (dS^T read as an MN-major A operand)
-//                       dQ_t is issued first; the query-row warps move it to
+//                       dV and dK run chunk by chunk (32 queries) as the key-row
+//                       work publishes them; dQ_t follows; the query-row warps move it to
 //                       registers (releasing its TMEM columns), then into the
 //                       step's Q/dO stage once dV and dK are done with it, and
 //                       warp 3 adds the staged tile to the fp32 accumulator
@@ -75,15 +76,15 @@ struct Shape {
     static constexpr int kQFull = 1;    // +s
     static constexpr int kQEmpty = 3;   // +s
     static constexpr int kSFull = 5;    // S^T and dP^T written (MMA commit)
-    static constexpr int kPFull = 6;    // P^T in TMEM and dS^T in shared memory (8 warps)
-    static constexpr int kDQFull = 7;   // dQ_t in TMEM (MMA commit)
-    static constexpr int kDQFree = 8;   // dQ_t read out (8 warps)
-    static constexpr int kDSFree = 9;   // dS^T no longer read; dK and dV of the step done (MMA commit)
-    static constexpr int kStageReady = 10;  // dQ_t staged in the step's Q/dO buffers (8 warps)
-    static constexpr int kStageFree = 11;   // +s: the bulk reduction has read stage s (1 thread)
-    static constexpr int kLFull = 13;       // the step's LSE and D values are in shared memory (bulk copy)
-    static constexpr int kTeardown = 14;
-    static constexpr int kNumBars = 15;
+    static constexpr int kPChunk = 6;   // +c: P^T and dS^T of queries [32c, 32c+32) written (4 warps)
+    static constexpr int kDQFull = 10;  // dQ_t in TMEM (MMA commit)
+    static constexpr int kDQFree = 11;  // dQ_t read out (8 warps)
+    static constexpr int kDSFree = 12;  // dS^T no longer read (MMA commit after dQ_t)
+    static constexpr int kStageReady = 13;  // dQ_t staged in the step's Q/dO buffers (8 warps)
+    static constexpr int kStageFree = 14;   // +s: the bulk reduction has read stage s (1 thread)
+    static constexpr int kLFull = 16;       // the step's LSE and D values are in shared memory (bulk copy)
+    static constexpr int kTeardown = 17;
+    static constexpr int kNumBars = 18;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kOffRows = 256;                     // float lse2[128], delta[128]
     static constexpr int kSmallBytes = kOffRows + 2 * 128 * 4;
@@ -204,8 +205,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n = p.n_qtiles > qt0 ? p.n_qtiles - qt0 : 0;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < S::kNumBars; ++i)
-            ptx::bar_init(bar(i), (i == S::kPFull || i == S::kDQFree || i == S::kStageReady) ? 2 * kBlock / 32 : 1u);
+        for (int i = 0; i < S::kNumBars; ++i) {
+            uint32_t count = 1;                                              // MMA commits, TMA
+            if (i >= S::kPChunk && i < S::kPChunk + 4) count = kBlock / 32;  // the owning warpgroup
+            if (i == S::kDQFree || i == S::kStageReady) count = 2 * kBlock / 32;
+            ptx::bar_init(bar(i), count);
+        }
         *abort_flag = 0;
         ptx::bar_init_fence();
     }
@@ -246,8 +251,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++nq;
             // the single row-value buffer is free once every compute warp has
-            // finished the previous step's P^T and dS^T (P_FULL)
-            if (it >= 1 && !wait(S::kPFull, (it - 1) & 1)) break;
+            // finished the previous step's P^T and dS^T (its four chunks)
+            if (it >= 1) {
+                bool got = true;
+                for (int c = 0; c < 4 && got; ++c) got = wait(S::kPChunk + c, (it - 1) & 1);
+                if (!got) break;
+            }
             if (leader) {
                 const size_t ro = static_cast<size_t>(bh) * p.Sq_pad + q0;
                 ptx::bar_arrive_expect_tx(bar(S::kLFull), 2 * 128 * 4);
@@ -304,29 +313,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::mma_commit(bar(S::kSFull));
             }
-            if (!(ok = wait(S::kPFull, it & 1))) break;
-            ptx::tc_fence_after();
+            // dV += P^T dO and dK += dS^T Q contract over the queries: each
+            // 32-query chunk goes to the tensor core as soon as its warps have
+            // published it, overlapping the rest of the key-row work. P^T of
+            // queries [0,64) sits in columns [0,32), of [64,128) in [64,96).
+            for (int c = 0; c < 4 && ok; ++c) {
+                if (!(ok = wait(S::kPChunk + c, it & 1))) break;
+                ptx::tc_fence_after();
+                if (leader) {
+#pragma unroll
+                    for (int k2 = 0; k2 < 2; ++k2) {
+                        const int kk = 2 * c + k2;
+                        ptx::mma_ts(tmem + S::kTmemDV, tmem + S::kTmemS + kk * 8 + (kk >= 4 ? 32 : 0),
+                                    do_mn + st + kk * kRows16, kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
+                        const uint64_t off = (kk / 4) * kBox16 + (kk % 4) * 2;
+                        ptx::mma_ss(tmem + S::kTmemDK, ds_kmaj + off, q_mn + st + kk * kRows16, kIdKV,
+                                    (it > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+            }
+            if (!ok) break;
             if (leader) {
-                // dQ_t = dS K into [128,256) first (dP^T there was consumed by
-                // the key-row warps), so that its reduction overlaps dV and dK
+                ptx::mma_commit(bar(S::kQEmpty + s));  // Q and dO of this step have all their readers
+                // dQ_t = dS K (over the keys: needs every chunk) into [128,256),
+                // where dP^T was consumed by the key-row warps
 #pragma unroll
                 for (int kk = 0; kk < kBlock / 16; ++kk)
                     ptx::mma_ss(tmem + S::kTmemDP, ds_mn + kk * kRows16, k_mn + kk * kRows16, kIdQ, kk > 0);
                 ptx::mma_commit(bar(S::kDQFull));
-                // dV += P^T dO: 8 MMAs over the 128 queries, P^T from TMEM
-                // (queries [0,64) in columns [0,32), [64,128) in [64,96))
-#pragma unroll
-                for (int kk = 0; kk < kBlock / 16; ++kk)
-                    ptx::mma_ts(tmem + S::kTmemDV, tmem + S::kTmemS + kk * 8 + (kk >= 4 ? 32 : 0),
-                                do_mn + st + kk * kRows16, kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
-                // dK += dS^T Q
-#pragma unroll
-                for (int kk = 0; kk < kBlock / 16; ++kk) {
-                    const uint64_t off = (kk / 4) * kBox16 + (kk % 4) * 2;
-                    ptx::mma_ss(tmem + S::kTmemDK, ds_kmaj + off, q_mn + st + kk * kRows16, kIdKV,
-                                (it > 0 || kk > 0) ? 1u : 0u);
-                }
-                ptx::mma_commit(bar(S::kQEmpty + s));  // Q and dO of this step have all their readers
                 ptx::mma_commit(bar(S::kDSFree));
             }
         }
@@ -350,9 +364,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0; it < n; ++it) {
             const int s = it & 1;
             const int q0 = (qt0 + it) * kBlock;
+            // the step's LSE and D values and the free dS^T buffer are ready
+            // well before S^T and dP^T: wait for them first, so that only one
+            // wait separates the tensor core's commit from the key-row work
+            if (!(ok = wait(S::kLFull, it & 1))) break;
+            if (it > 0 && !(ok = wait(S::kDSFree, (it - 1) & 1))) break;
             if (!(ok = wait(S::kSFull, it & 1))) break;
-            if (!(ok = wait(S::kLFull, it & 1))) break;  // the step's LSE and D values (broadcast reads)
-            if (it > 0 && !(ok = wait(S::kDSFree, (it - 1) & 1))) break;  // dS^T buffer free again
             ptx::tc_fence_after();
 #pragma unroll 1
             for (int cl = 0; cl < 2; ++cl) {
@@ -394,12 +411,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     st_shared_v4(ds_row + (c >> 1) * S::kBoxBytes + chunk * 16, dd[4 * m], dd[4 * m + 1],
                                  dd[4 * m + 2], dd[4 * m + 3]);
                 }
+                // publish the chunk: the tensor core reads P^T (TMEM) and dS^T (smem) next
+                ptx::tmem_st_wait();
+                ptx::tc_fence_before();
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::bar_arrive(bar(S::kPChunk + c));
             }
-            ptx::tmem_st_wait();
-            ptx::tc_fence_before();
-            ptx::fence_proxy_async_smem();  // dS^T is read by the tensor core next
-            __syncwarp();
-            if (lane == 0) ptx::bar_arrive(bar(S::kPFull));
 
             // dQ_t, this half's columns of query row r
             if (!(ok = wait(S::kDQFull, it & 1))) break;

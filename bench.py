@@ -67,7 +67,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end loop (profiling runs)")
     ap.add_argument("--parts", default="prefill,decode",
                     help="comma list of the path parts to run (profiling runs may isolate one: prefill, decode, "
-                         "backward, d256)")
+                         "backward, d256, splitd)")
     return ap.parse_args(argv)
 
 
@@ -345,13 +345,16 @@ def run_gpu(args, rank, world, local):
 
     parts = set(args.parts.split(","))
     run_pf, run_dc = "prefill" in parts, "decode" in parts
-    if parts & {"backward", "d256"} and not (run_pf or run_dc):
-        # profiling run of the backward pass or of the D = 256 forward alone
+    if parts & {"backward", "d256", "splitd"} and not (run_pf or run_dc):
+        # profiling run of the backward pass or of the large-head forwards alone
         rec = {"part": args.parts, "steps": args.steps}
         if "backward" in parts:
             rec["backward"] = run_bwd(args, fa, torch, stream, dev, flush, world, (q, k, v), o, lse, wp)
         if "d256" in parts:
-            rec["d256_prefill"] = run_d256(args, fa, torch, stream, dev, flush, world)
+            rec["d256_prefill"] = run_wide_head(args, fa, torch, dev, stream, flush, world, "d256")
+        if "splitd" in parts:
+            rec["split_d"] = {key: run_wide_head(args, fa, torch, dev, stream, flush, world, key)
+                              for key in ("large_head", "massive_head")}
         if rank == 0:
             print(json.dumps(rec), flush=True)
         return None
@@ -412,7 +415,9 @@ def run_gpu(args, rank, world, local):
     prefill_tflops = world * pf_flops * K / (pf_sum * 1e-3) / 1e12
     decode_gbs = world * dc_bytes * K / (dc_sum * 1e-3) / 1e9
     two = run_two_launch(args, fa, torch, stream, flush, world, (dq, dk, dv), ws, do, dlse, wd)
-    d256 = run_d256(args, fa, torch, stream, dev, flush, world)
+    d256 = run_wide_head(args, fa, torch, dev, stream, flush, world, "d256")
+    split_d = {key: run_wide_head(args, fa, torch, dev, stream, flush, world, key)
+               for key in ("large_head", "massive_head")}
     bwd = run_bwd(args, fa, torch, stream, dev, flush, world, (q, k, v), o, lse, wp)
     paged = run_paged(args, fa, torch, stream, dev, flush, world)
     # end-to-end through host buffers (pinned), copies inside the timed region
@@ -450,6 +455,7 @@ def run_gpu(args, rank, world, local):
         "e2e": e2e["prefill"],
         "paged_decode": paged,
         "d256_prefill": d256,
+        "split_d": split_d,
         "backward": bwd,
         "gpu_launches": 2 * K,
         "clocks": clock,
@@ -531,12 +537,16 @@ def run_bwd(args, fa, torch, stream, dev, flush, world, qkv, o, lse, wp):
             "traffic_main_kernel": committed_traffic().get("fa_bwd_kernel")}
 
 
-def run_d256(args, fa, torch, stream, dev, flush, world):
-    """The pages' large-head row (1, 16, 2048, 2048, 256), fp16, non-causal:
-    the D = 256 forward kernel, timed on its own loop with the same L2 flush."""
+def run_wide_head(args, fa, torch, dev, stream, flush, world, key):
+    """The pages' large-head rows, fp16, non-causal: "GPT-4 style" (1, 16,
+    2048, 2048, 256) on the 256-column kernel, "Large Head" (1, 8, 1024, 1024,
+    512) and "Massive Head" (1, 4, 512, 512, 1024) on its Split-D form; each
+    timed on its own loop with the same L2 flush. TFLOPS count the attention
+    FLOPs (4 B H Sq Sk D); Split-D also executes Q K^T once per 256-column
+    output slice, reported as executed_tflops."""
     from exact_attention_54_gb300 import inputs
     from exact_attention_54_gb300.metrics import attention_flops
-    w = inputs.WORKLOADS["d256"]
+    w = inputs.WORKLOADS[key]
     q, k, v = (t.to(dev) for t in inputs.make_workload(w))
     o = torch.empty_like(q)
     lse = torch.empty(w.B, w.H, w.Sq, dtype=torch.float32, device=dev)
@@ -559,11 +569,18 @@ def run_d256(args, fa, torch, stream, dev, flush, world):
     fa.fa_check_device_error()
     ms = aggregate_max([sum(e[0].elapsed_time(e[1]) for e in evs) / n], world)[0]
     flops = attention_flops(w.B, w.H, w.Sq, w.Sk, w.D, w.causal)
+    slices = max(1, w.D // 256)
+    executed = flops * (slices + 1) / 2 if slices > 1 else flops
     peaks, src = load_peaks()
     tf = world * flops / (ms * 1e-3) / 1e12
-    return {"workload": w.name, "value": tf, "unit": "TFLOPS", "ms_per_launch": ms, "steps": n,
-            "kernel": "fa_fwd_d256_kernel<fp16,non-causal,dense>", "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
-            "per_launch_flops": flops, "traffic": committed_traffic().get("fa_fwd_d256_kernel")}
+    rec = {"workload": w.name, "value": tf, "unit": "TFLOPS", "ms_per_launch": ms, "steps": n,
+           "kernel": f"fa_fwd_d256_kernel<{w.D},fp16,non-causal,dense>", "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+           "per_launch_flops": flops}
+    if slices > 1:
+        rec.update(output_slices=slices, executed_tflops=world * executed / (ms * 1e-3) / 1e12)
+    else:
+        rec["traffic"] = committed_traffic().get("fa_fwd_d256_kernel")
+    return rec
 
 
 def run_paged(args, fa, torch, stream, dev, flush, world):

@@ -101,6 +101,16 @@ bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+// Forward head dimensions: 64 and 128 (two query tiles per work item), 256
+// (one), 512 and 1024 (Split-D: one query tile and 256 output columns).
+bool fwd_head_dim_ok(int D) { return D == 64 || D == 128 || D == 256 || D == 512 || D == 1024; }
+
+long long fwd_work_items(int D, long long heads, int Sq) {
+    const long long n_qtiles = (Sq + 127) / 128;
+    if (D >= 256) return heads * n_qtiles * (D / 256);
+    return heads * ((n_qtiles + 1) / 2);
+}
 constexpr int kMaxLen = 1 << 30;
 
 }  // namespace
@@ -114,7 +124,7 @@ const char *fa_status_string(fa_status_t s) {
         case FA_OK: return "ok";
         case FA_ERR_NULL: return "a required pointer is NULL";
         case FA_ERR_SHAPE: return "invalid or too large tensor shape";
-        case FA_ERR_HEADDIM: return "unsupported head dimension (forward: 64, 128, 256; decode: 64, 128)";
+        case FA_ERR_HEADDIM: return "unsupported head dimension (forward: 64, 128, 256, 512, 1024; decode and backward: 64, 128)";
         case FA_ERR_DTYPE: return "dtype must be FA_FP16 or FA_BF16";
         case FA_ERR_ALIGN: return "tensor pointer is not 16-byte aligned";
         case FA_ERR_SPLITS: return "num_splits must be in [1, min(Sk, FA_MAX_SPLITS)]";
@@ -132,18 +142,19 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *
                    int D, int causal, float scale, fa_dtype_t dtype, void *stream) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
     if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_DTYPE;
-    if (D != 64 && D != 128 && D != 256) return FA_ERR_HEADDIM;
+    if (!fwd_head_dim_ok(D)) return FA_ERR_HEADDIM;
     if (B < 1 || H < 1 || Sq < 1 || Sk < 1 || Sq > kMaxLen || Sk > kMaxLen) return FA_ERR_SHAPE;
     const long long BH = static_cast<long long>(B) * H;
     const long long n_pairs = ((Sq + 127) / 128 + 1) / 2;
-    if (BH > INT_MAX || BH * n_pairs > INT_MAX) return FA_ERR_SHAPE;
+    const long long n_work = fwd_work_items(D, BH, Sq);
+    if (BH > INT_MAX || n_work > INT_MAX) return FA_ERR_SHAPE;
     if (!scale_ok(scale)) return FA_ERR_SCALE;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse)) return FA_ERR_ALIGN;
 
     const bool bf16 = dtype == FA_BF16;
     CUtensorMap maps[3];
     const uint64_t row = static_cast<uint64_t>(D) * 2;
-    const uint32_t kv_rows = D == 256 ? 64 : 128;  // K/V tile height of the kernel that runs
+    const uint32_t kv_rows = D >= 256 ? 64 : 128;  // K/V tile height of the kernel that runs
     if (!encode_map(&maps[0], bf16, q, D, Sq, BH, row, row * Sq, 128, 1) ||
         !encode_map(&maps[1], bf16, k, D, Sk, BH, row, row * Sk, kv_rows, 1) ||
         !encode_map(&maps[2], bf16, v, D, Sk, BH, row, row * Sk, kv_rows, 1))
@@ -162,14 +173,15 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *
     p.total_q = 0;
     p.n_pairs = static_cast<int>(n_pairs);
     p.n_qtiles = (Sq + 127) / 128;
-    p.num_work = static_cast<int>(D == 256 ? BH * p.n_qtiles : BH * n_pairs);
+    p.num_work = static_cast<int>(n_work);
     p.scale_log2 = scale * kLog2e;
     p.err = err;
     p.timeout_ns = fa::kWaitTimeoutNs;
     const int grid = p.num_work < sms ? p.num_work : sms;
-    const cudaError_t e =
-        D == 256 ? fa::launch_fwd_d256(bf16, causal != 0, false, maps, p, grid, static_cast<cudaStream_t>(stream))
-                 : fa::launch_fwd_dense(D, bf16, causal != 0, maps, p, grid, static_cast<cudaStream_t>(stream));
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = D > 256    ? fa::launch_fwd_splitd(D, bf16, causal != 0, false, maps, p, grid, st)
+                          : D == 256 ? fa::launch_fwd_d256(bf16, causal != 0, false, maps, p, grid, st)
+                                     : fa::launch_fwd_dense(D, bf16, causal != 0, maps, p, grid, st);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -179,13 +191,14 @@ fa_status_t fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, 
                           void *stream) {
     if (!q || !k || !v || !o || !lse || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_NULL;
     if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_DTYPE;
-    if (D != 64 && D != 128 && D != 256) return FA_ERR_HEADDIM;
+    if (!fwd_head_dim_ok(D)) return FA_ERR_HEADDIM;
     if (num_seqs < 1 || total_q < 1 || total_k < 1 || max_seqlen_q < 1 || H < 1 || max_seqlen_q > kMaxLen ||
         total_q > kMaxLen || total_k > kMaxLen)
         return FA_ERR_SHAPE;
     const long long SH = static_cast<long long>(num_seqs) * H;
     const long long n_pairs = ((max_seqlen_q + 127) / 128 + 1) / 2;
-    if (SH > INT_MAX || SH * n_pairs > INT_MAX) return FA_ERR_SHAPE;
+    const long long n_work = fwd_work_items(D, SH, max_seqlen_q);
+    if (SH > INT_MAX || n_work > INT_MAX) return FA_ERR_SHAPE;
     if (!scale_ok(scale)) return FA_ERR_SCALE;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse)) return FA_ERR_ALIGN;
 
@@ -193,7 +206,7 @@ fa_status_t fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, 
     CUtensorMap maps[3];
     const uint64_t row = static_cast<uint64_t>(D) * 2;
     const uint64_t tok = row * H;
-    const uint32_t kv_rows = D == 256 ? 64 : 128;
+    const uint32_t kv_rows = D >= 256 ? 64 : 128;
     if (!encode_map(&maps[0], bf16, q, D, H, total_q, row, tok, 1, 128) ||
         !encode_map(&maps[1], bf16, k, D, H, total_k, row, tok, 1, kv_rows) ||
         !encode_map(&maps[2], bf16, v, D, H, total_k, row, tok, 1, kv_rows))
@@ -214,14 +227,15 @@ fa_status_t fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, 
     p.total_q = total_q;
     p.n_pairs = static_cast<int>(n_pairs);
     p.n_qtiles = (max_seqlen_q + 127) / 128;
-    p.num_work = static_cast<int>(D == 256 ? SH * p.n_qtiles : SH * n_pairs);
+    p.num_work = static_cast<int>(n_work);
     p.scale_log2 = scale * kLog2e;
     p.err = err;
     p.timeout_ns = fa::kWaitTimeoutNs;
     const int grid = p.num_work < sms ? p.num_work : sms;
-    const cudaError_t e =
-        D == 256 ? fa::launch_fwd_d256(bf16, causal != 0, true, maps, p, grid, static_cast<cudaStream_t>(stream))
-                 : fa::launch_fwd_varlen(D, bf16, causal != 0, maps, p, grid, static_cast<cudaStream_t>(stream));
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = D > 256    ? fa::launch_fwd_splitd(D, bf16, causal != 0, true, maps, p, grid, st)
+                          : D == 256 ? fa::launch_fwd_d256(bf16, causal != 0, true, maps, p, grid, st)
+                                     : fa::launch_fwd_varlen(D, bf16, causal != 0, maps, p, grid, st);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

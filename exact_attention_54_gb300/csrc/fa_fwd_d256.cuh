@@ -1,4 +1,4 @@
-// FlashAttention-2 forward for head dimension 256 on sm_103a.
+// FlashAttention-2 forward for head dimensions 256, 512 and 1024 on sm_103a.
 //
 // Same method as the D <= 128 kernel ("FlashAttention-2 MMA", Technical
 // Details; "Adaptive High-Performance Attention Kernels in CUDA",
@@ -24,6 +24,20 @@
 // V, warps 4..7 softmax (one query row per thread). Q K^T is 16 MMAs of
 // 128x64x16 per K tile; P V is 4 MMAs of 128x256x16 per V tile with P read
 // from TMEM.
+//
+// Head dimensions above 256 (the pages' "Large Head" (1, 8, 1024, 1024, 512)
+// and "Massive Head" (1, 4, 512, 512, 1024) rows) take the Split-D strategy
+// ("Adaptive High-Performance Attention Kernels in CUDA", Supported Dispatch
+// Strategies 3: the head dimension is partitioned across thread blocks). A
+// work item is one query tile and one 256-column slice of the output: the
+// CTA forms the full S = Q K^T (the contraction runs over all DQK columns)
+// and accumulates only its slice O[:, 256 s : 256 s + 256] = P V[:, slice],
+// so O still fits TMEM next to the two S buffers. Every slice of a tile sees
+// the same S, the same masking and the same arithmetic, so the row statistics
+// agree bit for bit; slice 0 writes the LSE. Q no longer fits shared memory
+// (128 x 1024 x 2 B = 256 KB), so Q and K travel together through the ring,
+// 128 columns at a time (a 48 KB stage: 32 KB of Q, 16 KB of K); the Q
+// re-reads per K tile are served by L2, which the slices of a tile share.
 #pragma once
 
 #include <cuda.h>
@@ -36,23 +50,32 @@
 namespace fa {
 namespace d256 {
 
-constexpr int D = 256;
+constexpr int D = 256;            // output columns per work item (the whole row at DQK = 256)
 constexpr int kBlockM = 128;      // query rows per tile
 constexpr int kBlockN = 64;       // keys per K/V tile
 constexpr int kThreads = 256;     // 8 warps
 constexpr float kRescaleThreshold = 8.0f;
 
+template <int DQK>
 struct Shape {
-    static constexpr int kColBlocks = D / 64;             // 64-column (128-byte) boxes per row
+    static_assert(DQK % D == 0 && DQK >= D && DQK <= 1024, "head dimension");
+    static constexpr bool kStream = DQK > D;              // Split-D: Q streams with K
+    static constexpr int kSlices = DQK / D;               // 256-column output slices per query tile
+    static constexpr int kColBlocks = D / 64;             // 64-column (128-byte) boxes per slice row
     static constexpr int kQBoxBytes = kBlockM * 128;      // 128 rows x 64 columns
     static constexpr int kKVBoxBytes = kBlockN * 128;     // 64 rows x 64 columns
-    static constexpr int kQTileBytes = kBlockM * D * 2;   // 64 KB
-    static constexpr int kKVTileBytes = kBlockN * D * 2;  // 32 KB
+    static constexpr int kQTileBytes = kStream ? 0 : kBlockM * D * 2;  // resident Q: 64 KB
+    static constexpr int kKVTileBytes = kBlockN * D * 2;  // V tile of one slice: 32 KB
+    // One ring stage: a K tile (resident Q), or 128 columns of Q and of K.
+    static constexpr int kChunkCols = kStream ? 128 : D;
+    static constexpr int kChunks = DQK / kChunkCols;      // ring stages per S tile
+    static constexpr int kStageK = kStream ? kBlockM * kChunkCols * 2 : 0;  // K's offset in a stage
+    static constexpr int kStageBytes = kStageK + kBlockN * kChunkCols * 2;
     static constexpr int kKStages = 3;
     static constexpr int kVStages = 2;
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kQTileBytes;
-    static constexpr int kOffV = kOffK + kKStages * kKVTileBytes;
+    static constexpr int kOffV = kOffK + kKStages * kStageBytes;
     static constexpr int kOffBar = kOffV + kVStages * kKVTileBytes;
     static constexpr int kQFull = 0, kQEmpty = 1, kTeardown = 2;
     static constexpr int kKFull = 3;
@@ -71,9 +94,11 @@ struct Shape {
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
-// One unit of work: one 128-row query tile of one (sequence, head).
+// One unit of work: one 128-row query tile of one (sequence, head) and, for
+// DQK > 256, one 256-column slice of its output.
 struct Work {
     int b, h;
+    int slice;           // output columns [256 slice, 256 slice + 256)
     int seq_q0, seq_k0;  // token offsets of the sequence (varlen), else 0
     int Lq, Lk;          // query and key lengths of the sequence
     int q_start;         // first query row of the tile (relative to the sequence)
@@ -81,12 +106,15 @@ struct Work {
     int n_kv;            // K/V tiles the tile visits
 };
 
-template <bool CAUSAL, bool VARLEN>
+template <int DQK, bool CAUSAL, bool VARLEN>
 __device__ __forceinline__ Work get_work(const FwdParams &p, int w) {
+    constexpr int NS = Shape<DQK>::kSlices;
     Work k;
-    const int BH = p.B * p.H;
-    const int qt = p.n_qtiles - 1 - w / BH;  // longest causal work first
-    const int bh = w % BH;
+    const int units = p.B * p.H * NS;
+    const int qt = p.n_qtiles - 1 - w / units;  // longest causal work first
+    const int u = w % units;                    // the slices of a tile run side by side
+    const int bh = u / NS;
+    k.slice = u % NS;
     k.b = bh / p.H;
     k.h = bh % p.H;
     if constexpr (VARLEN) {
@@ -124,16 +152,17 @@ __device__ __forceinline__ int work_index(int r) {
     return r * G + pos;
 }
 
-// Rows [row0, row0 + rows) of (sequence/head) into `dst`, one box per 64 columns.
-template <bool VARLEN>
+// Columns [col0, col0 + 64 NBOX) of rows [row0, row0 + box rows) of
+// (sequence/head) into `dst`, one box per 64 columns.
+template <int NBOX, bool VARLEN>
 __device__ __forceinline__ void load_rows(const CUtensorMap *tm, uint32_t dst, uint32_t box_bytes, uint32_t bar,
-                                          const Work &wk, int seq0, int row0, int H) {
+                                          const Work &wk, int seq0, int row0, int H, int col0) {
 #pragma unroll
-    for (int c = 0; c < Shape::kColBlocks; ++c) {
+    for (int c = 0; c < NBOX; ++c) {
         if constexpr (VARLEN)
-            ptx::tma_load_3d(dst + c * box_bytes, tm, bar, c * 64, wk.h, seq0 + row0);
+            ptx::tma_load_3d(dst + c * box_bytes, tm, bar, col0 + c * 64, wk.h, seq0 + row0);
         else
-            ptx::tma_load_3d(dst + c * box_bytes, tm, bar, c * 64, row0, wk.b * H + wk.h);
+            ptx::tma_load_3d(dst + c * box_bytes, tm, bar, col0 + c * 64, row0, wk.b * H + wk.h);
     }
 }
 
@@ -146,10 +175,11 @@ __device__ __forceinline__ void drain_ring(uint32_t full0, uint32_t stages, uint
     }
 }
 
-template <bool CAUSAL, bool VARLEN>
+template <int DQK, bool CAUSAL, bool VARLEN>
 __device__ void producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, const FwdParams &p, uint32_t sbase,
                             volatile int *abort_flag) {
-    using S = Shape;
+    using S = Shape<DQK>;
+    constexpr int kBoxes = S::kChunkCols / 64;
     const uint32_t bars = sbase + S::kOffBar;
     auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
     auto wait = [&](int i, uint32_t parity) {
@@ -161,15 +191,16 @@ __device__ void producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, const 
     for (int r = 0; ok; ++r) {
         const int w = work_index(r);
         if (w >= p.num_work) break;
-        const Work wk = get_work<CAUSAL, VARLEN>(p, w);
+        const Work wk = get_work<DQK, CAUSAL, VARLEN>(p, w);
         if (wk.n_kv == 0) continue;
-        if (wi > 0 && !(ok = wait(S::kQEmpty, (wi - 1) & 1))) break;
-        if (leader) {
+        if (!S::kStream && wi > 0 && !(ok = wait(S::kQEmpty, (wi - 1) & 1))) break;
+        if (!S::kStream && leader) {
             ptx::bar_arrive_expect_tx(bar(S::kQFull), S::kQTileBytes);
-            load_rows<VARLEN>(tq, sbase + S::kOffQ, S::kQBoxBytes, bar(S::kQFull), wk, wk.seq_q0, wk.q_start, p.H);
+            load_rows<S::kColBlocks, VARLEN>(tq, sbase + S::kOffQ, S::kQBoxBytes, bar(S::kQFull), wk, wk.seq_q0,
+                                             wk.q_start, p.H, 0);
             const int wn = work_index(r + 1);
             if (wn < p.num_work) {
-                const Work nx = get_work<CAUSAL, VARLEN>(p, wn);
+                const Work nx = get_work<DQK, CAUSAL, VARLEN>(p, wn);
                 if (nx.n_kv > 0) {
 #pragma unroll
                     for (int c = 0; c < S::kColBlocks; ++c) {
@@ -181,24 +212,30 @@ __device__ void producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, const 
                 }
             }
         }
-        for (int j = 0; j < wk.n_kv; ++j, ++it) {
-            const uint32_t stage = it % S::kKStages;
-            if (it >= S::kKStages && !(ok = wait(S::kKEmpty + stage, ((it / S::kKStages) - 1) & 1))) break;
-            if (leader) {
-                ptx::bar_arrive_expect_tx(bar(S::kKFull + stage), S::kKVTileBytes);
-                load_rows<VARLEN>(tk, sbase + S::kOffK + stage * S::kKVTileBytes, S::kKVBoxBytes,
-                                  bar(S::kKFull + stage), wk, wk.seq_k0, j * kBlockN, p.H);
+        for (int j = 0; j < wk.n_kv && ok; ++j) {
+            for (int c = 0; c < S::kChunks; ++c, ++it) {
+                const uint32_t stage = it % S::kKStages;
+                if (it >= S::kKStages && !(ok = wait(S::kKEmpty + stage, ((it / S::kKStages) - 1) & 1))) break;
+                if (leader) {
+                    const uint32_t dst = sbase + S::kOffK + stage * S::kStageBytes;
+                    ptx::bar_arrive_expect_tx(bar(S::kKFull + stage), S::kStageBytes);
+                    if constexpr (S::kStream)
+                        load_rows<kBoxes, VARLEN>(tq, dst, S::kQBoxBytes, bar(S::kKFull + stage), wk, wk.seq_q0,
+                                                  wk.q_start, p.H, c * S::kChunkCols);
+                    load_rows<kBoxes, VARLEN>(tk, dst + S::kStageK, S::kKVBoxBytes, bar(S::kKFull + stage), wk,
+                                              wk.seq_k0, j * kBlockN, p.H, c * S::kChunkCols);
+                }
             }
         }
         ++wi;
     }
     drain_ring(bar(S::kKFull), S::kKStages, it, p.timeout_ns);
-    drain_ring(bar(S::kQFull), 1, wi, p.timeout_ns);
+    if (!S::kStream) drain_ring(bar(S::kQFull), 1, wi, p.timeout_ns);
 }
 
-template <bool CAUSAL, bool VARLEN>
+template <int DQK, bool CAUSAL, bool VARLEN>
 __device__ void producer_v(const CUtensorMap *tv, const FwdParams &p, uint32_t sbase, volatile int *abort_flag) {
-    using S = Shape;
+    using S = Shape<DQK>;
     const uint32_t bars = sbase + S::kOffBar;
     auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
     const bool leader = ptx::elect_one();
@@ -207,7 +244,7 @@ __device__ void producer_v(const CUtensorMap *tv, const FwdParams &p, uint32_t s
     for (int r = 0; ok; ++r) {
         const int w = work_index(r);
         if (w >= p.num_work) break;
-        const Work wk = get_work<CAUSAL, VARLEN>(p, w);
+        const Work wk = get_work<DQK, CAUSAL, VARLEN>(p, w);
         for (int j = 0; j < wk.n_kv; ++j, ++it) {
             const uint32_t stage = it % S::kVStages;
             if (it >= S::kVStages &&
@@ -216,17 +253,18 @@ __device__ void producer_v(const CUtensorMap *tv, const FwdParams &p, uint32_t s
                 break;
             if (leader) {
                 ptx::bar_arrive_expect_tx(bar(S::kVFull + stage), S::kKVTileBytes);
-                load_rows<VARLEN>(tv, sbase + S::kOffV + stage * S::kKVTileBytes, S::kKVBoxBytes,
-                                  bar(S::kVFull + stage), wk, wk.seq_k0, j * kBlockN, p.H);
+                load_rows<S::kColBlocks, VARLEN>(tv, sbase + S::kOffV + stage * S::kKVTileBytes, S::kKVBoxBytes,
+                                                 bar(S::kVFull + stage), wk, wk.seq_k0, j * kBlockN, p.H,
+                                                 wk.slice * D);
             }
         }
     }
     drain_ring(bar(S::kVFull), S::kVStages, it, p.timeout_ns);
 }
 
-template <bool BF16, bool CAUSAL, bool VARLEN>
+template <int DQK, bool BF16, bool CAUSAL, bool VARLEN>
 __device__ void mma_role(const FwdParams &p, uint32_t sbase, uint32_t tmem, volatile int *abort_flag) {
-    using S = Shape;
+    using S = Shape<DQK>;
     constexpr uint32_t kIdescQK = ptx::idesc_f16(BF16, kBlockM, kBlockN, false);
     constexpr uint32_t kIdescPV = ptx::idesc_f16(BF16, kBlockM, D, true);
     const uint32_t bars = sbase + S::kOffBar;
@@ -242,23 +280,30 @@ __device__ void mma_role(const FwdParams &p, uint32_t sbase, uint32_t tmem, vola
     const uint64_t dk0 = ptx::smem_desc_sw128(sbase + S::kOffK, 16, 1024);
     const uint64_t dv0 = ptx::smem_desc_sw128(sbase + S::kOffV, S::kKVBoxBytes, 1024);
     constexpr uint64_t kKVTile16 = S::kKVTileBytes >> 4;
+    constexpr uint64_t kStage16 = S::kStageBytes >> 4;
 
-    // S = Q K^T for tile t into S buffer t mod 2 (16 MMAs of K = 16).
+    // S = Q K^T for tile t into S buffer t mod 2: DQK / 16 MMAs of K = 16,
+    // over kChunks ring stages (Q from the stage too when it streams).
     auto qk = [&](uint32_t t) -> bool {
-        const uint32_t ks = t % S::kKStages;
-        if (!wait(S::kKFull + ks, (t / S::kKStages) & 1)) return false;
-        if (leader) {
-            const uint64_t kd = dk0 + static_cast<uint64_t>(ks) * kKVTile16;
-            const uint32_t dst = tmem + S::kTmemS + (t & 1) * kBlockN;
+        const uint32_t dst = tmem + S::kTmemS + (t & 1) * kBlockN;
+        for (int c = 0; c < S::kChunks; ++c) {
+            const uint32_t u = t * S::kChunks + c;
+            const uint32_t ks = u % S::kKStages;
+            if (!wait(S::kKFull + ks, (u / S::kKStages) & 1)) return false;
+            if (leader) {
+                const uint64_t sd = dk0 + static_cast<uint64_t>(ks) * kStage16;
+                const uint64_t qd = S::kStream ? sd : dq;
+                const uint64_t kd = sd + (S::kStageK >> 4);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t qo = (kk / 4) * (S::kQBoxBytes >> 4) + (kk % 4) * 2;
-                const uint64_t ko = (kk / 4) * (S::kKVBoxBytes >> 4) + (kk % 4) * 2;
-                ptx::mma_ss(dst, dq + qo, kd + ko, kIdescQK, kk > 0);
+                for (int kk = 0; kk < S::kChunkCols / 16; ++kk) {
+                    const uint64_t qo = (kk / 4) * (S::kQBoxBytes >> 4) + (kk % 4) * 2;
+                    const uint64_t ko = (kk / 4) * (S::kKVBoxBytes >> 4) + (kk % 4) * 2;
+                    ptx::mma_ss(dst, qd + qo, kd + ko, kIdescQK, (c > 0 || kk > 0) ? 1u : 0u);
+                }
+                ptx::mma_commit(bar(S::kKEmpty + ks));
             }
-            ptx::mma_commit(bar(S::kSFull + (t & 1)));
-            ptx::mma_commit(bar(S::kKEmpty + ks));
         }
+        if (leader) ptx::mma_commit(bar(S::kSFull + (t & 1)));
         return true;
     };
     // O (+)= P V for tile t (4 MMAs of K = 16 keys, N = 256).
@@ -286,20 +331,21 @@ __device__ void mma_role(const FwdParams &p, uint32_t sbase, uint32_t tmem, vola
     for (int r = 0; ok; ++r) {
         const int w = work_index(r);
         if (w >= p.num_work) break;
-        const Work wk = get_work<CAUSAL, VARLEN>(p, w);
+        const Work wk = get_work<DQK, CAUSAL, VARLEN>(p, w);
         const int n = wk.n_kv;
         if (n == 0) continue;
-        if (!(ok = wait(S::kQFull, wi & 1))) break;
+        if (!S::kStream && !(ok = wait(S::kQFull, wi & 1))) break;
         const uint32_t g0 = g;
         if (!(ok = qk(g0))) break;
         if (n > 1 && !(ok = qk(g0 + 1))) break;
-        if (n <= 2 && leader) ptx::mma_commit(bar(S::kQEmpty));  // every Q K^T of this tile issued
+        // every Q K^T of this tile issued: the resident Q may be replaced
+        if (!S::kStream && n <= 2 && leader) ptx::mma_commit(bar(S::kQEmpty));
         for (int i = 0; i < n && ok; ++i) {
             const uint32_t t = g0 + i;
             if (!(ok = pv(t, i > 0))) break;
             if (i + 2 < n) {
                 if (!(ok = qk(t + 2))) break;
-                if (i + 3 == n && leader) ptx::mma_commit(bar(S::kQEmpty));
+                if (!S::kStream && i + 3 == n && leader) ptx::mma_commit(bar(S::kQEmpty));
             }
         }
         if (!ok) break;
@@ -311,10 +357,10 @@ __device__ void mma_role(const FwdParams &p, uint32_t sbase, uint32_t tmem, vola
     ptx::bar_wait(bar(S::kTeardown), 0, nullptr, p.timeout_ns);
 }
 
-template <bool BF16, bool CAUSAL, bool VARLEN>
+template <int DQK, bool BF16, bool CAUSAL, bool VARLEN>
 __device__ void softmax_role(const FwdParams &p, uint32_t sbase, uint32_t tmem, int wq, int lane,
                              volatile int *abort_flag) {
-    using S = Shape;
+    using S = Shape<DQK>;
     using Elem = uint16_t;
     const uint32_t bars = sbase + S::kOffBar;
     auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
@@ -332,7 +378,7 @@ __device__ void softmax_role(const FwdParams &p, uint32_t sbase, uint32_t tmem, 
     for (int r = 0; ok; ++r) {
         const int w = work_index(r);
         if (w >= p.num_work) break;
-        const Work wk = get_work<CAUSAL, VARLEN>(p, w);
+        const Work wk = get_work<DQK, CAUSAL, VARLEN>(p, w);
         const int n = wk.n_kv;
         if (n == 0) continue;
         const int q_row = wk.q_start + row;
@@ -436,11 +482,12 @@ __device__ void softmax_role(const FwdParams &p, uint32_t sbase, uint32_t tmem, 
             ptx::tc_fence_after();
         }
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
-        Elem *orow;
+        Elem *orow;  // this slice's 256 columns of the output row
         if constexpr (VARLEN)
-            orow = static_cast<Elem *>(p.o) + (static_cast<size_t>(wk.seq_q0 + q_row) * p.H + wk.h) * D;
+            orow = static_cast<Elem *>(p.o) + (static_cast<size_t>(wk.seq_q0 + q_row) * p.H + wk.h) * DQK;
         else
-            orow = static_cast<Elem *>(p.o) + (static_cast<size_t>(wk.b * p.H + wk.h) * p.Sq + q_row) * D;
+            orow = static_cast<Elem *>(p.o) + (static_cast<size_t>(wk.b * p.H + wk.h) * p.Sq + q_row) * DQK;
+        orow += wk.slice * D;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
@@ -457,7 +504,7 @@ __device__ void softmax_role(const FwdParams &p, uint32_t sbase, uint32_t tmem, 
                 for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
             }
         }
-        if (row_valid) {
+        if (row_valid && wk.slice == 0) {
             const float lse = l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
             if constexpr (VARLEN)
                 p.lse[static_cast<size_t>(wk.h) * p.total_q + wk.seq_q0 + q_row] = lse;
@@ -470,11 +517,11 @@ __device__ void softmax_role(const FwdParams &p, uint32_t sbase, uint32_t tmem, 
     }
 }
 
-template <bool BF16, bool CAUSAL, bool VARLEN>
+template <int DQK, bool BF16, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_d256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-    using S = Shape;
+    using S = Shape<DQK>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_addr(smem);
@@ -507,13 +554,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        producer_qk<CAUSAL, VARLEN>(&tm_q, &tm_k, p, sbase, abort_flag);
+        producer_qk<DQK, CAUSAL, VARLEN>(&tm_q, &tm_k, p, sbase, abort_flag);
     } else if (warp == 1) {
-        mma_role<BF16, CAUSAL, VARLEN>(p, sbase, tmem, abort_flag);
+        mma_role<DQK, BF16, CAUSAL, VARLEN>(p, sbase, tmem, abort_flag);
     } else if (warp == 2) {
-        producer_v<CAUSAL, VARLEN>(&tm_v, p, sbase, abort_flag);
+        producer_v<DQK, CAUSAL, VARLEN>(&tm_v, p, sbase, abort_flag);
     } else if (warp >= 4) {
-        softmax_role<BF16, CAUSAL, VARLEN>(p, sbase, tmem, warp - 4, lane, abort_flag);
+        softmax_role<DQK, BF16, CAUSAL, VARLEN>(p, sbase, tmem, warp - 4, lane, abort_flag);
     }
 
     ptx::tc_fence_before();
@@ -526,10 +573,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && *abort_flag) atomicExch(p.err, kDeviceErrTimeout);
 }
 
-template <bool BF16, bool CAUSAL, bool VARLEN>
+template <int DQK, bool BF16, bool CAUSAL, bool VARLEN>
 cudaError_t launch(const CUtensorMap *maps, const FwdParams &p, int grid, cudaStream_t stream) {
-    auto kern = fa_fwd_d256_kernel<BF16, CAUSAL, VARLEN>;
-    constexpr int kSmem = Shape::kSmemBytes;
+    auto kern = fa_fwd_d256_kernel<DQK, BF16, CAUSAL, VARLEN>;
+    constexpr int kSmem = Shape<DQK>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, kSmem, stream>>>(maps[0], maps[1], maps[2], p);

@@ -29,7 +29,7 @@ struct FwdParams {
     int total_q;           // varlen: LSE row stride of one head
     int n_pairs;           // query-tile pairs per (sequence, head): ceil(ceil(Sq/128)/2)
     int n_qtiles;          // 128-row query tiles per (sequence, head): ceil(Sq/128)
-    int num_work;          // work items: n_pairs * B * H (D <= 128) or n_qtiles * B * H (D = 256)
+    int num_work;          // work items: n_pairs * B * H (D <= 128), n_qtiles * B * H * D / 256 (D >= 256)
     float scale_log2;      // scale * log2(e)
     int *err;              // device error word
     unsigned long long timeout_ns;
@@ -83,6 +83,10 @@ cudaError_t launch_fwd_varlen(int D, bool bf16, bool causal, const CUtensorMap *
 // D = 256: one query tile per work item; maps: Q boxes of 128 rows, K/V boxes of 64.
 cudaError_t launch_fwd_d256(bool bf16, bool causal, bool varlen, const CUtensorMap *maps, const FwdParams &p,
                             int grid, cudaStream_t stream);
+// D = 512, 1024 (Split-D): one query tile and one 256-column output slice per
+// work item; same maps (boxes of 64 columns; 128 rows for Q, 64 for K/V).
+cudaError_t launch_fwd_splitd(int D, bool bf16, bool causal, bool varlen, const CUtensorMap *maps,
+                              const FwdParams &p, int grid, cudaStream_t stream);
 
 cudaError_t launch_decode_split(int D, bool bf16, const void *q, const void *k, const void *v,
                                 float *o_part, float *m_part, float *l_part, int BH, int Sk,

@@ -58,6 +58,12 @@ WORKLOADS = {
     # printed TFLOPS match the non-causal FLOP count; fp16 (the page's T4 has
     # no bf16)
     "d256": Workload("gpt4style_b1h16s2048d256_fp16", "dense", 1, 16, 2048, 2048, 256, torch.float16, False, 1007),
+    # the pages' Split-D rows, "Large Head" (1, 8, 1024, 1024, 512) and
+    # "Massive Head" (1, 4, 512, 512, 1024), non-causal fp16 like the row above
+    "large_head": Workload("large_head_b1h8s1024d512_fp16", "dense", 1, 8, 1024, 1024, 512, torch.float16, False,
+                           1008),
+    "massive_head": Workload("massive_head_b1h4s512d1024_fp16", "dense", 1, 4, 512, 512, 1024, torch.float16, False,
+                             1009),
     "paged_decode": Workload("paged_decode_b16h8sk8192d128_bf16_block16_split32", "paged", 16, 8, 1, 8192, 128,
                              torch.bfloat16, False, 1006, num_splits=32, extra={"block_size": 16}),
 }

@@ -67,7 +67,8 @@ def test_fwd_validation(lib):
     assert _fwd(lib, lse=None) == NULL
     assert _fwd(lib, dtype=2) == DTYPE
     assert _fwd(lib, D=96) == HEADDIM
-    assert _fwd(lib, D=512) == HEADDIM
+    for d in (384, 768, 2048):  # Split-D serves 512 and 1024 only
+        assert _fwd(lib, D=d) == HEADDIM, d
     for kw in ({"B": 0}, {"H": 0}, {"Sq": 0}, {"Sk": 0}, {"Sq": -5}, {"Sk": (1 << 30) + 1}):
         assert _fwd(lib, **kw) == SHAPE, kw
     assert _fwd(lib, B=1 << 16, H=1 << 16) == SHAPE  # B*H overflows 32-bit work indexing

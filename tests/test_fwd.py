@@ -60,6 +60,14 @@ SHAPES = [
     (2, 1, 129, 500, 256, torch.bfloat16, False),
     (1, 2, 77, 300, 256, torch.float16, True),
     (2, 2, 640, 640, 256, torch.bfloat16, True),
+    # D = 512, 1024 (Split-D: 256-column output slices, Q and K streamed)
+    (1, 1, 1, 1, 512, torch.float16, True),
+    (1, 2, 300, 300, 512, torch.bfloat16, True),
+    (2, 1, 129, 500, 512, torch.float16, False),
+    (1, 1, 1, 1, 1024, torch.bfloat16, False),
+    (1, 2, 200, 77, 1024, torch.float16, False),
+    (1, 1, 77, 300, 1024, torch.bfloat16, True),
+    (1, 2, 640, 640, 1024, torch.bfloat16, True),
 ]
 
 
@@ -90,7 +98,33 @@ def test_d256_workload_full_size_sampled_rows():
     check(q, k, v, True, w.scale, rows=rows, what=w.name + " causal")
 
 
-@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("key", ["large_head", "massive_head"])
+def test_split_d_workloads_full_size(key):
+    """The pages' Split-D rows at full size, every row against the oracle,
+    non-causal as printed and causal."""
+    w = inputs.WORKLOADS[key]
+    q, k, v = inputs.make_workload(w)
+    check(q, k, v, w.causal, w.scale, what=w.name)
+    check(q, k, v, True, w.scale, what=w.name + " causal")
+
+
+@pytest.mark.parametrize("D", [512, 1024])
+def test_split_d_slices_share_row_statistics(D):
+    """Every 256-column slice of a Split-D tile recomputes S = Q K^T over the
+    whole head dimension: with V's slices all equal, the slices of O must be
+    equal bit for bit (same P, same max, same sum in every CTA)."""
+    q, k, v = inputs.make_dense(1, 2, 300, 400, D, torch.bfloat16, seed=17)
+    v = v[..., :256].repeat(1, 1, 1, D // 256).contiguous()
+    for causal in (False, True):
+        o, lse = run(q, k, v, causal, 1.0 / D ** 0.5)
+        for s in range(1, D // 256):
+            assert torch.equal(o[..., :256].view(torch.int16), o[..., 256 * s:256 * s + 256].view(torch.int16))
+        ro, rl = oracle.attention(q, k, v, causal, 1.0 / D ** 0.5)
+        assert_close(o, ro, O_TOL, f"O D={D} causal={causal}")
+        assert_close(lse, rl, LSE_TOL, f"LSE D={D} causal={causal}")
+
+
+@pytest.mark.parametrize("D", [128, 256, 512])
 def test_causal_skipped_tiles_never_read(D):
     """Causal, Sq = 256 < Sk = 512: keys 256.. are above every row's diagonal,
     so their tiles are skipped. NaN there must not change a single bit."""
@@ -104,7 +138,7 @@ def test_causal_skipped_tiles_never_read(D):
     assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
 
 
-@pytest.mark.parametrize("D", [64, 256])
+@pytest.mark.parametrize("D", [64, 256, 1024])
 def test_causal_mask_inside_diagonal_tiles_is_exact(D):
     """Rows [0, r) of a causal run depend on keys [0, r) only. With huge K/V
     values planted in keys [r, S) (masked inside the straddling tile), rows
@@ -127,7 +161,7 @@ def test_ragged_key_tail_is_masked():
     check(q, k, v, False, 0.125, what="ragged key tail")
 
 
-@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("D", [128, 256, 512])
 def test_outputs_do_not_spill_past_the_buffer(D):
     B, H, Sq = 1, 2, 200
     q, k, v = dev(*inputs.make_dense(B, H, Sq, Sq, D, torch.bfloat16, seed=14))

@@ -23,7 +23,8 @@ def run_varlen(q, k, v, cu, causal, scale):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("D,dtype", [(64, torch.float16), (128, torch.bfloat16), (256, torch.float16)])
+@pytest.mark.parametrize("D,dtype", [(64, torch.float16), (128, torch.bfloat16), (256, torch.float16),
+                                     (512, torch.bfloat16)])
 def test_small_varlen_all_rows(causal, D, dtype):
     lengths = [1, 127, 128, 129, 0, 300, 5]
     _, cu, q, k, v = inputs.make_varlen(len(lengths), 0, 0, 3, D, dtype, seed=21, lengths=lengths)
@@ -34,7 +35,7 @@ def test_small_varlen_all_rows(causal, D, dtype):
     assert_close(lse, rl, LSE_TOL, "varlen LSE")
 
 
-@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("D", [128, 256, 1024])
 def test_varlen_equals_dense_per_sequence_bitwise(D):
     lengths = [200, 1, 384, 129, 77]
     H = 4

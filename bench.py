@@ -51,6 +51,8 @@ KERNEL_SOURCES = {
     "fa_decode_split_kernel_fused": [_CSRC + "fa_decode.cu", _CSRC + "fa_launch.h"],
     "fa_splitkv_merge_kernel": [_CSRC + "fa_decode.cu", _CSRC + "fa_launch.h"],
     "fa_fwd_d256_kernel": [_CSRC + "fa_fwd_d256.cuh", _CSRC + "sm103_ptx.cuh", _CSRC + "fa_launch.h"],
+    "fa_fwd_d256_kernel_d512": [_CSRC + "fa_fwd_d256.cuh", _CSRC + "sm103_ptx.cuh", _CSRC + "fa_launch.h"],
+    "fa_fwd_d256_kernel_d1024": [_CSRC + "fa_fwd_d256.cuh", _CSRC + "sm103_ptx.cuh", _CSRC + "fa_launch.h"],
     "fa_bwd_kernel": [_CSRC + "fa_bwd.cu", _CSRC + "sm103_ptx.cuh", _CSRC + "fa_launch.h"],
 }
 
@@ -578,8 +580,7 @@ def run_wide_head(args, fa, torch, dev, stream, flush, world, key):
            "per_launch_flops": flops}
     if slices > 1:
         rec.update(output_slices=slices, executed_tflops=world * executed / (ms * 1e-3) / 1e12)
-    else:
-        rec["traffic"] = committed_traffic().get("fa_fwd_d256_kernel")
+    rec["traffic"] = committed_traffic().get("fa_fwd_d256_kernel" + (f"_d{w.D}" if slices > 1 else ""))
     return rec
 
 

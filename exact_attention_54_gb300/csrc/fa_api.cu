@@ -81,14 +81,14 @@ bool encode_map(CUtensorMap *m, bool bf16, const void *base, uint64_t d0, uint64
     return r == CUDA_SUCCESS;
 }
 
-// 3-D map over the fp32 dQ accumulator [B*H][Sq][D] with 32 x 128 x 1 boxes
+// 3-D map over the fp32 dQ accumulator [B*H][Sq][D] with 32 x rows x 1 boxes
 // and 128-byte swizzle: the target of the backward pass's bulk reductions.
-bool encode_map_f32(CUtensorMap *m, void *base, uint64_t D, uint64_t Sq, uint64_t BH) {
+bool encode_map_f32(CUtensorMap *m, void *base, uint64_t D, uint64_t Sq, uint64_t BH, uint32_t rows) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint64_t dims[3] = {D, Sq, BH};
     const cuuint64_t strides[2] = {D * 4, D * 4 * Sq};
-    const cuuint32_t box[3] = {32, 128, 1};
+    const cuuint32_t box[3] = {32, rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -416,11 +416,12 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
     const bool bf16 = dtype == FA_BF16;
     CUtensorMap maps[5];
     const uint64_t row = static_cast<uint64_t>(D) * 2;
-    if (!encode_map(&maps[0], bf16, q, D, Sq, BH, row, row * Sq, 128, 1) ||
+    const uint32_t q_rows = D == 128 ? 64 : 128;  // query rows per step of the kernel that runs
+    if (!encode_map(&maps[0], bf16, q, D, Sq, BH, row, row * Sq, q_rows, 1) ||
         !encode_map(&maps[1], bf16, k, D, Sk, BH, row, row * Sk, 128, 1) ||
         !encode_map(&maps[2], bf16, v, D, Sk, BH, row, row * Sk, 128, 1) ||
-        !encode_map(&maps[3], bf16, dout, D, Sq, BH, row, row * Sq, 128, 1) ||
-        !encode_map_f32(&maps[4], workspace, D, Sq, BH))
+        !encode_map(&maps[3], bf16, dout, D, Sq, BH, row, row * Sq, q_rows, 1) ||
+        !encode_map_f32(&maps[4], workspace, D, Sq, BH, q_rows))
         return FA_ERR_CUDA;
     int *err = device_error_word();
     if (err == nullptr) return FA_ERR_CUDA;

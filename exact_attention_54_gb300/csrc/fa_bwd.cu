@@ -11,9 +11,10 @@
 //   fa_bwd_prep_kernel  per query row: D_i, the LSE in base 2 (padded to whole
 //                       128-row tiles with +inf, which zeroes P there), and a
 //                       zeroed fp32 dQ accumulator row.
-//   fa_bwd_kernel       one CTA per (head, 128-key tile), looping over the
-//                       query tiles that see those keys (causal: from the
-//                       diagonal on). Per query tile, on the tensor core:
+//   fa_bwd_d64_kernel   (D = 64) one CTA per (head, 128-key tile), looping
+//                       over the query tiles that see those keys (causal:
+//                       from the diagonal on). Per query tile, on the tensor
+//                       core:
 //                         S^T  = K Q^T     (TMEM, lanes = keys)
 //                         dP^T = V dO^T    (TMEM)
 //                       the key-row warps turn them into P^T (16-bit, back into
@@ -29,9 +30,13 @@
 //                       warp 3 adds the staged tile to the fp32 accumulator
 //                       with TMA bulk tensor reductions. dK and dV stay in
 //                       TMEM for the whole loop and are written once.
+//   fa_bwd_kernel       (D = 128) the same products on 64-query sub-steps with
+//                       two TMEM buffers, so that the key-row work of one
+//                       sub-step overlaps the tensor core's products of the
+//                       next; described where it is defined below.
 //   fa_bwd_dq_kernel    dQ = scale * accumulator, in the input dtype.
 //
-// Roles of fa_bwd_kernel (384 threads): warp 0 TMA producer (K, V once; Q and
+// Roles of fa_bwd_d64_kernel (384 threads): warp 0 TMA producer (K, V once; Q and
 // dO double-buffered), warp 1 MMA issuer and TMEM owner, warp 3 bulk
 // reductions of dQ_t, warps 4..11 two warpgroups that split every step by
 // halves: warpgroup h computes P^T and dS^T for queries [64h, 64h+64) of each
@@ -178,7 +183,7 @@ __device__ __forceinline__ void load_tile(const CUtensorMap *tm, uint32_t dst, u
 
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
-    fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    fa_bwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     using S = Shape<D>;
@@ -522,6 +527,424 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && *abort_flag) atomicExch(p.err, kDeviceErrTimeout);
 }
 
+
+// ------------------------------------------- main kernel, head dimension 128 --
+//
+// D = 128 runs the same products on 64-query sub-steps so that the tensor
+// core and the key-row warps overlap: TMEM holds dV [0,128) and dK [128,256)
+// plus two sub-step buffers b = 0, 1 at 256 + 128 b, each S^T (64 columns;
+// P^T of queries [32h, 32h+32) packed over its own first 16) and dP^T (64
+// columns, then dQ_t^T). While the key-row warps turn buffer b into P^T and
+// dS^T, the tensor core already forms S^T and dP^T of the next sub-step in
+// the other buffer. dQ_t is produced transposed, dQ_t^T = K^T dS^T (K read
+// as an MN-major A operand, dS^T as an MN-major B operand), so its M side is
+// the 128 head columns and no 64-row MMA is needed; each compute thread then
+// owns one head column and stages it into the fp32 tile that warp 2 adds to
+// the accumulator with TMA bulk tensor reductions.
+//
+// Roles (512 threads): warp 0 TMA producer (K, V once; Q, dO and the step's
+// LSE/D rows in a ring of 3), warp 1 MMA issuer and TMEM owner, warp 2 bulk
+// reductions, warps 4..11 two warpgroups: warpgroup h handles queries
+// [32h, 32h+32) of every sub-step (P^T, dS^T) and, at the end, head columns
+// [64h, 64h+64) of dK and dV; warps 12..15 move each dQ_t^T out of TMEM
+// (releasing the buffer for the next S^T/dP^T) and stage it, off the key-row
+// warps' path.
+constexpr int kThreadsQ64 = 512;
+
+struct ShapeQ64 {
+    static constexpr int D = 128;
+    static constexpr int kQ = 64;                        // queries per sub-step
+    static constexpr int kKTileBytes = kBlock * D * 2;   // K or V: 32 KB (2 boxes of 128 rows x 64 columns)
+    static constexpr int kKBoxBytes = kBlock * 128;
+    static constexpr int kQTileBytes = kQ * D * 2;       // Q_j or dO_j: 16 KB (2 boxes of 64 rows x 64 columns)
+    static constexpr int kQBoxBytes = kQ * 128;
+    static constexpr int kStages = 3;
+    static constexpr int kStageBytes = 2 * kQTileBytes;  // Q_j then dO_j
+    static constexpr int kDSBytes = kBlock * kQ * 2;     // dS^T [128 keys][64 queries]: one 16 KB box
+    static constexpr int kDQBoxBytes = kQ * 128;         // 64 query rows x 32 fp32 head columns
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kOffK + kKTileBytes;
+    static constexpr int kOffQ = kOffV + kKTileBytes;    // + stage * kStageBytes
+    static constexpr int kOffDS = kOffQ + kStages * kStageBytes;  // + b * kDSBytes
+    static constexpr int kOffDQ = kOffDS + 2 * kDSBytes;          // dQ_t staging, 4 boxes
+    static constexpr int kTilesBytes = kOffDQ + 4 * kDQBoxBytes;
+    // small region: barriers, TMEM base and abort flag, then per stage the
+    // sub-step's 64 base-2 LSE values and 64 D values
+    static constexpr int kKVFull = 0;
+    static constexpr int kQFull = 1;       // +stage: Q_j, dO_j and the rows landed (TMA)
+    static constexpr int kQEmpty = 4;      // +stage: dV_j and dK_j done with them (MMA commit)
+    static constexpr int kSFull = 7;       // +b: S^T and dP^T of the buffer written (MMA commit)
+    static constexpr int kPFull = 9;       // +b: P^T and dS^T written (8 warps)
+    static constexpr int kDQFull = 11;     // +b: dQ_t^T written (MMA commit)
+    static constexpr int kBufFree = 13;    // +b: dQ_t^T read out, the buffer's dP^T columns free (4 warps)
+    static constexpr int kDSFree = 15;     // +b: products of the buffer done: P^T, dS^T no longer read (MMA commit)
+    static constexpr int kStageReady = 17; // dQ_t staged (4 warps)
+    static constexpr int kStageFree = 18;  // the bulk reductions have read the staging tile (1 thread)
+    static constexpr int kTeardown = 19;
+    static constexpr int kPTFree = 20;     // +b: dV of the buffer done, its S^T columns free (MMA commit)
+    static constexpr int kNumBars = 22;
+    static constexpr int kOffMisc = kNumBars * 8;
+    static constexpr int kOffRows = 256;   // + stage * 512: float lse2[64], delta[64]
+    static constexpr int kSmallBytes = kOffRows + kStages * 2 * kQ * 4;
+    static_assert(kOffMisc + 16 <= kOffRows, "small region layout");
+    static constexpr int kSmemBytes = kSmallBytes + 1024 + kTilesBytes;
+    static constexpr uint32_t kTmemDV = 0;
+    static constexpr uint32_t kTmemDK = 128;
+    static constexpr uint32_t kTmemBuf = 256;  // + 128 b: S^T [0,64), dP^T / dQ_t^T [64,128)
+    static constexpr uint32_t kTmemCols = 512;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+template <bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kThreadsQ64, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+    using S = ShapeQ64;
+    constexpr int D = S::D;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + S::kSmallBytes + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = ptx::smem_addr(smem);
+    const uint32_t ssmall = ptx::smem_addr(smem_raw);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem_raw + S::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_raw + S::kOffMisc + 4);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    auto bar = [&](int i) { return ssmall + 8u * static_cast<uint32_t>(i); };
+    auto wait = [&](int i, uint32_t parity) {
+        return __all_sync(0xffffffffu, ptx::bar_wait(bar(i), parity, abort_flag, p.timeout_ns));
+    };
+
+    // work item: key tile kt of head bh, heavy causal tiles first; sub-steps of
+    // 64 queries from the first query that sees any of these keys
+    const int kt = static_cast<int>(blockIdx.x) / p.BH;
+    const int bh = static_cast<int>(blockIdx.x) % p.BH;
+    const int k0 = kt * kBlock;
+    const int qs0 = CAUSAL ? k0 : 0;
+    const int n = p.Sq > qs0 ? (p.Sq - qs0 + S::kQ - 1) / S::kQ : 0;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S::kNumBars; ++i) {
+            uint32_t count = 1;  // MMA commits, TMA, the reduction thread
+            if (i >= S::kPFull && i < S::kPFull + 2) count = 2 * kBlock / 32;  // the key-row warps
+            if ((i >= S::kBufFree && i < S::kBufFree + 2) || i == S::kStageReady) count = kBlock / 32;  // dQ warps
+            if (i == S::kTeardown) count = 2;  // one commit per MMA-issuing warp
+            ptx::bar_init(bar(i), count);
+        }
+        *abort_flag = 0;
+        ptx::bar_init_fence();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tm_q);
+        ptx::prefetch_tmap(&tm_k);
+        ptx::prefetch_tmap(&tm_v);
+        ptx::prefetch_tmap(&tm_do);
+        ptx::prefetch_tmap(&tm_dq);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), S::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && n > 0) {
+        // ---- TMA producer ----
+        const bool leader = ptx::elect_one();
+        if (leader) {
+            ptx::bar_arrive_expect_tx(bar(S::kKVFull), 2 * S::kKTileBytes);
+            for (int c = 0; c < 2; ++c) {
+                ptx::tma_load_3d(sbase + S::kOffK + c * S::kKBoxBytes, &tm_k, bar(S::kKVFull), c * 64, k0, bh);
+                ptx::tma_load_3d(sbase + S::kOffV + c * S::kKBoxBytes, &tm_v, bar(S::kKVFull), c * 64, k0, bh);
+            }
+        }
+        int nq = 0;
+        for (int j = 0; j < n; ++j) {
+            const int st = j % S::kStages;
+            if (j >= S::kStages && !wait(S::kQEmpty + st, ((j / S::kStages) - 1) & 1)) break;
+            const int q0 = qs0 + j * S::kQ;
+            if (leader) {
+                const uint32_t qb = sbase + S::kOffQ + st * S::kStageBytes;
+                const uint32_t rows = ssmall + S::kOffRows + st * 2 * S::kQ * 4;
+                const size_t ro = static_cast<size_t>(bh) * p.Sq_pad + q0;
+                ptx::bar_arrive_expect_tx(bar(S::kQFull + st), S::kStageBytes + 2 * S::kQ * 4);
+                for (int c = 0; c < 2; ++c) {
+                    ptx::tma_load_3d(qb + c * S::kQBoxBytes, &tm_q, bar(S::kQFull + st), c * 64, q0, bh);
+                    ptx::tma_load_3d(qb + S::kQTileBytes + c * S::kQBoxBytes, &tm_do, bar(S::kQFull + st), c * 64,
+                                     q0, bh);
+                }
+                ptx::bulk_load(rows, p.lse2 + ro, S::kQ * 4, bar(S::kQFull + st));
+                ptx::bulk_load(rows + S::kQ * 4, p.delta + ro, S::kQ * 4, bar(S::kQFull + st));
+            }
+            ++nq;
+        }
+        // never leave with copies in flight
+        ptx::bar_wait(bar(S::kKVFull), 0, nullptr, p.timeout_ns);
+        for (int st = 0; st < S::kStages && st < nq; ++st) {
+            const int last = (nq - 1) - ((nq - 1 - st) % S::kStages);
+            ptx::bar_wait(bar(S::kQFull + st), (last / S::kStages) & 1, nullptr, p.timeout_ns);
+        }
+    } else if ((warp == 1 || warp == 3) && n > 0) {
+        // ---- MMA issuers: warp 1 forms S^T and dP^T of each sub-step, warp 3
+        // the products of the sub-step before it. A warp blocks in
+        // tcgen05.mma while the tensor core's queue (a few MMAs) is full, so
+        // one issuer alone starves the pipe at every barrier wait; with two,
+        // one keeps the queue filled while the other waits. ----
+        const bool leader = ptx::elect_one();
+        constexpr uint32_t kIdS = ptx::idesc_f16(BF16, kBlock, S::kQ, false);        // S^T, dP^T: N = 64 queries
+        constexpr uint32_t kIdKV = ptx::idesc_f16(BF16, kBlock, D, true);            // dV, dK: B MN-major
+        constexpr uint32_t kIdQ = ptx::idesc_f16(BF16, D, S::kQ, true, true);       // dQ_t^T: A, B MN-major
+        constexpr uint64_t kKBox16 = S::kKBoxBytes >> 4, kQBox16 = S::kQBoxBytes >> 4;
+        constexpr uint64_t kStage16 = S::kStageBytes >> 4, kDS16 = S::kDSBytes >> 4, kRows16 = 2048 >> 4;
+        bool ok = wait(S::kKVFull, 0);
+        if (warp == 1) {
+            const uint64_t k_kmaj = ptx::smem_desc_sw128(sbase + S::kOffK, 16, 1024);
+            const uint64_t v_kmaj = ptx::smem_desc_sw128(sbase + S::kOffV, 16, 1024);
+            const uint64_t q_kmaj = ptx::smem_desc_sw128(sbase + S::kOffQ, 16, 1024);
+            const uint64_t do_kmaj = ptx::smem_desc_sw128(sbase + S::kOffQ + S::kQTileBytes, 16, 1024);
+            for (int j = 0; j < n && ok; ++j) {
+                const int st = j % S::kStages, b = j & 1;
+                // S^T: Q_j landed and the buffer's P^T of sub-step j-2 consumed by its dV
+                const bool ready = ptx::bar_try_wait(bar(S::kQFull + st), (j / S::kStages) & 1) &&
+                                   (j < 2 || ptx::bar_try_wait(bar(S::kPTFree + b), ((j - 2) >> 1) & 1));
+                if (!__all_sync(0xffffffffu, ready)) {
+                    if (!(ok = wait(S::kQFull + st, (j / S::kStages) & 1))) break;
+                    if (j >= 2 && !(ok = wait(S::kPTFree + b, ((j - 2) >> 1) & 1))) break;
+                }
+                ptx::tc_fence_after();
+                const uint64_t so = static_cast<uint64_t>(st) * kStage16;
+                const uint32_t tb = tmem + S::kTmemBuf + 128 * b;
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t ka = (kk / 4) * kKBox16 + (kk % 4) * 2;
+                        const uint64_t qa = (kk / 4) * kQBox16 + (kk % 4) * 2;
+                        ptx::mma_ss(tb, k_kmaj + ka, q_kmaj + so + qa, kIdS, kk > 0);
+                    }
+                }
+                // dP^T: the buffer's dQ_t^T of sub-step j-2 read out
+                if (j >= 2 && !(ok = wait(S::kBufFree + b, ((j - 2) >> 1) & 1))) break;
+                ptx::tc_fence_after();
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t ka = (kk / 4) * kKBox16 + (kk % 4) * 2;
+                        const uint64_t qa = (kk / 4) * kQBox16 + (kk % 4) * 2;
+                        ptx::mma_ss(tb + 64, v_kmaj + ka, do_kmaj + so + qa, kIdS, kk > 0);
+                    }
+                    ptx::mma_commit(bar(S::kSFull + b));
+                }
+                __syncwarp();
+            }
+        } else {
+            const uint64_t k_mn = ptx::smem_desc_sw128(sbase + S::kOffK, S::kKBoxBytes, 1024);
+            const uint64_t q_mn = ptx::smem_desc_sw128(sbase + S::kOffQ, S::kQBoxBytes, 1024);
+            const uint64_t do_mn = ptx::smem_desc_sw128(sbase + S::kOffQ + S::kQTileBytes, S::kQBoxBytes, 1024);
+            const uint64_t ds_kmaj = ptx::smem_desc_sw128(sbase + S::kOffDS, 16, 1024);
+            const uint64_t ds_mn = ptx::smem_desc_sw128(sbase + S::kOffDS, S::kDSBytes, 1024);
+            for (int j = 0; j < n && ok; ++j) {
+                const int st = j % S::kStages, b = j & 1;
+                if (!(ok = wait(S::kPFull + b, (j >> 1) & 1))) break;
+                ptx::tc_fence_after();
+                if (leader) {
+                    const uint64_t so = static_cast<uint64_t>(st) * kStage16;
+                    const uint32_t tb = tmem + S::kTmemBuf + 128 * b;
+                    // dQ_t^T = K^T dS^T over the 128 keys, into the buffer's dP^T
+                    // columns, first: its read-out frees them for sub-step j+2
+#pragma unroll
+                    for (int kk = 0; kk < kBlock / 16; ++kk)
+                        ptx::mma_ss(tb + 64, k_mn + kk * kRows16, ds_mn + b * kDS16 + kk * kRows16, kIdQ, kk > 0);
+                    ptx::mma_commit(bar(S::kDQFull + b));
+                    // dV += P^T dO over the 64 queries (P^T of queries [32h, 32h+32)
+                    // in columns [32h, 32h+16) of the buffer): frees the S^T columns
+#pragma unroll
+                    for (int kk = 0; kk < S::kQ / 16; ++kk)
+                        ptx::mma_ts(tmem + S::kTmemDV, tb + kk * 8 + (kk >= 2 ? 16 : 0), do_mn + so + kk * kRows16,
+                                    kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
+                    ptx::mma_commit(bar(S::kPTFree + b));
+                    // dK += dS^T Q
+#pragma unroll
+                    for (int kk = 0; kk < S::kQ / 16; ++kk)
+                        ptx::mma_ss(tmem + S::kTmemDK, ds_kmaj + b * kDS16 + kk * 2, q_mn + so + kk * kRows16, kIdKV,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+                    ptx::mma_commit(bar(S::kQEmpty + st));  // Q_j and dO_j have all their readers
+                    ptx::mma_commit(bar(S::kDSFree + b));   // and so has dS^T of buffer b
+                }
+                __syncwarp();
+            }
+        }
+        // each issuer waits for its own MMAs before the CTA may free TMEM
+        if (leader) ptx::mma_commit(bar(S::kTeardown));
+        __syncwarp();
+        ptx::bar_wait(bar(S::kTeardown), 0, nullptr, p.timeout_ns);
+    } else if (warp >= 4 && warp < 12) {
+        // ---- key-row warps ----
+        const int wq = warp % 4;       // TMEM lane quarter
+        const int h = (warp - 4) / 4;  // query half of every sub-step
+        const int r = wq * 32 + lane;  // key row
+        const int key = k0 + r;
+        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t ds_row = sbase + S::kOffDS + (r >> 3) * 1024 + (r & 7) * 128;
+        bool ok = true;
+        for (int j = 0; j < n; ++j) {
+            const int st = j % S::kStages, b = j & 1;
+            const int qc = qs0 + j * S::kQ + 32 * h;  // first query of this warp's chunk
+            const uint32_t tb = tmem + lane_base + S::kTmemBuf + 128 * b;
+            // the stage's rows, then S^T and dP^T: one test of both first,
+            // the bounded waits only when one is open
+            const bool ready = ptx::bar_try_wait(bar(S::kSFull + b), (j >> 1) & 1) &&
+                               ptx::bar_try_wait(bar(S::kQFull + st), (j / S::kStages) & 1);
+            if (!__all_sync(0xffffffffu, ready)) {
+                if (!(ok = wait(S::kQFull + st, (j / S::kStages) & 1))) break;
+                if (!(ok = wait(S::kSFull + b, (j >> 1) & 1))) break;
+            }
+            ptx::tc_fence_after();
+            uint32_t sv[32], dpv[32];
+            ptx::tmem_ld32(tb + 32 * h, sv);
+            ptx::tmem_ld32(tb + 64 + 32 * h, dpv);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence(sv);
+            ptx::reg_fence(dpv);
+            const bool need_mask = (CAUSAL && key > qc) || key >= p.Sk;
+            const float *rows = reinterpret_cast<const float *>(smem_raw + S::kOffRows + st * 2 * S::kQ * 4);
+            const float4 *lq = reinterpret_cast<const float4 *>(rows + 32 * h);
+            const float4 *dq4 = reinterpret_cast<const float4 *>(rows + S::kQ + 32 * h);
+            uint32_t pp[16], dd[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const float4 lv = lq[i / 4], dv4 = dq4[i / 4];
+                const float l0 = (i % 4 == 0) ? lv.x : lv.z, l1 = (i % 4 == 0) ? lv.y : lv.w;
+                const float d0 = (i % 4 == 0) ? dv4.x : dv4.z, d1 = (i % 4 == 0) ? dv4.y : dv4.w;
+                float e0 = ptx::ex2(fmaf(__uint_as_float(sv[i]), p.scale_log2, -l0));
+                float e1 = ptx::ex2(fmaf(__uint_as_float(sv[i + 1]), p.scale_log2, -l1));
+                if (need_mask) {
+                    if ((CAUSAL && key > qc + i) || key >= p.Sk) e0 = 0.f;
+                    if ((CAUSAL && key > qc + i + 1) || key >= p.Sk) e1 = 0.f;
+                }
+                pp[i / 2] = ptx::pack2<BF16>(e0, e1);
+                dd[i / 2] = ptx::pack2<BF16>(e0 * (__uint_as_float(dpv[i]) - d0),
+                                             e1 * (__uint_as_float(dpv[i + 1]) - d1));
+            }
+            // P^T over the first 16 of this half's own S^T columns
+            ptx::tmem_st16(tb + 32 * h, pp);
+            // dS^T buffer b is free once sub-step j-2's dQ_t^T and dK have read it
+            if (j >= 2 && !(ok = wait(S::kDSFree + b, ((j - 2) >> 1) & 1))) break;
+            // dS^T row r, queries [32h, 32h+32): 16-byte chunks 4h..4h+3, 128-byte swizzle
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t chunk = static_cast<uint32_t>((4 * h + m) ^ (r & 7));
+                st_shared_v4(ds_row + b * S::kDSBytes + chunk * 16, dd[4 * m], dd[4 * m + 1], dd[4 * m + 2],
+                             dd[4 * m + 3]);
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::fence_proxy_async_smem();  // dS^T is read by the tensor core next
+            __syncwarp();
+            if (lane == 0) ptx::bar_arrive(bar(S::kPFull + b));
+        }
+        // epilogue: head columns [64h, 64h+64) of dV and scale * dK for this key row
+        if (ok && n > 0) {
+            ok = wait(S::kDSFree + ((n - 1) & 1), ((n - 1) >> 1) & 1);  // the last dV and dK are done
+            ptx::tc_fence_after();
+        }
+        // The TMEM loads are warp-collective (.sync.aligned): every lane runs
+        // them; only the global stores are limited to keys that exist.
+        if (ok) {
+            const bool row_valid = key < p.Sk;
+            const size_t row_g = (static_cast<size_t>(bh) * p.Sk + key) * D + h * (D / 2);
+#pragma unroll 1
+            for (int t = 0; t < 2; ++t) {
+                const float f = t == 0 ? 1.f : p.scale;
+                uint16_t *dst = static_cast<uint16_t *>(t == 0 ? p.dv : p.dk) + row_g;
+#pragma unroll 1
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t w[32];
+                    if (n > 0) {
+                        ptx::tmem_ld32(tmem + lane_base + (t == 0 ? S::kTmemDV : S::kTmemDK) + h * (D / 2) + 32 * c,
+                                       w);
+                        ptx::tmem_ld_wait();
+                        ptx::reg_fence(w);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) w[k] = 0u;
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        pk[k] = ptx::pack2<BF16>(__uint_as_float(w[2 * k]) * f, __uint_as_float(w[2 * k + 1]) * f);
+                    if (row_valid) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                    }
+                }
+            }
+        }
+    } else if (warp >= 12 && n > 0) {
+        // ---- dQ_t^T warps: head column r, all 64 queries of the sub-step ----
+        const int wq = warp % 4;
+        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+        // head column r = 32 wq + lane of the staging tile: box wq, 4-byte word lane
+        const uint32_t dq_col = sbase + S::kOffDQ + wq * S::kDQBoxBytes + (lane & 3) * 4;
+        for (int j = 0; j < n; ++j) {
+            const int b = j & 1;
+            if (!wait(S::kDQFull + b, (j >> 1) & 1)) break;
+            ptx::tc_fence_after();
+            uint32_t v0[32], v1[32];
+            const uint32_t tb = tmem + lane_base + S::kTmemBuf + 128 * b + 64;
+            ptx::tmem_ld32(tb, v0);
+            ptx::tmem_ld32(tb + 32, v1);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence(v0);
+            ptx::reg_fence(v1);
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::bar_arrive(bar(S::kBufFree + b));
+            if (j >= 1 && !wait(S::kStageFree, (j - 1) & 1)) break;  // the last reduction has read the tile
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const uint32_t chunk = static_cast<uint32_t>((lane >> 2) ^ (i & 7));
+                asm volatile("st.shared.b32 [%0], %1;" ::"r"(dq_col + i * 128 + chunk * 16),
+                             "r"(i < 32 ? v0[i] : v1[i - 32])
+                             : "memory");
+            }
+            ptx::fence_proxy_async_smem();  // the bulk reduction reads the tile next
+            __syncwarp();
+            if (lane == 0) ptx::bar_arrive(bar(S::kStageReady));
+        }
+    } else if (warp == 2 && n > 0) {
+        // ---- bulk reductions of the staged dQ_t into the accumulator ----
+        const bool leader = ptx::elect_one();
+        for (int j = 0; j < n; ++j) {
+            if (!wait(S::kStageReady, j & 1)) break;
+            if (leader) {
+                const int q0 = qs0 + j * S::kQ;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c)
+                    ptx::tma_reduce_add_3d(&tm_dq, sbase + S::kOffDQ + c * S::kDQBoxBytes, 32 * c, q0, bh);
+                ptx::bulk_commit();
+                ptx::bulk_wait_read_all();  // the staging tile may be rewritten now
+                ptx::bar_arrive(bar(S::kStageFree));
+            }
+            __syncwarp();
+        }
+        if (leader) ptx::bulk_wait_all();  // the reductions themselves are complete
+        __syncwarp();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, S::kTmemCols);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicExch(p.err, kDeviceErrTimeout);
+}
+
 template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch_t(const CUtensorMap *maps, const void *o, const void *dout, const float *lse, void *dq,
                      const BwdParams &p, cudaStream_t st) {
@@ -530,12 +953,13 @@ cudaError_t launch_t(const CUtensorMap *maps, const void *o, const void *dout, c
         static_cast<const uint16_t *>(o), static_cast<const uint16_t *>(dout), lse, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    auto kern = fa_bwd_kernel<D, BF16, CAUSAL>;
-    constexpr int kSmem = Shape<D>::kSmemBytes;
+    // D = 64: 128-query steps; D = 128: 64-query sub-steps, double-buffered in TMEM
+    auto kern = D == 64 ? fa_bwd_d64_kernel<64, BF16, CAUSAL> : fa_bwd_kernel<BF16, CAUSAL>;
+    constexpr int kSmem = D == 64 ? Shape<64>::kSmemBytes : ShapeQ64::kSmemBytes;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(p.BH * p.n_ktiles), kThreads, kSmem, st>>>(maps[0], maps[1], maps[2], maps[3],
-                                                                             maps[4], p);
+    kern<<<static_cast<unsigned>(p.BH * p.n_ktiles), D == 64 ? kThreads : kThreadsQ64, kSmem, st>>>(
+        maps[0], maps[1], maps[2], maps[3], maps[4], p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long n8 = static_cast<long long>(p.BH) * p.Sq * D / 8;

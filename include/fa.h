@@ -22,7 +22,7 @@
  *     device arrays (cu_seqlens) are not read on the host.
  *   - 16-bit tensors are contiguous, row-major, 16-byte aligned; fp32 arrays
  *     are contiguous and 4-byte aligned. D is 64 or 128 (the forward also
- *     takes 256).
+ *     takes 256, 512 and 1024).
  *   - `scale` multiplies Q K^T before the softmax and must be finite and > 0
  *     (1/sqrt(D) is the usual value).
  *   - LSE outputs are natural-log sums over the scaled, masked scores:
@@ -52,7 +52,7 @@ typedef enum {
     FA_OK = 0,
     FA_ERR_NULL = -1,           /* a required pointer is NULL */
     FA_ERR_SHAPE = -2,          /* a size is <= 0, or too large for 32-bit indexing */
-    FA_ERR_HEADDIM = -3,        /* D not supported: forward 64/128/256, decode 64/128 */
+    FA_ERR_HEADDIM = -3,        /* D not supported: forward 64/128/256/512/1024, decode and backward 64/128 */
     FA_ERR_DTYPE = -4,          /* dtype is not FA_FP16 or FA_BF16 */
     FA_ERR_ALIGN = -5,          /* a 16-bit tensor is not 16-byte aligned (fp32: 4-byte) */
     FA_ERR_SPLITS = -6,         /* num_splits < 1 or > Sk (or > FA_MAX_SPLITS) */
@@ -83,9 +83,15 @@ typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype_t;
  *   lse  [B,H,Sq]    fp32 output
  *   causal  0 or 1. When 1, query i sees keys j <= i (top-left alignment,
  *           also when Sq != Sk).
- *   D       64, 128 or 256. D = 256 covers the pages' large-head ("GPT-4
- *           style", head_dim 256) configuration and runs a kernel with one
- *           query tile per CTA and 64-key K/V tiles (same results contract).
+ *   D       64, 128, 256, 512 or 1024. D = 256 covers the pages' large-head
+ *           ("GPT-4 style", head_dim 256) configuration and runs a kernel with
+ *           one query tile per CTA and 64-key K/V tiles. D = 512 and 1024 (the
+ *           pages' "Large Head" and "Massive Head" rows) take the Split-D
+ *           strategy ("Adaptive High-Performance Attention Kernels in CUDA",
+ *           Supported Dispatch Strategies 3: head_dim > 256 partitions the
+ *           head dimension across thread blocks): each CTA forms the full
+ *           scores and writes one 256-column slice of O. Same results
+ *           contract for every D.
  * Errors: FA_ERR_NULL, FA_ERR_SHAPE (B,H,Sq,Sk < 1), FA_ERR_HEADDIM,
  * FA_ERR_DTYPE, FA_ERR_ALIGN, FA_ERR_SCALE, FA_ERR_CUDA.
  */

@@ -542,13 +542,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // owns one head column and stages it into the fp32 tile that warp 2 adds to
 // the accumulator with TMA bulk tensor reductions.
 //
-// Roles (512 threads): warp 0 TMA producer (K, V once; Q, dO and the step's
-// LSE/D rows in a ring of 3), warp 1 MMA issuer and TMEM owner, warp 2 bulk
-// reductions, warps 4..11 two warpgroups: warpgroup h handles queries
-// [32h, 32h+32) of every sub-step (P^T, dS^T) and, at the end, head columns
+// Roles (512 threads): warp 0 TMA producer (K, V once; Q and dO in a ring of
+// 4 stages, the sub-step's LSE/D rows double-buffered), warps 1 and 3 MMA
+// issuers (warp 1 also owns TMEM), warp 2 bulk reductions, warps 4..11 two
+// warpgroups: warpgroup h handles queries [32h, 32h+32) of every sub-step
+// (P^T, dS^T) and, at the end, head columns
 // [64h, 64h+64) of dK and dV; warps 12..15 move each dQ_t^T out of TMEM
 // (releasing the buffer for the next S^T/dP^T) and stage it, off the key-row
-// warps' path.
+// warps' path, into the sub-step's own Q/dO stage once dV and dK are done with
+// it; the stage is refilled only after the bulk reductions have read it.
 constexpr int kThreadsQ64 = 512;
 
 struct ShapeQ64 {
@@ -558,34 +560,38 @@ struct ShapeQ64 {
     static constexpr int kKBoxBytes = kBlock * 128;
     static constexpr int kQTileBytes = kQ * D * 2;       // Q_j or dO_j: 16 KB (2 boxes of 64 rows x 64 columns)
     static constexpr int kQBoxBytes = kQ * 128;
-    static constexpr int kStages = 3;
-    static constexpr int kStageBytes = 2 * kQTileBytes;  // Q_j then dO_j
+    static constexpr int kStages = 4;
+    static constexpr int kStageBytes = 2 * kQTileBytes;  // Q_j then dO_j; later the sub-step's fp32 dQ_t tile
     static constexpr int kDSBytes = kBlock * kQ * 2;     // dS^T [128 keys][64 queries]: one 16 KB box
     static constexpr int kDQBoxBytes = kQ * 128;         // 64 query rows x 32 fp32 head columns
+    static_assert(4 * kDQBoxBytes == kStageBytes, "the dQ_t tile fills its sub-step's stage");
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kOffK + kKTileBytes;
     static constexpr int kOffQ = kOffV + kKTileBytes;    // + stage * kStageBytes
     static constexpr int kOffDS = kOffQ + kStages * kStageBytes;  // + b * kDSBytes
-    static constexpr int kOffDQ = kOffDS + 2 * kDSBytes;          // dQ_t staging, 4 boxes
-    static constexpr int kTilesBytes = kOffDQ + 4 * kDQBoxBytes;
-    // small region: barriers, TMEM base and abort flag, then per stage the
-    // sub-step's 64 base-2 LSE values and 64 D values
+    static constexpr int kTilesBytes = kOffDS + 2 * kDSBytes;
+    // small region: barriers, TMEM base and abort flag, then for sub-steps
+    // j mod 2 the 64 base-2 LSE values and 64 D values
     static constexpr int kKVFull = 0;
-    static constexpr int kQFull = 1;       // +stage: Q_j, dO_j and the rows landed (TMA)
-    static constexpr int kQEmpty = 4;      // +stage: dV_j and dK_j done with them (MMA commit)
-    static constexpr int kSFull = 7;       // +b: S^T and dP^T of the buffer written (MMA commit)
-    static constexpr int kPFull = 9;       // +b: P^T and dS^T written (8 warps)
-    static constexpr int kDQFull = 11;     // +b: dQ_t^T written (MMA commit)
-    static constexpr int kBufFree = 13;    // +b: dQ_t^T read out, the buffer's dP^T columns free (4 warps)
-    static constexpr int kDSFree = 15;     // +b: products of the buffer done: P^T, dS^T no longer read (MMA commit)
-    static constexpr int kStageReady = 17; // dQ_t staged (4 warps)
-    static constexpr int kStageFree = 18;  // the bulk reductions have read the staging tile (1 thread)
-    static constexpr int kTeardown = 19;
-    static constexpr int kPTFree = 20;     // +b: dV of the buffer done, its S^T columns free (MMA commit)
-    static constexpr int kNumBars = 22;
+    static constexpr int kQFull = 1;       // +stage: Q_j and dO_j landed (TMA)
+    static constexpr int kQEmpty = 5;      // +stage: dV_j and dK_j done with them (MMA commit)
+    static constexpr int kSFull = 9;       // +b: S^T and dP^T of the buffer written (MMA commit)
+    static constexpr int kPFull = 11;      // +b: P^T and dS^T written (8 warps)
+    static constexpr int kDQFull = 13;     // +b: dQ_t^T written (MMA commit)
+    static constexpr int kBufFree = 15;    // +b: dQ_t^T read out, the buffer's dP^T columns free (4 warps)
+    static constexpr int kDSFree = 17;     // +b: products of the buffer done: dS^T no longer read (MMA commit)
+    // The dQ warps may run up to a ring's length ahead of the reductions, so
+    // the hand-off between them is per stage (a single barrier waited by
+    // parity would alias phases two or more apart).
+    static constexpr int kStageReady = 19; // +stage: dQ_t staged in its sub-step's stage (4 warps)
+    static constexpr int kStageFree = 23;  // +stage: the bulk reductions have read the stage (1 thread)
+    static constexpr int kTeardown = 27;
+    static constexpr int kPTFree = 28;     // +b: dV of the buffer done, its S^T columns free (MMA commit)
+    static constexpr int kLFull = 30;      // +b: the sub-step's LSE and D values landed (bulk copy)
+    static constexpr int kNumBars = 32;
     static constexpr int kOffMisc = kNumBars * 8;
-    static constexpr int kOffRows = 256;   // + stage * 512: float lse2[64], delta[64]
-    static constexpr int kSmallBytes = kOffRows + kStages * 2 * kQ * 4;
+    static constexpr int kOffRows = 384;   // + b * 512: float lse2[64], delta[64]
+    static constexpr int kSmallBytes = kOffRows + 2 * 2 * kQ * 4;
     static_assert(kOffMisc + 16 <= kOffRows, "small region layout");
     static constexpr int kSmemBytes = kSmallBytes + 1024 + kTilesBytes;
     static constexpr uint32_t kTmemDV = 0;
@@ -627,7 +633,8 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
         for (int i = 0; i < S::kNumBars; ++i) {
             uint32_t count = 1;  // MMA commits, TMA, the reduction thread
             if (i >= S::kPFull && i < S::kPFull + 2) count = 2 * kBlock / 32;  // the key-row warps
-            if ((i >= S::kBufFree && i < S::kBufFree + 2) || i == S::kStageReady) count = kBlock / 32;  // dQ warps
+            if ((i >= S::kBufFree && i < S::kBufFree + 2) || (i >= S::kStageReady && i < S::kStageReady + S::kStages))
+                count = kBlock / 32;  // dQ warps
             if (i == S::kTeardown) count = 2;  // one commit per MMA-issuing warp
             ptx::bar_init(bar(i), count);
         }
@@ -660,31 +667,42 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
                 ptx::tma_load_3d(sbase + S::kOffV + c * S::kKBoxBytes, &tm_v, bar(S::kKVFull), c * 64, k0, bh);
             }
         }
-        int nq = 0;
+        int nq = 0, nl = 0;  // Q/dO and row-value loads issued
         for (int j = 0; j < n; ++j) {
-            const int st = j % S::kStages;
-            if (j >= S::kStages && !wait(S::kQEmpty + st, ((j / S::kStages) - 1) & 1)) break;
+            const int st = j % S::kStages, b = j & 1;
+            // the stage held sub-step j-4's staged dQ_t until its reductions read it
+            if (j >= S::kStages && !wait(S::kStageFree + st, ((j / S::kStages) - 1) & 1)) break;
             const int q0 = qs0 + j * S::kQ;
             if (leader) {
                 const uint32_t qb = sbase + S::kOffQ + st * S::kStageBytes;
-                const uint32_t rows = ssmall + S::kOffRows + st * 2 * S::kQ * 4;
-                const size_t ro = static_cast<size_t>(bh) * p.Sq_pad + q0;
-                ptx::bar_arrive_expect_tx(bar(S::kQFull + st), S::kStageBytes + 2 * S::kQ * 4);
+                ptx::bar_arrive_expect_tx(bar(S::kQFull + st), S::kStageBytes);
                 for (int c = 0; c < 2; ++c) {
                     ptx::tma_load_3d(qb + c * S::kQBoxBytes, &tm_q, bar(S::kQFull + st), c * 64, q0, bh);
                     ptx::tma_load_3d(qb + S::kQTileBytes + c * S::kQBoxBytes, &tm_do, bar(S::kQFull + st), c * 64,
                                      q0, bh);
                 }
-                ptx::bulk_load(rows, p.lse2 + ro, S::kQ * 4, bar(S::kQFull + st));
-                ptx::bulk_load(rows + S::kQ * 4, p.delta + ro, S::kQ * 4, bar(S::kQFull + st));
             }
             ++nq;
+            // row buffer b is free once the key-row warps are done with sub-step j-2
+            if (j >= 2 && !wait(S::kPFull + b, ((j - 2) >> 1) & 1)) break;
+            if (leader) {
+                const uint32_t rows = ssmall + S::kOffRows + b * 2 * S::kQ * 4;
+                const size_t ro = static_cast<size_t>(bh) * p.Sq_pad + q0;
+                ptx::bar_arrive_expect_tx(bar(S::kLFull + b), 2 * S::kQ * 4);
+                ptx::bulk_load(rows, p.lse2 + ro, S::kQ * 4, bar(S::kLFull + b));
+                ptx::bulk_load(rows + S::kQ * 4, p.delta + ro, S::kQ * 4, bar(S::kLFull + b));
+            }
+            ++nl;
         }
         // never leave with copies in flight
         ptx::bar_wait(bar(S::kKVFull), 0, nullptr, p.timeout_ns);
         for (int st = 0; st < S::kStages && st < nq; ++st) {
             const int last = (nq - 1) - ((nq - 1 - st) % S::kStages);
             ptx::bar_wait(bar(S::kQFull + st), (last / S::kStages) & 1, nullptr, p.timeout_ns);
+        }
+        for (int b = 0; b < 2 && b < nl; ++b) {
+            const int last = (nl - 1) - ((nl - 1 - b) % 2);
+            ptx::bar_wait(bar(S::kLFull + b), (last >> 1) & 1, nullptr, p.timeout_ns);
         }
     } else if ((warp == 1 || warp == 3) && n > 0) {
         // ---- MMA issuers: warp 1 forms S^T and dP^T of each sub-step, warp 3
@@ -789,15 +807,15 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
         const uint32_t ds_row = sbase + S::kOffDS + (r >> 3) * 1024 + (r & 7) * 128;
         bool ok = true;
         for (int j = 0; j < n; ++j) {
-            const int st = j % S::kStages, b = j & 1;
+            const int b = j & 1;
             const int qc = qs0 + j * S::kQ + 32 * h;  // first query of this warp's chunk
             const uint32_t tb = tmem + lane_base + S::kTmemBuf + 128 * b;
-            // the stage's rows, then S^T and dP^T: one test of both first,
+            // the sub-step's rows, then S^T and dP^T: one test of both first,
             // the bounded waits only when one is open
             const bool ready = ptx::bar_try_wait(bar(S::kSFull + b), (j >> 1) & 1) &&
-                               ptx::bar_try_wait(bar(S::kQFull + st), (j / S::kStages) & 1);
+                               ptx::bar_try_wait(bar(S::kLFull + b), (j >> 1) & 1);
             if (!__all_sync(0xffffffffu, ready)) {
-                if (!(ok = wait(S::kQFull + st, (j / S::kStages) & 1))) break;
+                if (!(ok = wait(S::kLFull + b, (j >> 1) & 1))) break;
                 if (!(ok = wait(S::kSFull + b, (j >> 1) & 1))) break;
             }
             ptx::tc_fence_after();
@@ -808,7 +826,7 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             ptx::reg_fence(sv);
             ptx::reg_fence(dpv);
             const bool need_mask = (CAUSAL && key > qc) || key >= p.Sk;
-            const float *rows = reinterpret_cast<const float *>(smem_raw + S::kOffRows + st * 2 * S::kQ * 4);
+            const float *rows = reinterpret_cast<const float *>(smem_raw + S::kOffRows + b * 2 * S::kQ * 4);
             const float4 *lq = reinterpret_cast<const float4 *>(rows + 32 * h);
             const float4 *dq4 = reinterpret_cast<const float4 *>(rows + S::kQ + 32 * h);
             uint32_t pp[16], dd[16];
@@ -888,9 +906,9 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
         const int wq = warp % 4;
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         // head column r = 32 wq + lane of the staging tile: box wq, 4-byte word lane
-        const uint32_t dq_col = sbase + S::kOffDQ + wq * S::kDQBoxBytes + (lane & 3) * 4;
+        const uint32_t dq_col = sbase + S::kOffQ + wq * S::kDQBoxBytes + (lane & 3) * 4;
         for (int j = 0; j < n; ++j) {
-            const int b = j & 1;
+            const int b = j & 1, st = j % S::kStages;
             if (!wait(S::kDQFull + b, (j >> 1) & 1)) break;
             ptx::tc_fence_after();
             uint32_t v0[32], v1[32];
@@ -903,31 +921,35 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::bar_arrive(bar(S::kBufFree + b));
-            if (j >= 1 && !wait(S::kStageFree, (j - 1) & 1)) break;  // the last reduction has read the tile
+            // the sub-step's stage takes the tile once dV and dK are done with Q_j, dO_j
+            if (!wait(S::kQEmpty + st, (j / S::kStages) & 1)) break;
+            const uint32_t col = dq_col + st * S::kStageBytes;
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
                 const uint32_t chunk = static_cast<uint32_t>((lane >> 2) ^ (i & 7));
-                asm volatile("st.shared.b32 [%0], %1;" ::"r"(dq_col + i * 128 + chunk * 16),
+                asm volatile("st.shared.b32 [%0], %1;" ::"r"(col + i * 128 + chunk * 16),
                              "r"(i < 32 ? v0[i] : v1[i - 32])
                              : "memory");
             }
             ptx::fence_proxy_async_smem();  // the bulk reduction reads the tile next
             __syncwarp();
-            if (lane == 0) ptx::bar_arrive(bar(S::kStageReady));
+            if (lane == 0) ptx::bar_arrive(bar(S::kStageReady + st));
         }
     } else if (warp == 2 && n > 0) {
         // ---- bulk reductions of the staged dQ_t into the accumulator ----
         const bool leader = ptx::elect_one();
         for (int j = 0; j < n; ++j) {
-            if (!wait(S::kStageReady, j & 1)) break;
+            const int st = j % S::kStages;
+            if (!wait(S::kStageReady + st, (j / S::kStages) & 1)) break;
             if (leader) {
                 const int q0 = qs0 + j * S::kQ;
+                const uint32_t tile = sbase + S::kOffQ + st * S::kStageBytes;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c)
-                    ptx::tma_reduce_add_3d(&tm_dq, sbase + S::kOffDQ + c * S::kDQBoxBytes, 32 * c, q0, bh);
+                    ptx::tma_reduce_add_3d(&tm_dq, tile + c * S::kDQBoxBytes, 32 * c, q0, bh);
                 ptx::bulk_commit();
-                ptx::bulk_wait_read_all();  // the staging tile may be rewritten now
-                ptx::bar_arrive(bar(S::kStageFree));
+                ptx::bulk_wait_read_all();  // the stage may be refilled now
+                ptx::bar_arrive(bar(S::kStageFree + st));
             }
             __syncwarp();
         }

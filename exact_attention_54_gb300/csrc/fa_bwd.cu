@@ -133,13 +133,25 @@ __global__ void __launch_bounds__(256)
         return;
     }
     const size_t off = (static_cast<size_t>(bh) * p.Sq + r) * D + lane * E;
+    // E = 2 or 4 consecutive 16-bit values per lane: one 4- or 8-byte load
+    // each from O and dO, one 8- or 16-byte store of zeros
+    uint16_t ov[E], gv[E];
+    if constexpr (E == 4) {
+        const uint2 a = *reinterpret_cast<const uint2 *>(o + off), c = *reinterpret_cast<const uint2 *>(dout + off);
+        ov[0] = a.x & 0xffffu, ov[1] = a.x >> 16, ov[2] = a.y & 0xffffu, ov[3] = a.y >> 16;
+        gv[0] = c.x & 0xffffu, gv[1] = c.x >> 16, gv[2] = c.y & 0xffffu, gv[3] = c.y >> 16;
+        *reinterpret_cast<float4 *>(p.dq_acc + off) = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+        const uint32_t a = *reinterpret_cast<const uint32_t *>(o + off), c = *reinterpret_cast<const uint32_t *>(dout + off);
+        ov[0] = a & 0xffffu, ov[1] = a >> 16;
+        gv[0] = c & 0xffffu, gv[1] = c >> 16;
+        *reinterpret_cast<float2 *>(p.dq_acc + off) = make_float2(0.f, 0.f);
+    }
     float acc = 0.f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc = fmaf(to_f32<BF16>(o[off + e]), to_f32<BF16>(dout[off + e]), acc);
+    for (int e = 0; e < E; ++e) acc = fmaf(to_f32<BF16>(ov[e]), to_f32<BF16>(gv[e]), acc);
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-#pragma unroll
-    for (int e = 0; e < E; ++e) p.dq_acc[off + e] = 0.f;
     if (lane == 0) {
         p.delta[srow] = acc;
         p.lse2[srow] = lse[static_cast<size_t>(bh) * p.Sq + r] * 1.4426950408889634f;

@@ -69,7 +69,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end loop (profiling runs)")
     ap.add_argument("--parts", default="prefill,decode",
                     help="comma list of the path parts to run (profiling runs may isolate one: prefill, decode, "
-                         "backward, d256, splitd)")
+                         "backward, d256, splitd, varlen)")
     return ap.parse_args(argv)
 
 
@@ -347,7 +347,7 @@ def run_gpu(args, rank, world, local):
 
     parts = set(args.parts.split(","))
     run_pf, run_dc = "prefill" in parts, "decode" in parts
-    if parts & {"backward", "d256", "splitd"} and not (run_pf or run_dc):
+    if parts & {"backward", "d256", "splitd", "varlen"} and not (run_pf or run_dc):
         # profiling run of the backward pass or of the large-head forwards alone
         rec = {"part": args.parts, "steps": args.steps}
         if "backward" in parts:
@@ -357,6 +357,9 @@ def run_gpu(args, rank, world, local):
         if "splitd" in parts:
             rec["split_d"] = {key: run_wide_head(args, fa, torch, dev, stream, flush, world, key)
                               for key in ("large_head", "massive_head")}
+        if "varlen" in parts:
+            rec["varlen_prefill"] = run_varlen(args, fa, torch, dev, stream, flush, world)
+            rec["small_prefill"] = run_wide_head(args, fa, torch, dev, stream, flush, world, "small")
         if rank == 0:
             print(json.dumps(rec), flush=True)
         return None
@@ -420,6 +423,8 @@ def run_gpu(args, rank, world, local):
     d256 = run_wide_head(args, fa, torch, dev, stream, flush, world, "d256")
     split_d = {key: run_wide_head(args, fa, torch, dev, stream, flush, world, key)
                for key in ("large_head", "massive_head")}
+    varlen = run_varlen(args, fa, torch, dev, stream, flush, world)
+    small = run_wide_head(args, fa, torch, dev, stream, flush, world, "small")
     bwd = run_bwd(args, fa, torch, stream, dev, flush, world, (q, k, v), o, lse, wp)
     paged = run_paged(args, fa, torch, stream, dev, flush, world)
     # end-to-end through host buffers (pinned), copies inside the timed region
@@ -458,6 +463,8 @@ def run_gpu(args, rank, world, local):
         "paged_decode": paged,
         "d256_prefill": d256,
         "split_d": split_d,
+        "varlen_prefill": varlen,
+        "small_prefill": small,
         "backward": bwd,
         "gpu_launches": 2 * K,
         "clocks": clock,
@@ -540,12 +547,13 @@ def run_bwd(args, fa, torch, stream, dev, flush, world, qkv, o, lse, wp):
 
 
 def run_wide_head(args, fa, torch, dev, stream, flush, world, key):
-    """The pages' large-head rows, fp16, non-causal: "GPT-4 style" (1, 16,
-    2048, 2048, 256) on the 256-column kernel, "Large Head" (1, 8, 1024, 1024,
-    512) and "Massive Head" (1, 4, 512, 512, 1024) on its Split-D form; each
-    timed on its own loop with the same L2 flush. TFLOPS count the attention
-    FLOPs (4 B H Sq Sk D); Split-D also executes Q K^T once per 256-column
-    output slice, reported as executed_tflops."""
+    """A dense forward workload timed on its own loop with the same L2 flush:
+    the pages' large-head rows, fp16, non-causal ("GPT-4 style" (1, 16, 2048,
+    2048, 256) on the 256-column kernel, "Large Head" (1, 8, 1024, 1024, 512)
+    and "Massive Head" (1, 4, 512, 512, 1024) on its Split-D form) and the
+    small (8, 16, 256, 256, 64) case. TFLOPS count the attention FLOPs
+    (4 B H Sq Sk D); Split-D also executes Q K^T once per 256-column output
+    slice, reported as executed_tflops."""
     from exact_attention_54_gb300 import inputs
     from exact_attention_54_gb300.metrics import attention_flops
     w = inputs.WORKLOADS[key]
@@ -575,13 +583,55 @@ def run_wide_head(args, fa, torch, dev, stream, flush, world, key):
     executed = flops * (slices + 1) / 2 if slices > 1 else flops
     peaks, src = load_peaks()
     tf = world * flops / (ms * 1e-3) / 1e12
+    kernel = (f"fa_fwd_d256_kernel<{w.D},fp16,non-causal,dense>" if w.D >= 256 else
+              f"fa_fwd_kernel<{w.D},fp16,non-causal,dense>")
     rec = {"workload": w.name, "value": tf, "unit": "TFLOPS", "ms_per_launch": ms, "steps": n,
-           "kernel": f"fa_fwd_d256_kernel<{w.D},fp16,non-causal,dense>", "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
-           "per_launch_flops": flops}
+           "kernel": kernel, "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "per_launch_flops": flops}
+    if w.D < 256:
+        return rec
     if slices > 1:
         rec.update(output_slices=slices, executed_tflops=world * executed / (ms * 1e-3) / 1e12)
     rec["traffic"] = committed_traffic().get("fa_fwd_d256_kernel" + (f"_d{w.D}" if slices > 1 else ""))
     return rec
+
+
+def run_varlen(args, fa, torch, dev, stream, flush, world):
+    """The pages' packed-sequence row: 16 sequences with lengths drawn
+    uniformly from [64, 2048], [T, 16, 128] bf16, causal, int32 cu_seqlens.
+    TFLOPS count sum_i 2 H L_i^2 D (the causal half of 4 H L_i^2 D); timed
+    on its own loop with the same L2 flush."""
+    from exact_attention_54_gb300 import inputs
+    from exact_attention_54_gb300.metrics import varlen_flops
+    w = inputs.WORKLOADS["varlen"]
+    lengths, cu, q, k, v = inputs.make_workload(w)
+    q, k, v, cu = (t.to(dev) for t in (q, k, v, cu.to(torch.int32)))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.H, q.shape[0], dtype=torch.float32, device=dev)
+    max_len = int(lengths.max())
+    n = max(1, min(args.steps, 500))
+
+    def step(evs=None):
+        flush.fill_(float(1.0))
+        if evs:
+            evs[0].record(stream)
+        fa.fa_fwd_varlen(q, k, v, o, lse, cu, cu, max_len, w.causal, w.scale, stream)
+        if evs:
+            evs[1].record(stream)
+
+    for _ in range(3):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        step(evs[i])
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    ms = aggregate_max([sum(e[0].elapsed_time(e[1]) for e in evs) / n], world)[0]
+    flops = varlen_flops(lengths.tolist(), lengths.tolist(), w.H, w.D, w.causal)
+    peaks, _ = load_peaks()
+    tf = world * flops / (ms * 1e-3) / 1e12
+    return {"workload": w.name, "value": tf, "unit": "TFLOPS", "ms_per_launch": ms, "steps": n,
+            "kernel": "fa_fwd_kernel<128,bf16,causal,varlen>", "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+            "per_launch_flops": flops, "total_tokens": int(q.shape[0]), "max_seqlen": max_len}
 
 
 def run_paged(args, fa, torch, stream, dev, flush, world):

@@ -47,6 +47,11 @@ constexpr int kBlockN = 128;      // keys per K/V tile
 constexpr int kFwdThreads = 384;  // 12 warps
 constexpr float kRescaleThreshold = 8.0f;
 
+// Size of the packed-sequence schedule table (see VarlenSched).
+constexpr int kSchedSeqs = 256;
+constexpr int kSchedPairs = 64;
+constexpr int kSchedInts = 2 + 2 * kSchedPairs + kSchedSeqs;
+
 template <int D>
 struct FwdShape {
     static_assert(D == 64 || D == 128, "head dim");
@@ -71,12 +76,42 @@ struct FwdShape {
     static constexpr int kODone = kPFull2 + 2;           // +t
     static constexpr int kNumBars = kODone + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
+    // packed-sequence schedule (varlen): see VarlenSched
+    static constexpr int kOffSched = (kOffMisc + 16 + 15) & ~15;
+    static constexpr int kSmemBytes = kOffSched + kSchedInts * 4 + 1024;  // + slack to align the base to 1024
     static constexpr uint32_t kTmemS = 0;                     // + t * 128
     static constexpr uint32_t kTmemO = 256;                   // + t * D
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
+
+// Packed-sequence schedule, built by every CTA from cu_seqlens_q at launch
+// (no host synchronisation, no workspace): only the work items that exist are
+// handed out, heaviest first. Item order: query-tile pair index descending;
+// within a pair index, sequences ascending (those long enough to have that
+// pair), then heads. In shared memory, as ints: [0] 1 when the table is in
+// use, [1] the number of items, then for each pair index p the first item of
+// its bucket and the number of sequences in it, then each sequence's pair
+// count. Batches beyond the table's size use the plain enumeration (every
+// (pair, sequence, head) up to the longest sequence; missing tiles inactive).
+struct VarlenSched {
+    static constexpr int kOn = 0, kItems = 1, kStart = 2, kCount = 2 + kSchedPairs, kPairs = 2 + 2 * kSchedPairs;
+};
+
+__device__ __forceinline__ int lds_int(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+// Work items of this launch: the packed-sequence table's count when it is in use.
+template <bool VARLEN>
+__device__ __forceinline__ int num_items(const FwdParams &p, uint32_t sched) {
+    if constexpr (VARLEN) {
+        if (lds_int(sched + 4 * VarlenSched::kOn)) return lds_int(sched + 4 * VarlenSched::kItems);
+    }
+    return p.num_work;
+}
 
 // One unit of work: a pair of consecutive 128-row query tiles of one
 // (sequence, head). Tiles past the end of the sequence are inactive.
@@ -91,14 +126,26 @@ struct Work {
 };
 
 template <bool CAUSAL, bool VARLEN>
-__device__ __forceinline__ Work get_work(const FwdParams &p, int w) {
+__device__ __forceinline__ Work get_work(const FwdParams &p, int w, uint32_t sched) {
     Work k;
     const int BH = p.B * p.H;
-    const int pair = p.n_pairs - 1 - w / BH;  // longest causal work first
+    int pair = p.n_pairs - 1 - w / BH;  // longest causal work first
     const int bh = w % BH;
     k.b = bh / p.H;
     k.h = bh % p.H;
     if constexpr (VARLEN) {
+        if (lds_int(sched + 4 * VarlenSched::kOn)) {
+            // bucket of pair index `pair` holds items [start(pair), start(pair - 1))
+            pair = p.n_pairs - 1;
+            while (pair > 0 && w >= lds_int(sched + 4 * (VarlenSched::kStart + pair - 1))) --pair;
+            const int wr = w - lds_int(sched + 4 * (VarlenSched::kStart + pair));
+            int idx = wr / p.H;
+            k.h = wr % p.H;
+            int b = 0;
+            for (; b < p.B; ++b)
+                if (lds_int(sched + 4 * (VarlenSched::kPairs + b)) > pair && idx-- == 0) break;
+            k.b = b;
+        }
         k.seq_q0 = p.cu_q[k.b];
         k.Lq = p.cu_q[k.b + 1] - k.seq_q0;
         k.seq_k0 = p.cu_k[k.b];
@@ -162,12 +209,13 @@ template <int D, bool CAUSAL, bool VARLEN>
 __device__ void fwd_producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, const FwdParams &p, uint32_t sbase,
                                 volatile int *abort_flag) {
     using S = FwdShape<D>;
+    const uint32_t sched = sbase + S::kOffSched;
     const uint32_t bars = sbase + S::kOffBar;
     auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
     const bool leader = ptx::elect_one();
     auto prefetch_q = [&](int w) {
-        if (w >= p.num_work) return;
-        const Work nx = get_work<CAUSAL, VARLEN>(p, w);
+        if (w >= num_items<VARLEN>(p, sched)) return;
+        const Work nx = get_work<CAUSAL, VARLEN>(p, w, sched);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             if (nx.n_kv[t] == 0) continue;
@@ -186,8 +234,8 @@ __device__ void fwd_producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, co
     bool ok = true;
     for (int r = 0; ok; ++r) {
         const int w = work_index(r);
-        if (w >= p.num_work) break;
-        const Work wk = get_work<CAUSAL, VARLEN>(p, w);
+        if (w >= num_items<VARLEN>(p, sched)) break;
+        const Work wk = get_work<CAUSAL, VARLEN>(p, w, sched);
         if (wk.n_kv_max == 0) continue;
         if (wi > 0 && !(ok = ptx::warp_all(ptx::bar_wait(bar(S::kQEmpty), (wi - 1) & 1, abort_flag, p.timeout_ns))))
             break;
@@ -235,6 +283,7 @@ __device__ void fwd_producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, co
 template <int D, bool CAUSAL, bool VARLEN>
 __device__ void fwd_producer_v(const CUtensorMap *tv, const FwdParams &p, uint32_t sbase, volatile int *abort_flag) {
     using S = FwdShape<D>;
+    const uint32_t sched = sbase + S::kOffSched;
     const uint32_t bars = sbase + S::kOffBar;
     auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
     const bool leader = ptx::elect_one();
@@ -242,8 +291,8 @@ __device__ void fwd_producer_v(const CUtensorMap *tv, const FwdParams &p, uint32
     bool ok = true;
     for (int r = 0; ok; ++r) {
         const int w = work_index(r);
-        if (w >= p.num_work) break;
-        const Work wk = get_work<CAUSAL, VARLEN>(p, w);
+        if (w >= num_items<VARLEN>(p, sched)) break;
+        const Work wk = get_work<CAUSAL, VARLEN>(p, w, sched);
         for (int j = 0; j < wk.n_kv_max; ++j, ++it) {
             const uint32_t stage = it % S::kVStages;
             if (it >= S::kVStages &&
@@ -266,6 +315,7 @@ __device__ void fwd_producer_v(const CUtensorMap *tv, const FwdParams &p, uint32
 template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 __device__ void fwd_mma(const FwdParams &p, uint32_t sbase, uint32_t tmem, volatile int *abort_flag) {
     using S = FwdShape<D>;
+    const uint32_t sched = sbase + S::kOffSched;
     constexpr uint32_t kIdescQK = ptx::idesc_f16(BF16, kBlockM, kBlockN, false);
     constexpr uint32_t kIdescPV = ptx::idesc_f16(BF16, kBlockM, D, true);
     const uint32_t bars = sbase + S::kOffBar;
@@ -311,8 +361,8 @@ __device__ void fwd_mma(const FwdParams &p, uint32_t sbase, uint32_t tmem, volat
     bool ok = true;
     for (int r = 0; ok; ++r) {
         const int w = work_index(r);
-        if (w >= p.num_work) break;
-        const Work wk = get_work<CAUSAL, VARLEN>(p, w);
+        if (w >= num_items<VARLEN>(p, sched)) break;
+        const Work wk = get_work<CAUSAL, VARLEN>(p, w, sched);
         if (wk.n_kv_max == 0) continue;
         if (!(ok = ptx::warp_all(ptx::bar_wait(bar(S::kQFull), wi & 1, abort_flag, p.timeout_ns)))) break;
         {
@@ -393,6 +443,7 @@ __device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, i
                             volatile int *abort_flag) {
     using S = FwdShape<D>;
     using Elem = uint16_t;
+    const uint32_t sched = sbase + S::kOffSched;
     const uint32_t bars = sbase + S::kOffBar;
     auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
     const int row = wq * 32 + lane;                             // row within the query tile
@@ -407,8 +458,8 @@ __device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, i
 
     for (int r = 0; ok; ++r) {
         const int w = work_index(r);
-        if (w >= p.num_work) break;
-        const Work wk = get_work<CAUSAL, VARLEN>(p, w);
+        if (w >= num_items<VARLEN>(p, sched)) break;
+        const Work wk = get_work<CAUSAL, VARLEN>(p, w, sched);
         if (wk.rows[t] == 0) continue;
         const int q_row = wk.q_start[t] + row;
         const bool row_valid = row < wk.rows[t];
@@ -597,6 +648,36 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), S::kTmemCols);
         ptx::tmem_relinquish();
+    }
+    if constexpr (VARLEN) {
+        // the packed-sequence schedule (uniform decision across the CTA)
+        int *sch = reinterpret_cast<int *>(smem + S::kOffSched);
+        const int nb = p.B, np = p.n_pairs;
+        if (nb <= kSchedSeqs && np <= kSchedPairs) {
+            for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+                const int len = p.cu_q[b + 1] - p.cu_q[b];
+                const int tiles = len > 0 ? (len + kBlockM - 1) / kBlockM : 0;
+                sch[VarlenSched::kPairs + b] = (tiles + 1) / 2;
+            }
+            __syncthreads();
+            for (int q = threadIdx.x; q < np; q += blockDim.x) {
+                int c = 0;
+                for (int b = 0; b < nb; ++b) c += sch[VarlenSched::kPairs + b] > q ? 1 : 0;
+                sch[VarlenSched::kCount + q] = c;
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                int off = 0;
+                for (int q = np - 1; q >= 0; --q) {
+                    sch[VarlenSched::kStart + q] = off;
+                    off += sch[VarlenSched::kCount + q] * p.H;
+                }
+                sch[VarlenSched::kItems] = off;
+                sch[VarlenSched::kOn] = 1;
+            }
+        } else if (threadIdx.x == 0) {
+            sch[VarlenSched::kOn] = 0;
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();

@@ -102,3 +102,21 @@ def test_varlen_workload_sampled_rows():
         got_l = lse[:, a:b][:, rows]
         assert_close(got_o, ro, O_TOL, f"seq {i} O")
         assert_close(got_l, rl, LSE_TOL, f"seq {i} LSE")
+
+
+@pytest.mark.parametrize("num_seqs", [300, 40])
+def test_varlen_schedule_table_and_fallback(num_seqs):
+    """The kernel schedules packed sequences from a table it builds from
+    cu_seqlens (up to 256 sequences) and falls back to enumerating every
+    (pair, sequence, head) beyond that: both must give the oracle's result,
+    with empty and one-token sequences mixed in."""
+    g = torch.Generator().manual_seed(31 + num_seqs)
+    lengths = torch.randint(0, 400 if num_seqs < 256 else 60, (num_seqs,), generator=g)
+    lengths[::7] = 0
+    lengths[3::11] = 1
+    _, cu, q, k, v = inputs.make_varlen(num_seqs, 0, 0, 2, 64, torch.bfloat16, seed=33, lengths=lengths.tolist())
+    for causal in (True, False):
+        o, lse = run_varlen(q, k, v, cu, causal, 0.125)
+        ro, rl = oracle.attention_varlen(q, k, v, cu, cu, causal, 0.125)
+        assert_close(o, ro, O_TOL, f"varlen O {num_seqs} causal={causal}")
+        assert_close(lse, rl, LSE_TOL, f"varlen LSE {num_seqs} causal={causal}")

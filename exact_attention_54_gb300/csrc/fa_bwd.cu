@@ -177,11 +177,6 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float *__restrict_
 
 // ------------------------------------------------------------ main kernel --
 
-__device__ __forceinline__ void red_add4(float *dst, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
-
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }

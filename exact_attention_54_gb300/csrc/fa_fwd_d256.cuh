@@ -71,8 +71,12 @@ struct Shape {
     static constexpr int kChunks = DQK / kChunkCols;      // ring stages per S tile
     static constexpr int kStageK = kStream ? kBlockM * kChunkCols * 2 : 0;  // K's offset in a stage
     static constexpr int kStageBytes = kStageK + kBlockN * kChunkCols * 2;
-    static constexpr int kKStages = 3;
-    static constexpr int kVStages = 2;
+    // Streaming (Split-D) keeps more of the Q/K ring in flight: each stage
+    // is consumed in a few hundred cycles and the ring must cover an L2 round
+    // trip; one V stage suffices, its next tile has a whole Q K^T and softmax
+    // period to land.
+    static constexpr int kKStages = kStream ? 4 : 3;
+    static constexpr int kVStages = kStream ? 1 : 2;
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kQTileBytes;
     static constexpr int kOffV = kOffK + kKStages * kStageBytes;

@@ -35,9 +35,10 @@
 // so O still fits TMEM next to the two S buffers. Every slice of a tile sees
 // the same S, the same masking and the same arithmetic, so the row statistics
 // agree bit for bit; slice 0 writes the LSE. Q no longer fits shared memory
-// (128 x 1024 x 2 B = 256 KB), so Q and K travel together through the ring,
-// 128 columns at a time (a 48 KB stage: 32 KB of Q, 16 KB of K); the Q
-// re-reads per K tile are served by L2, which the slices of a tile share.
+// (128 x 1024 x 2 B = 256 KB), so Q and K travel together through a 192 KB
+// ring, 64 columns a stage at DQK = 512 and 128 at 1024 (a 48 KB stage: 32 KB
+// of Q, 16 KB of K), with one V stage beside it; the Q re-reads per K tile
+// are served by L2, which the slices of a tile share.
 #pragma once
 
 #include <cuda.h>
@@ -66,8 +67,10 @@ struct Shape {
     static constexpr int kKVBoxBytes = kBlockN * 128;     // 64 rows x 64 columns
     static constexpr int kQTileBytes = kStream ? 0 : kBlockM * D * 2;  // resident Q: 64 KB
     static constexpr int kKVTileBytes = kBlockN * D * 2;  // V tile of one slice: 32 KB
-    // One ring stage: a K tile (resident Q), or 128 columns of Q and of K.
-    static constexpr int kChunkCols = kStream ? 128 : D;
+    // One ring stage: a K tile (resident Q), or kChunkCols columns of Q and of
+    // K: 64 at DQK = 512 (24 KB stages), 128 at DQK = 1024 (48 KB; with 64 the
+    // extra waits per K tile cost more than the earlier starts gain).
+    static constexpr int kChunkCols = kStream ? (DQK <= 512 ? 64 : 128) : D;
     static constexpr int kChunks = DQK / kChunkCols;      // ring stages per S tile
     static constexpr int kStageK = kStream ? kBlockM * kChunkCols * 2 : 0;  // K's offset in a stage
     static constexpr int kStageBytes = kStageK + kBlockN * kChunkCols * 2;
@@ -75,7 +78,7 @@ struct Shape {
     // is consumed in a few hundred cycles and the ring must cover an L2 round
     // trip; one V stage suffices, its next tile has a whole Q K^T and softmax
     // period to land.
-    static constexpr int kKStages = kStream ? 4 : 3;
+    static constexpr int kKStages = kStream ? 192 * 1024 / kStageBytes : 3;
     static constexpr int kVStages = kStream ? 1 : 2;
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kQTileBytes;

@@ -69,7 +69,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end loop (profiling runs)")
     ap.add_argument("--parts", default="prefill,decode",
                     help="comma list of the path parts to run (profiling runs may isolate one: prefill, decode, "
-                         "backward, d256, splitd, varlen)")
+                         "backward, d256, splitd, varlen, shapes)")
     return ap.parse_args(argv)
 
 
@@ -347,7 +347,7 @@ def run_gpu(args, rank, world, local):
 
     parts = set(args.parts.split(","))
     run_pf, run_dc = "prefill" in parts, "decode" in parts
-    if parts & {"backward", "d256", "splitd", "varlen"} and not (run_pf or run_dc):
+    if parts & {"backward", "d256", "splitd", "varlen", "shapes"} and not (run_pf or run_dc):
         # profiling run of the backward pass or of the large-head forwards alone
         rec = {"part": args.parts, "steps": args.steps}
         if "backward" in parts:
@@ -360,6 +360,8 @@ def run_gpu(args, rank, world, local):
         if "varlen" in parts:
             rec["varlen_prefill"] = run_varlen(args, fa, torch, dev, stream, flush, world)
             rec["small_prefill"] = run_wide_head(args, fa, torch, dev, stream, flush, world, "small")
+        if "shapes" in parts:
+            rec["shapes"] = run_shapes(args, fa, torch, dev, stream, flush, world)
         if rank == 0:
             print(json.dumps(rec), flush=True)
         return None
@@ -593,6 +595,46 @@ def run_wide_head(args, fa, torch, dev, stream, flush, world, key):
         rec.update(output_slices=slices, executed_tflops=world * executed / (ms * 1e-3) / 1e12)
     rec["traffic"] = committed_traffic().get("fa_fwd_d256_kernel" + (f"_d{w.D}" if slices > 1 else ""))
     return rec
+
+
+def run_shapes(args, fa, torch, dev, stream, flush, world):
+    """Context rows outside the default run: the LLaMA-7B shape without the
+    causal mask and the pages' BERT-large shape (8, 32, 2048, 2048, 128),
+    bf16, seeded N(0,1) inputs; each timed like the prefill (L2 flushed,
+    CUDA events per launch)."""
+    from exact_attention_54_gb300 import inputs
+    from exact_attention_54_gb300.metrics import attention_flops
+    shapes = {"llama7b_noncausal": (1, 32, 4096, 128, False), "bert_large_noncausal": (8, 32, 2048, 128, False),
+              "bert_large_causal": (8, 32, 2048, 128, True)}
+    peaks, _ = load_peaks()
+    out = {}
+    n = max(1, min(args.steps, 300))
+    for name, (B, H, S, D, causal) in shapes.items():
+        q, k, v = (t.to(dev) for t in inputs.make_dense(B, H, S, S, D, torch.bfloat16, seed=2024))
+        o = torch.empty_like(q)
+        lse = torch.empty(B, H, S, dtype=torch.float32, device=dev)
+
+        def step(evs=None):
+            flush.fill_(float(1.0))
+            if evs:
+                evs[0].record(stream)
+            fa.fa_fwd(q, k, v, o, lse, causal, D ** -0.5, stream)
+            if evs:
+                evs[1].record(stream)
+
+        for _ in range(3):
+            step()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for i in range(n):
+            step(evs[i])
+        torch.cuda.synchronize()
+        fa.fa_check_device_error()
+        ms = aggregate_max([sum(e[0].elapsed_time(e[1]) for e in evs) / n], world)[0]
+        tf = world * attention_flops(B, H, S, S, D, causal) / (ms * 1e-3) / 1e12
+        out[name] = {"shape": [B, H, S, S, D], "causal": causal, "ms_per_launch": ms, "value": tf, "unit": "TFLOPS",
+                     "frac_of_bf16_peak": tf / peaks["bf16_tflops"]}
+        del q, k, v, o, lse
+    return out
 
 
 def run_varlen(args, fa, torch, dev, stream, flush, world):

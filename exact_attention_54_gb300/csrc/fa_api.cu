@@ -117,7 +117,7 @@ constexpr int kMaxLen = 1 << 30;
 
 extern "C" {
 
-int fa_version(void) { return 100; }
+int fa_version(void) { return 200; }
 
 const char *fa_status_string(fa_status_t s) {
     switch (s) {
@@ -134,6 +134,9 @@ const char *fa_status_string(fa_status_t s) {
         case FA_ERR_SCRATCH: return "problem larger than the built-in decode scratch";
         case FA_ERR_DEVICE_INDEX: return "a kernel met an out-of-range block-table entry";
         case FA_ERR_WORKSPACE: return "workspace smaller than fa_bwd_workspace_bytes()";
+        case FA_ERR_DEVICE_SEQLENS:
+            return "cu_seqlens do not describe sequences inside total_q/total_k, or a query sequence is longer "
+                   "than max_seqlen_q (nothing was computed)";
     }
     return "unknown status";
 }
@@ -225,6 +228,7 @@ fa_status_t fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, 
     p.Sq = max_seqlen_q;
     p.Sk = 0;
     p.total_q = total_q;
+    p.total_k = total_k;
     p.n_pairs = static_cast<int>(n_pairs);
     p.n_qtiles = (max_seqlen_q + 127) / 128;
     p.num_work = static_cast<int>(n_work);
@@ -473,7 +477,9 @@ fa_status_t fa_check_device_error(void *stream) {
     if (host == 0) return FA_OK;
     const int zero = 0;
     if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
-    return host == fa::kDeviceErrBadIndex ? FA_ERR_DEVICE_INDEX : FA_ERR_DEVICE_TIMEOUT;
+    if (host == fa::kDeviceErrBadIndex) return FA_ERR_DEVICE_INDEX;
+    if (host == fa::kDeviceErrSeqLens) return FA_ERR_DEVICE_SEQLENS;
+    return FA_ERR_DEVICE_TIMEOUT;
 }
 
 }  // extern "C"

@@ -27,9 +27,9 @@
 //
 // Head dimensions above 256 (the pages' "Large Head" (1, 8, 1024, 1024, 512)
 // and "Massive Head" (1, 4, 512, 512, 1024) rows) take the Split-D strategy
-// ("Adaptive High-Performance Attention Kernels in CUDA", Supported Dispatch
-// Strategies 3: the head dimension is partitioned across thread blocks). A
-// work item is one query tile and one 256-column slice of the output: the
+// ("FlashAttention-2 MMA", Supported Dispatch Strategies 3: the head
+// dimension is partitioned across thread blocks). A work item is one query
+// tile and one 256-column slice of the output: the
 // CTA forms the full S = Q K^T (the contraction runs over all DQK columns)
 // and accumulates only its slice O[:, 256 s : 256 s + 256] = P V[:, slice],
 // so O still fits TMEM next to the two S buffers. Every slice of a tile sees
@@ -151,6 +151,18 @@ __device__ __forceinline__ Work get_work(const FwdParams &p, int w) {
     return k;
 }
 
+// Work items of this launch. Packed sequences: the count each CTA stored
+// after checking the sequence offsets (0 when they are inconsistent).
+template <int DQK, bool VARLEN>
+__device__ __forceinline__ int num_items(const FwdParams &p, uint32_t sbase) {
+    if constexpr (VARLEN) {
+        int v;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(sbase + Shape<DQK>::kOffMisc + 8));
+        return v;
+    }
+    return p.num_work;
+}
+
 // Static persistent schedule: round r hands out items [r*G, (r+1)*G) in
 // alternating direction, so heavy early items and light late items balance.
 __device__ __forceinline__ int work_index(int r) {
@@ -197,7 +209,7 @@ __device__ void producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, const 
     bool ok = true;
     for (int r = 0; ok; ++r) {
         const int w = work_index(r);
-        if (w >= p.num_work) break;
+        if (w >= num_items<DQK, VARLEN>(p, sbase)) break;
         const Work wk = get_work<DQK, CAUSAL, VARLEN>(p, w);
         if (wk.n_kv == 0) continue;
         if (!S::kStream && wi > 0 && !(ok = wait(S::kQEmpty, (wi - 1) & 1))) break;
@@ -206,7 +218,7 @@ __device__ void producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, const 
             load_rows<S::kColBlocks, VARLEN>(tq, sbase + S::kOffQ, S::kQBoxBytes, bar(S::kQFull), wk, wk.seq_q0,
                                              wk.q_start, p.H, 0);
             const int wn = work_index(r + 1);
-            if (wn < p.num_work) {
+            if (wn < num_items<DQK, VARLEN>(p, sbase)) {
                 const Work nx = get_work<DQK, CAUSAL, VARLEN>(p, wn);
                 if (nx.n_kv > 0) {
 #pragma unroll
@@ -250,7 +262,7 @@ __device__ void producer_v(const CUtensorMap *tv, const FwdParams &p, uint32_t s
     bool ok = true;
     for (int r = 0; ok; ++r) {
         const int w = work_index(r);
-        if (w >= p.num_work) break;
+        if (w >= num_items<DQK, VARLEN>(p, sbase)) break;
         const Work wk = get_work<DQK, CAUSAL, VARLEN>(p, w);
         for (int j = 0; j < wk.n_kv; ++j, ++it) {
             const uint32_t stage = it % S::kVStages;
@@ -337,7 +349,7 @@ __device__ void mma_role(const FwdParams &p, uint32_t sbase, uint32_t tmem, vola
     bool ok = true;
     for (int r = 0; ok; ++r) {
         const int w = work_index(r);
-        if (w >= p.num_work) break;
+        if (w >= num_items<DQK, VARLEN>(p, sbase)) break;
         const Work wk = get_work<DQK, CAUSAL, VARLEN>(p, w);
         const int n = wk.n_kv;
         if (n == 0) continue;
@@ -384,7 +396,7 @@ __device__ void softmax_role(const FwdParams &p, uint32_t sbase, uint32_t tmem, 
 
     for (int r = 0; ok; ++r) {
         const int w = work_index(r);
-        if (w >= p.num_work) break;
+        if (w >= num_items<DQK, VARLEN>(p, sbase)) break;
         const Work wk = get_work<DQK, CAUSAL, VARLEN>(p, w);
         const int n = wk.n_kv;
         if (n == 0) continue;
@@ -554,6 +566,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), S::kTmemCols);
         ptx::tmem_relinquish();
+    }
+    if constexpr (VARLEN) {
+        // offsets that do not describe sequences inside the tensors: no work
+        // (nothing is read or written; the error word says why)
+        const bool offsets_ok = varlen_offsets_ok(p);
+        if (threadIdx.x == 0) *reinterpret_cast<int *>(smem + S::kOffMisc + 8) = offsets_ok ? p.num_work : 0;
     }
     ptx::tc_fence_before();
     __syncthreads();

@@ -650,10 +650,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ptx::tmem_relinquish();
     }
     if constexpr (VARLEN) {
-        // the packed-sequence schedule (uniform decision across the CTA)
+        // the packed-sequence schedule (uniform decision across the CTA);
+        // offsets that do not describe sequences inside the tensors leave it
+        // empty (nothing is read or written, the error word says why)
         int *sch = reinterpret_cast<int *>(smem + S::kOffSched);
         const int nb = p.B, np = p.n_pairs;
-        if (nb <= kSchedSeqs && np <= kSchedPairs) {
+        if (!varlen_offsets_ok(p)) {
+            if (threadIdx.x == 0) {
+                sch[VarlenSched::kItems] = 0;
+                sch[VarlenSched::kOn] = 1;
+            }
+        } else if (nb <= kSchedSeqs && np <= kSchedPairs) {
             for (int b = threadIdx.x; b < nb; b += blockDim.x) {
                 const int len = p.cu_q[b + 1] - p.cu_q[b];
                 const int tiles = len > 0 ? (len + kBlockM - 1) / kBlockM : 0;

@@ -8,10 +8,13 @@
 
 namespace fa {
 
-// Values written to the device error word: a kernel abandoned a wait, or met
-// an out-of-range device-side index (a page number in a block table).
+// Values written to the device error word: a kernel abandoned a wait, met an
+// out-of-range device-side index (a page number in a block table), or found
+// packed-sequence offsets that do not describe sequences inside the tensors
+// (or a query sequence longer than the launch was sized for).
 constexpr int kDeviceErrTimeout = 1;
 constexpr int kDeviceErrBadIndex = 2;
+constexpr int kDeviceErrSeqLens = 3;
 
 // Default bound on any single wait on an on-chip barrier.
 constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;  // 1 s
@@ -27,6 +30,7 @@ struct FwdParams {
     int Sq;                // query length (dense) or max query length (varlen)
     int Sk;                // key length (dense only)
     int total_q;           // varlen: LSE row stride of one head
+    int total_k;           // varlen: key tokens (bound of cu_k)
     int n_pairs;           // query-tile pairs per (sequence, head): ceil(ceil(Sq/128)/2)
     int n_qtiles;          // 128-row query tiles per (sequence, head): ceil(Sq/128)
     int num_work;          // work items: n_pairs * B * H (D <= 128), n_qtiles * B * H * D / 256 (D >= 256)
@@ -36,6 +40,22 @@ struct FwdParams {
 };
 
 int fwd_smem_bytes(int D);
+
+// Packed-sequence offsets check, run by every thread of a CTA (all must call
+// it): true when 0 <= cu[0] <= ... <= cu[B] <= total for queries and keys and
+// no query sequence is longer than p.Sq (the max_seqlen_q the launch was
+// sized for). Every CTA reaches the same answer; thread 0 of each CTA that
+// finds a fault records it in the device error word.
+__device__ __forceinline__ bool varlen_offsets_ok(const FwdParams &p) {
+    bool bad = false;
+    for (int b = static_cast<int>(threadIdx.x); b < p.B; b += static_cast<int>(blockDim.x)) {
+        const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1], k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
+        bad |= q0 < 0 || q1 < q0 || q1 > p.total_q || q1 - q0 > p.Sq || k0 < 0 || k1 < k0 || k1 > p.total_k;
+    }
+    bad = __syncthreads_or(bad) != 0;
+    if (bad && threadIdx.x == 0) atomicExch(p.err, kDeviceErrSeqLens);
+    return !bad;
+}
 
 // Parameters of the split-KV decode kernel (dense and paged K/V).
 struct DecodeParams {

@@ -43,7 +43,9 @@ float *scratch_address() {
     return cache[dev];
 }
 
-long long round16(long long nfloats) { return (nfloats + 3) / 4 * 4; }
+// Rounds a float count up to a multiple of 4 floats (16 bytes), so that each
+// part of the scratch starts 16-byte aligned.
+long long round_up_4_floats(long long nfloats) { return (nfloats + 3) / 4 * 4; }
 
 }  // namespace
 
@@ -56,9 +58,12 @@ fa_status_t fa_decode_noalloc(const void *q, const void *k, const void *v, void 
     if (D != 64 && D != 128) return FA_ERR_HEADDIM;
     if (B < 1 || H < 1 || Sk < 1 || Sk > (1 << 30)) return FA_ERR_SHAPE;
     if (num_splits < 1 || num_splits > Sk || num_splits > FA_MAX_SPLITS) return FA_ERR_SPLITS;
+    // B*H*num_splits*D may not fit 64 bits for absurd B and H: bound the head
+    // count by the scratch size first (num_splits >= 1 here), then form sizes.
+    if (static_cast<long long>(B) * H > FA_NOALLOC_SCRATCH_FLOATS / num_splits) return FA_ERR_SCRATCH;
     const long long parts = static_cast<long long>(B) * H * num_splits;
-    const long long o_floats = round16(parts * D);
-    const long long ml_floats = round16(parts);
+    const long long o_floats = round_up_4_floats(parts * D);
+    const long long ml_floats = round_up_4_floats(parts);
     if (o_floats + 2 * ml_floats > FA_NOALLOC_SCRATCH_FLOATS) return FA_ERR_SCRATCH;
     if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |

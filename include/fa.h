@@ -61,7 +61,8 @@ typedef enum {
     FA_ERR_DEVICE_TIMEOUT = -9, /* a kernel gave up waiting on an on-chip barrier */
     FA_ERR_SCRATCH = -10,       /* fa_decode_noalloc: problem larger than its built-in scratch */
     FA_ERR_DEVICE_INDEX = -11,  /* a kernel met an out-of-range block-table entry */
-    FA_ERR_WORKSPACE = -12      /* caller workspace smaller than required */
+    FA_ERR_WORKSPACE = -12,     /* caller workspace smaller than required */
+    FA_ERR_DEVICE_SEQLENS = -13 /* fa_fwd_varlen: cu_seqlens inconsistent with the sizes (see there) */
 } fa_status_t;
 
 typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype_t;
@@ -87,8 +88,8 @@ typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype_t;
  *           ("GPT-4 style", head_dim 256) configuration and runs a kernel with
  *           one query tile per CTA and 64-key K/V tiles. D = 512 and 1024 (the
  *           pages' "Large Head" and "Massive Head" rows) take the Split-D
- *           strategy ("Adaptive High-Performance Attention Kernels in CUDA",
- *           Supported Dispatch Strategies 3: head_dim > 256 partitions the
+ *           strategy ("FlashAttention-2 MMA", Supported Dispatch
+ *           Strategies 3: head_dim > 256 partitions the
  *           head dimension across thread blocks): each CTA forms the full
  *           scores and writes one 256-column slice of O. Same results
  *           contract for every D.
@@ -110,10 +111,14 @@ FA_API fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, 
  *   lse           [H,total_q] fp32   (per-head contiguous)
  *   cu_seqlens_q  device int32[num_seqs+1], 0 = cu[0] <= cu[1] <= ... = total_q
  *   cu_seqlens_k  device int32[num_seqs+1], same rules with total_k
- *   max_seqlen_q  >= every query length (sizes the launch; rows of a longer
- *                 sequence would be left unwritten)
+ *   max_seqlen_q  >= every query length (sizes the launch)
  * Sequence i attends its own keys only; causal positions are counted from the
  * start of each sequence. Zero-length sequences are allowed.
+ * The offsets are checked on the device (the host cannot read them without a
+ * synchronisation): if cu_seqlens_q or cu_seqlens_k is negative, decreasing or
+ * beyond total_q / total_k, or a query sequence is longer than max_seqlen_q,
+ * the launch computes nothing (o and lse are neither read nor written) and
+ * the next fa_check_device_error returns FA_ERR_DEVICE_SEQLENS.
  * Errors: as fa_fwd, plus FA_ERR_SHAPE for num_seqs < 1 or total_* < 1.
  */
 FA_API fa_status_t fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -280,8 +285,9 @@ FA_API fa_status_t fa_bwd(const void *q, const void *k, const void *v, const voi
  * current device's error word. Kernels bound every wait on an on-chip barrier;
  * a wait that runs out sets the word, releases what the CTA holds and returns.
  * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT, FA_ERR_DEVICE_INDEX (an out-of-range
- * block-table entry was skipped), or FA_ERR_CUDA when the runtime itself
- * reports an error.
+ * block-table entry was skipped), FA_ERR_DEVICE_SEQLENS (a packed-sequence
+ * launch found inconsistent cu_seqlens and computed nothing), or FA_ERR_CUDA
+ * when the runtime itself reports an error.
  */
 FA_API fa_status_t fa_check_device_error(void *stream);
 

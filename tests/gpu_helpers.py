@@ -34,16 +34,3 @@ def assert_close(actual, expected, tol, what=""):
     err, where = max_abs_err(actual, expected)
     assert err <= tol, f"{what}: max abs err {err:.3e} at {where} > {tol:.1e}"
     return err
-
-
-def sample_rows(S: int, n_random: int = 24, seed: int = 0):
-    """Rows worth checking in a length-S sequence: the edges of every 128-row
-    tile near the start and end, the last rows, and a seeded random sample."""
-    rows = {0, 1, 2, S - 1, S - 2}
-    for t in (127, 128, 129, 255, 256, 257, S // 2, S - 128, S - 129):
-        if 0 <= t < S:
-            rows.add(t)
-    g = torch.Generator().manual_seed(seed)
-    if S > 0:
-        rows.update(torch.randint(0, S, (n_random,), generator=g).tolist())
-    return sorted(r for r in rows if 0 <= r < S)

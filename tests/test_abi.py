@@ -46,11 +46,11 @@ def test_only_the_abi_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    for code in range(-12, 1):
+    for code in range(-13, 1):
         s = fa.fa_status_string(code)
         assert s and s != "unknown status"
     assert fa.fa_status_string(-1234) == "unknown status"
-    assert lib.fa_version() == 100
+    assert lib.fa_version() == 200
 
 
 # Fake device addresses: validation must fail before any of them is used.

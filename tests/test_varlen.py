@@ -8,7 +8,7 @@ import torch
 import exact_attention_54_gb300 as fa
 import oracle
 from exact_attention_54_gb300 import inputs
-from gpu_helpers import LSE_TOL, O_TOL, assert_close, dev, sample_rows
+from gpu_helpers import LSE_TOL, O_TOL, assert_close, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -87,21 +87,48 @@ def test_varlen_poison_past_total_is_never_read():
     assert_close(lse.cpu(), rl, LSE_TOL, "poisoned tail LSE")
 
 
-def test_varlen_workload_sampled_rows():
+def test_varlen_workload_all_rows():
     """16 sequences, lengths uniform on [64, 2048], H=16, D=128, bf16, causal:
-    every sequence checked on sampled rows (all heads)."""
+    every row of every sequence and head against the oracle."""
     w = inputs.WORKLOADS["varlen"]
     lengths, cu, q, k, v = inputs.make_workload(w)
     o, lse = run_varlen(q, k, v, cu, w.causal, w.scale)
-    for i in range(w.num_seqs):
-        a, b = int(cu[i]), int(cu[i + 1])
-        rows = sample_rows(b - a, n_random=8, seed=i)
-        qs, ks, vs = (x[a:b].transpose(0, 1) for x in (q, k, v))  # [H, L, D]
-        ro, rl = oracle.attention(qs, ks, vs, True, w.scale, rows=rows)
-        got_o = o[a:b].transpose(0, 1)[:, rows]
-        got_l = lse[:, a:b][:, rows]
-        assert_close(got_o, ro, O_TOL, f"seq {i} O")
-        assert_close(got_l, rl, LSE_TOL, f"seq {i} LSE")
+    ro, rl = oracle.attention_varlen(q, k, v, cu, cu, w.causal, w.scale)
+    assert_close(o, ro, O_TOL, "varlen workload O")
+    assert_close(lse, rl, LSE_TOL, "varlen workload LSE")
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_inconsistent_offsets_compute_nothing_and_report(D):
+    """cu_seqlens are only readable on the device. A query sequence longer
+    than max_seqlen_q, or offsets past the tensors' token counts, must leave
+    O and LSE untouched (no out-of-range reads or writes) and make
+    fa_check_device_error report FA_ERR_DEVICE_SEQLENS; the next valid call
+    works."""
+    H = 2
+    lengths = [100, 300]
+    _, cu, q, k, v = inputs.make_varlen(len(lengths), 0, 0, H, D, torch.bfloat16, seed=25, lengths=lengths)
+    qd, kd, vd, cud = dev(q, k, v, cu.to(torch.int32))
+    T = int(cu[-1])
+    cases = {
+        "longer than max_seqlen_q": (qd, kd, vd, 200),
+        "offsets past total_q/total_k": (qd[:250].contiguous(), kd[:250].contiguous(), vd[:250].contiguous(), 300),
+    }
+    for what, (qq, kk, vv, mx) in cases.items():
+        o = torch.full_like(qq, 3.0)
+        lse = torch.full((H, qq.shape[0]), 5.0, dtype=torch.float32, device="cuda")
+        fa.fa_fwd_varlen(qq, kk, vv, o, lse, cud, cud, mx, True, 0.1)
+        with pytest.raises(fa.FAError) as e:
+            fa.fa_check_device_error()
+        assert e.value.status == -13, what
+        assert torch.all(o == 3.0), what
+        assert torch.all(lse == 5.0), what
+    o, lse = fa.flash_attention_varlen(qd, kd, vd, cud, cud, 300, causal=True, scale=0.1)
+    fa.fa_check_device_error()
+    ro, rl = oracle.attention_varlen(q, k, v, cu, cu, True, 0.1)
+    assert_close(o.cpu(), ro, O_TOL, "O after the rejected launches")
+    assert_close(lse.cpu(), rl, LSE_TOL, "LSE after the rejected launches")
+    assert T == 400
 
 
 @pytest.mark.parametrize("num_seqs", [300, 40])

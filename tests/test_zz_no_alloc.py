@@ -5,11 +5,12 @@ engine hook that must not allocate, a latency-critical loop that cannot take
 the device-wide synchronisation an allocation may bring, a process whose
 memory is fully reserved by a pool). For them the library keeps its decode
 partials in a fixed, built-in device array. This test calls that entry point
-through the C ABI twice in a row, with different inputs, and checks each
-result against the allocating path (fa_decode_splitkv + fa_splitkv_merge with
-a caller-owned workspace), within the same tolerances as the other decode
-tests. It also checks that a problem too large for the built-in array is
-rejected before anything runs.
+twice in a row, with different inputs (the first call through the C ABI
+directly, the second through the Python binding), and checks each result
+against the allocating path (fa_decode_splitkv + fa_splitkv_merge with a
+caller-owned workspace) and against the fp64 oracle, within the same
+tolerances as the other decode tests. It also checks that problems too large
+for the built-in array are rejected before anything runs.
 """
 import ctypes
 
@@ -17,6 +18,7 @@ import pytest
 import torch
 
 import exact_attention_54_gb300 as fa
+import oracle
 from exact_attention_54_gb300 import inputs
 from gpu_helpers import LSE_TOL, O_TOL, assert_close
 
@@ -33,14 +35,17 @@ def _lib():
     return lib
 
 
-def _noalloc(lib, q, k, v, num_splits, scale):
+def _noalloc(lib, q, k, v, num_splits, scale, through_binding):
     B, H, Sk, D = k.shape
     o = torch.full((B, H, 1, D), float("nan"), dtype=k.dtype, device="cuda")
     lse = torch.full((B, H), float("nan"), dtype=torch.float32, device="cuda")
-    st = lib.fa_decode_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Sk, D,
-                               num_splits, scale, int(k.dtype == torch.bfloat16),
-                               torch.cuda.current_stream().cuda_stream)
-    assert st == 0, fa.fa_status_string(st)
+    if through_binding:
+        fa.fa_decode_noalloc(q, k, v, o, lse, num_splits, scale)
+    else:
+        st = lib.fa_decode_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Sk,
+                                   D, num_splits, scale, int(k.dtype == torch.bfloat16),
+                                   torch.cuda.current_stream().cuda_stream)
+        assert st == 0, fa.fa_status_string(st)
     torch.cuda.synchronize()
     return o, lse
 
@@ -52,13 +57,16 @@ def test_noalloc_matches_allocating_path_two_calls_in_a_row():
         (inputs.make_workload(w), w.num_splits, w.scale),  # 16x8 heads, 8192 keys, 32 partitions
         (inputs.make_dense(3, 5, 1, 1000, 64, torch.float16, seed=77), 7, 0.125),
     ]
-    for (q, k, v), S, scale in cases:
+    for call, ((q, k, v), S, scale) in enumerate(cases):
+        exp_o, exp_lse = oracle.decode(q, k, v, scale)
         q, k, v = (t.cuda() for t in (q, k, v))
         ref_o, ref_lse = fa.flash_decode(q, k, v, S, scale=scale)
         torch.cuda.synchronize()
-        o, lse = _noalloc(lib, q, k, v, S, scale)
-        assert_close(o.cpu(), ref_o.cpu().double(), O_TOL, "no-alloc O")
-        assert_close(lse.cpu(), ref_lse.cpu().double(), LSE_TOL, "no-alloc LSE")
+        o, lse = _noalloc(lib, q, k, v, S, scale, through_binding=call == 1)
+        assert_close(o.cpu(), ref_o.cpu().double(), O_TOL, f"no-alloc O, call {call}")
+        assert_close(lse.cpu(), ref_lse.cpu().double(), LSE_TOL, f"no-alloc LSE, call {call}")
+        assert_close(o.cpu(), exp_o, O_TOL, f"no-alloc O vs oracle, call {call}")
+        assert_close(lse.cpu(), exp_lse[..., 0], LSE_TOL, f"no-alloc LSE vs oracle, call {call}")
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch():
@@ -66,5 +74,8 @@ def test_noalloc_rejects_problems_beyond_the_scratch():
     A = 0x10000  # never dereferenced: the size check comes first
     # 64 x 64 heads x 1024 partitions x (128 + 2) floats is far beyond the built-in array
     st = lib.fa_decode_noalloc(A, A, A, A, A, 64, 64, 8192, 128, 1024, 0.088, 1, None)
+    assert st == FA_ERR_SCRATCH
+    # head counts near INT_MAX: rejected by the size check, with no overflow on the way
+    st = lib.fa_decode_noalloc(A, A, A, A, A, 2**31 - 1, 2**31 - 1, 1 << 30, 128, 1024, 0.088, 1, None)
     assert st == FA_ERR_SCRATCH
     assert "scratch" in fa.fa_status_string(st)

@@ -12,7 +12,9 @@ The headline `value` is prefill attention TFLOPS (causal FLOPs counted at half
 of 4*B*H*S^2*D); the decode throughput in GB/s (K and V read once, plus q and
 O) sits in the `decode` object. Inputs are resident in HBM, and L2 is flushed
 (a 256 MiB write) before every step, outside the timed kernels. Each kernel is
-timed with CUDA events on the stream it is launched on.
+timed with CUDA events on the stream it is launched on. After the timed loop,
+a sustained leg runs the prefill kernel back to back for about a second with
+the SM clock sampled (`sustained_prefill`), next to the short loop's figure.
 
 `--impl reference` times the fp64 CPU oracle instead (a bounded sample of the
 same workload per step) with the same metric and unit.
@@ -67,6 +69,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end loop (profiling runs)")
+    ap.add_argument("--sustained-seconds", type=float, default=1.0,
+                    help="kernel seconds of the back-to-back prefill leg (0 skips it)")
     ap.add_argument("--parts", default="prefill,decode",
                     help="comma list of the path parts to run (profiling runs may isolate one: prefill, decode, "
                          "backward, d256, splitd, varlen, shapes)")
@@ -174,7 +178,7 @@ class ClockSampler:
         source = "during"
         if not lines:
             lines, source = self._snapshot(), "after"
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         inside = []
         for ln in lines:
@@ -198,13 +202,17 @@ class ClockSampler:
                 mx.append(float(f[3]))
             except ValueError:
                 continue
+            try:
+                pw.append(float(f[4]))
+            except ValueError:
+                pass
             for name, val in zip(names, f[6:10]):
                 if val.lower() == "active":
                     reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "when": source}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm), "when": source}
+                "samples": len(sm), "when": source, "power_w_max": max(pw) if pw else None}
 
 
 # ------------------------------------------------------------------ oracle --
@@ -219,15 +227,16 @@ def _cached_inputs(w):
     return _INPUT_CACHE[w.name]
 
 
-def oracle_rate(w, target_s: float):
+def oracle_rate(w, target_s: float, threads: int | None = None):
     """Time the fp64 oracle, as it stands, on a bounded sample of workload w:
-    one head per host thread, a strided subset of query rows in each. Returns
-    (TFLOPS of useful attention work, threads, description, seconds)."""
+    one head per host thread (all host cores unless `threads` is given), a
+    strided subset of query rows in each. Returns (TFLOPS of useful attention
+    work, threads, description, seconds)."""
     import oracle
     from exact_attention_54_gb300 import inputs
     from exact_attention_54_gb300.metrics import attention_flops
 
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     heads = min(threads, w.B * w.H)
     q, k, v = _cached_inputs(w)
     q = q.reshape(-1, w.Sq, w.D)[:heads]
@@ -329,24 +338,27 @@ def run_gpu(args, rank, world, local):
 
     wp = inputs.WORKLOADS[PREFILL]
     wd = inputs.WORKLOADS[DECODE]
-    q, k, v = (t.to(dev) for t in inputs.make_workload(wp))
-    o = torch.empty_like(q)
-    lse = torch.empty(wp.B, wp.H, wp.Sq, dtype=torch.float32, device=dev)
-    dq, dk, dv = (t.to(dev) for t in inputs.make_workload(wd))
-    S = wd.num_splits
-    ws = (torch.empty(wd.B, wd.H, S, wd.D, dtype=torch.float32, device=dev),
-          torch.empty(wd.B, wd.H, S, dtype=torch.float32, device=dev),
-          torch.empty(wd.B, wd.H, S, dtype=torch.float32, device=dev))
-    counters = torch.zeros(wd.B * wd.H, dtype=torch.int32, device=dev)
-    do = torch.empty(wd.B, wd.H, 1, wd.D, dtype=wd.dtype, device=dev)
-    dlse = torch.empty(wd.B, wd.H, dtype=torch.float32, device=dev)
+    parts = set(args.parts.split(","))
+    run_pf, run_dc = "prefill" in parts, "decode" in parts
+    full = run_pf and run_dc  # the report; a profiling run of some parts allocates only what they use
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    if run_pf or "backward" in parts:
+        q, k, v = (t.to(dev) for t in inputs.make_workload(wp))
+        o = torch.empty_like(q)
+        lse = torch.empty(wp.B, wp.H, wp.Sq, dtype=torch.float32, device=dev)
+    if run_dc:
+        dq, dk, dv = (t.to(dev) for t in inputs.make_workload(wd))
+        S = wd.num_splits
+        ws = (torch.empty(wd.B, wd.H, S, wd.D, dtype=torch.float32, device=dev),
+              torch.empty(wd.B, wd.H, S, dtype=torch.float32, device=dev),
+              torch.empty(wd.B, wd.H, S, dtype=torch.float32, device=dev))
+        counters = torch.zeros(wd.B * wd.H, dtype=torch.int32, device=dev)
+        do = torch.empty(wd.B, wd.H, 1, wd.D, dtype=wd.dtype, device=dev)
+        dlse = torch.empty(wd.B, wd.H, dtype=torch.float32, device=dev)
 
     pf_flops = attention_flops(wp.B, wp.H, wp.Sq, wp.Sk, wp.D, wp.causal)
     dc_bytes = decode_bytes(wd.B, wd.H, wd.Sk, wd.D)
 
-    parts = set(args.parts.split(","))
-    run_pf, run_dc = "prefill" in parts, "decode" in parts
     if parts & {"backward", "d256", "splitd", "varlen", "shapes"} and not (run_pf or run_dc):
         # profiling run of the backward pass or of the large-head forwards alone
         rec = {"part": args.parts, "steps": args.steps}
@@ -409,7 +421,7 @@ def run_gpu(args, rank, world, local):
     pf_sum, dc_sum, wall = aggregate_max([sum(pf), sum(dc), wall], world)
     K = args.steps
 
-    if not (run_pf and run_dc):  # a profiling run of one part: a short record, not the report
+    if not full:  # a profiling run of one part: a short record, not the report
         rec = {"part": args.parts, "steps": args.steps, "clocks": clock}
         if run_pf:
             rec.update(prefill_tflops=pf_flops / (statistics.mean(pf) * 1e-3) / 1e12,
@@ -429,6 +441,9 @@ def run_gpu(args, rank, world, local):
     small = run_wide_head(args, fa, torch, dev, stream, flush, world, "small")
     bwd = run_bwd(args, fa, torch, stream, dev, flush, world, (q, k, v), o, lse, wp)
     paged = run_paged(args, fa, torch, stream, dev, flush, world)
+    sustained = (None if args.sustained_seconds <= 0 else
+                 run_sustained(args, fa, torch, stream, flush, world, local, (q, k, v), o, lse, wp,
+                               statistics.mean(pf)))
     # end-to-end through host buffers (pinned), copies inside the timed region
     e2e = ({"prefill": None, "decode": None} if args.no_e2e else
            run_e2e(args, fa, torch, stream, dev, wp, wd, (q, k, v), (dq, dk, dv), world))
@@ -462,6 +477,9 @@ def run_gpu(args, rank, world, local):
             "e2e": e2e["decode"],
         },
         "e2e": e2e["prefill"],
+        "decode_gbs": decode_gbs,
+        "decode_frac": achieved_gbs / peaks["hbm_gbs"],
+        "sustained_prefill": sustained,
         "paged_decode": paged,
         "d256_prefill": d256,
         "split_d": split_d,
@@ -473,6 +491,41 @@ def run_gpu(args, rank, world, local):
         "wall_ms_per_step": 1e3 * wall / K,
     }
     return line
+
+
+def run_sustained(args, fa, torch, stream, flush, world, local, qkv, o, lse, wp, launch_ms):
+    """The prefill kernel back to back for at least --sustained-seconds of
+    kernel time (L2 flushed before every launch, as in the timed loop), each
+    launch timed with CUDA events, the SM clock and power sampled throughout:
+    the steady-state figure beside the short timed loop. kcycles_per_launch =
+    time x median SM clock, to compare runs at different clocks."""
+    from exact_attention_54_gb300.metrics import attention_flops
+    q, k, v = qkv
+    n = max(10, int(math.ceil(args.sustained_seconds / (launch_ms * 1e-3))))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    clocks = ClockSampler(local)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_begin = time.time()
+    for a, b in evs:
+        flush.fill_(float(1.0))
+        a.record(stream)
+        fa.fa_fwd(q, k, v, o, lse, wp.causal, wp.scale, stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    clock = clocks.stop(t_begin, t_end)
+    fa.fa_check_device_error()
+    ms = aggregate_max([statistics.mean(a.elapsed_time(b) for a, b in evs)], world)[0]
+    flops = attention_flops(wp.B, wp.H, wp.Sq, wp.Sk, wp.D, wp.causal)
+    peaks, src = load_peaks()
+    tf = world * flops / (ms * 1e-3) / 1e12
+    mhz = clock.get("sm_mhz")
+    return {"value": tf, "unit": "TFLOPS", "launches": n, "kernel_seconds": n * ms * 1e-3, "ms_per_launch": ms,
+            "frac_of_sustained_peak": tf / peaks["bf16_tflops_sustained"],
+            "frac_of_burst_peak": tf / peaks["bf16_tflops"], "peak_source": src, "clocks": clock,
+            "kcycles_per_launch": (ms * 1e-3 * mhz * 1e6 / 1e3) if mhz else None}
 
 
 def run_two_launch(args, fa, torch, stream, flush, world, dec, ws, o, lse, wd):
@@ -805,6 +858,9 @@ def main(argv=None):
                 r, threads, desc, dt = oracle_rate(inputs.WORKLOADS[PREFILL], args.cpu_seconds)
                 line["cpu_baseline"] = {"value": r, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
                                         "sample": desc, "seconds": dt}
+                r1, t1, desc1, dt1 = oracle_rate(inputs.WORKLOADS[PREFILL], args.cpu_seconds / 3, threads=1)
+                line["cpu_baseline"]["single_core"] = {"value": r1, "unit": "TFLOPS", "cores": t1,
+                                                       "sample": desc1, "seconds": dt1}
                 r2, t2, desc2, dt2 = oracle_decode_rate(inputs.WORKLOADS[DECODE], args.cpu_seconds / 3)
                 line["decode"]["cpu_baseline"] = {"value": r2, "unit": "GB/s", "cores": t2, "kind": "oracle",
                                                   "sample": desc2, "seconds": dt2}

@@ -50,7 +50,7 @@ constexpr float kRescaleThreshold = 8.0f;
 // Size of the packed-sequence schedule table (see VarlenSched).
 constexpr int kSchedSeqs = 256;
 constexpr int kSchedPairs = 64;
-constexpr int kSchedInts = 2 + 2 * kSchedPairs + kSchedSeqs;
+constexpr int kSchedInts = 4 + 2 * kSchedPairs + kSchedSeqs;
 
 template <int D>
 struct FwdShape {
@@ -74,7 +74,8 @@ struct FwdShape {
     static constexpr int kPFull = kSFull + 2;            // +t: P keys [0,64) written, O corrected
     static constexpr int kPFull2 = kPFull + 2;           // +t: P keys [64,128) written
     static constexpr int kODone = kPFull2 + 2;           // +t
-    static constexpr int kNumBars = kODone + 2;
+    static constexpr int kFirstQ = kODone + 2;           // the CTA's first Q pair has landed (one phase only)
+    static constexpr int kNumBars = kFirstQ + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     // packed-sequence schedule (varlen): see VarlenSched
     static constexpr int kOffSched = (kOffMisc + 16 + 15) & ~15;
@@ -90,17 +91,35 @@ struct FwdShape {
 // handed out, heaviest first. Item order: query-tile pair index descending;
 // within a pair index, sequences ascending (those long enough to have that
 // pair), then heads. In shared memory, as ints: [0] 1 when the table is in
-// use, [1] the number of items, then for each pair index p the first item of
-// its bucket and the number of sequences in it, then each sequence's pair
-// count. Batches beyond the table's size use the plain enumeration (every
-// (pair, sequence, head) up to the longest sequence; missing tiles inactive).
+// use, [1] the number of items, [2] the number of cached item records (see
+// below), then for each pair index p the first item of its bucket and the
+// number of sequences in it, then each sequence's pair count. Batches beyond
+// the table's size use the plain enumeration (every (pair, sequence, head) up
+// to the longest sequence; missing tiles inactive).
+//
+// Looking an item up in the table walks the pair buckets and the sequences
+// and reads the item's offsets from cu_seqlens in global memory, which cost
+// more than a microsecond per item on every role. So once the table is
+// built, the CTA resolves all of its own items at once (one thread per
+// round) and keeps them as 32-byte records {b, h, pair, q0, k0, Lq, Lk} in
+// place of the table, when they fit; every role then reads its item with two
+// shared-memory loads.
 struct VarlenSched {
-    static constexpr int kOn = 0, kItems = 1, kStart = 2, kCount = 2 + kSchedPairs, kPairs = 2 + 2 * kSchedPairs;
+    static constexpr int kOn = 0, kItems = 1, kRecs = 2;
+    static constexpr int kStart = 4, kCount = kStart + kSchedPairs, kPairs = kCount + kSchedPairs;
+    static constexpr int kRec0 = 4, kRecInts = 8;
+    static constexpr int kMaxRecs = (kSchedInts - kRec0) / kRecInts;
 };
 
 __device__ __forceinline__ int lds_int(uint32_t addr) {
     int v;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ int4 lds_int4(uint32_t addr) {
+    int4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
     return v;
 }
 
@@ -125,8 +144,36 @@ struct Work {
     int n_kv_max;
 };
 
+// Query tiles, rows and key-tile counts of a work item from its sequence
+// lengths and pair index.
+template <bool CAUSAL>
+__device__ __forceinline__ void finish_work(Work &k, int pair) {
+    const int nk_all = (k.Lk + kBlockN - 1) / kBlockN;
+    k.n_kv_max = 0;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int qs = (2 * pair + t) * kBlockM;
+        k.q_start[t] = qs;
+        const int rows = k.Lq - qs;
+        k.rows[t] = rows <= 0 ? 0 : (rows < kBlockM ? rows : kBlockM);
+        int nkv = 0;
+        if (k.rows[t] > 0) {
+            nkv = nk_all;
+            if (CAUSAL) {
+                const int last = (qs + k.rows[t] - 1) / kBlockN + 1;
+                nkv = last < nk_all ? last : nk_all;
+            }
+        }
+        k.n_kv[t] = nkv;
+        k.n_kv_max = nkv > k.n_kv_max ? nkv : k.n_kv_max;
+    }
+}
+
+// Work item w, resolved from the launch parameters (dense), the schedule
+// table or the plain enumeration (packed sequences). `pair_out` receives its
+// query-tile pair index.
 template <bool CAUSAL, bool VARLEN>
-__device__ __forceinline__ Work get_work(const FwdParams &p, int w, uint32_t sched) {
+__device__ __forceinline__ Work resolve_work(const FwdParams &p, int w, uint32_t sched, int *pair_out = nullptr) {
     Work k;
     const int BH = p.B * p.H;
     int pair = p.n_pairs - 1 - w / BH;  // longest causal work first
@@ -156,26 +203,33 @@ __device__ __forceinline__ Work get_work(const FwdParams &p, int w, uint32_t sch
         k.Lq = p.Sq;
         k.Lk = p.Sk;
     }
-    const int nk_all = (k.Lk + kBlockN - 1) / kBlockN;
-    k.n_kv_max = 0;
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        const int qs = (2 * pair + t) * kBlockM;
-        k.q_start[t] = qs;
-        const int rows = k.Lq - qs;
-        k.rows[t] = rows <= 0 ? 0 : (rows < kBlockM ? rows : kBlockM);
-        int nkv = 0;
-        if (k.rows[t] > 0) {
-            nkv = nk_all;
-            if (CAUSAL) {
-                const int last = (qs + k.rows[t] - 1) / kBlockN + 1;
-                nkv = last < nk_all ? last : nk_all;
-            }
-        }
-        k.n_kv[t] = nkv;
-        k.n_kv_max = nkv > k.n_kv_max ? nkv : k.n_kv_max;
-    }
+    if (pair_out != nullptr) *pair_out = pair;
+    finish_work<CAUSAL>(k, pair);
     return k;
+}
+
+__device__ __forceinline__ int work_index(int r);
+
+// The work item of this CTA's round r (an item of the launch: callers check
+// work_index(r) < num_items first).
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ Work get_work(const FwdParams &p, int r, uint32_t sched) {
+    if constexpr (VARLEN) {
+        if (r < lds_int(sched + 4 * VarlenSched::kRecs)) {
+            const uint32_t rec = sched + 4 * (VarlenSched::kRec0 + VarlenSched::kRecInts * r);
+            const int4 a = lds_int4(rec), c = lds_int4(rec + 16);
+            Work k;
+            k.b = a.x;
+            k.h = a.y;
+            k.seq_q0 = a.w;
+            k.seq_k0 = c.x;
+            k.Lq = c.y;
+            k.Lk = c.z;
+            finish_work<CAUSAL>(k, a.z);
+            return k;
+        }
+    }
+    return resolve_work<CAUSAL, VARLEN>(p, work_index(r), sched);
 }
 
 // Static persistent schedule: round r hands out work items [r*G, (r+1)*G),
@@ -213,9 +267,9 @@ __device__ void fwd_producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, co
     const uint32_t bars = sbase + S::kOffBar;
     auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
     const bool leader = ptx::elect_one();
-    auto prefetch_q = [&](int w) {
-        if (w >= num_items<VARLEN>(p, sched)) return;
-        const Work nx = get_work<CAUSAL, VARLEN>(p, w, sched);
+    auto prefetch_q = [&](int r) {
+        if (work_index(r) >= num_items<VARLEN>(p, sched)) return;
+        const Work nx = get_work<CAUSAL, VARLEN>(p, r, sched);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             if (nx.n_kv[t] == 0) continue;
@@ -229,13 +283,14 @@ __device__ void fwd_producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, co
             }
         }
     };
+    const uint64_t stream_pol = ptx::l2_policy_evict_first();
     uint32_t it = 0;  // K tiles issued
     uint32_t wi = 0;  // work items loaded
     bool ok = true;
     for (int r = 0; ok; ++r) {
         const int w = work_index(r);
         if (w >= num_items<VARLEN>(p, sched)) break;
-        const Work wk = get_work<CAUSAL, VARLEN>(p, w, sched);
+        const Work wk = get_work<CAUSAL, VARLEN>(p, r, sched);
         if (wk.n_kv_max == 0) continue;
         if (wi > 0 && !(ok = ptx::warp_all(ptx::bar_wait(bar(S::kQEmpty), (wi - 1) & 1, abort_flag, p.timeout_ns))))
             break;
@@ -248,15 +303,23 @@ __device__ void fwd_producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, co
             if (wk.n_kv[t] == 0 || !leader) continue;
 #pragma unroll
             for (int c = 0; c < S::kColBlocks; ++c) {
+                // Q tiles are read once: evict them first, keep L2 for K and V
                 const uint32_t dst = sbase + S::kOffQ + t * S::kTileBytes + c * S::kBlockBytes;
                 if constexpr (VARLEN)
-                    ptx::tma_load_3d(dst, tq, bar(S::kQFull), c * 64, wk.h, wk.seq_q0 + wk.q_start[t]);
+                    ptx::tma_load_3d_hint(dst, tq, bar(S::kQFull), c * 64, wk.h, wk.seq_q0 + wk.q_start[t], stream_pol);
                 else
-                    ptx::tma_load_3d(dst, tq, bar(S::kQFull), c * 64, wk.q_start[t], wk.b * p.H + wk.h);
+                    ptx::tma_load_3d_hint(dst, tq, bar(S::kQFull), c * 64, wk.q_start[t], wk.b * p.H + wk.h,
+                                          stream_pol);
             }
         }
-        prefetch_q(work_index(r + 1));
+        prefetch_q(r + 1);
         for (int j = 0; j < wk.n_kv_max; ++j, ++it) {
+            // All CTAs fill their rings at once when the kernel starts; the
+            // first products need only Q and K tile 0, so the rest of the
+            // first ring fill waits until this CTA's first Q pair has landed.
+            if (wi == 0 && j == 1 &&
+                !(ok = ptx::warp_all(ptx::bar_wait(bar(S::kQFull), 0, abort_flag, p.timeout_ns))))
+                break;
             const uint32_t stage = it % S::kKStages;
             if (it >= S::kKStages &&
                 !(ok = ptx::warp_all(ptx::bar_wait(bar(S::kKEmpty + stage), ((it / S::kKStages) - 1) & 1, abort_flag,
@@ -292,8 +355,11 @@ __device__ void fwd_producer_v(const CUtensorMap *tv, const FwdParams &p, uint32
     for (int r = 0; ok; ++r) {
         const int w = work_index(r);
         if (w >= num_items<VARLEN>(p, sched)) break;
-        const Work wk = get_work<CAUSAL, VARLEN>(p, w, sched);
+        const Work wk = get_work<CAUSAL, VARLEN>(p, r, sched);
         for (int j = 0; j < wk.n_kv_max; ++j, ++it) {
+            // V tile 0 goes with the first Q and K tiles; later V tiles wait
+            // until the first Q pair has landed (see the Q/K producer).
+            if (it == 1 && !(ok = ptx::warp_all(ptx::bar_wait(bar(S::kFirstQ), 0, abort_flag, p.timeout_ns)))) break;
             const uint32_t stage = it % S::kVStages;
             if (it >= S::kVStages &&
                 !(ok = ptx::warp_all(ptx::bar_wait(bar(S::kVEmpty + stage), ((it / S::kVStages) - 1) & 1, abort_flag,
@@ -362,9 +428,10 @@ __device__ void fwd_mma(const FwdParams &p, uint32_t sbase, uint32_t tmem, volat
     for (int r = 0; ok; ++r) {
         const int w = work_index(r);
         if (w >= num_items<VARLEN>(p, sched)) break;
-        const Work wk = get_work<CAUSAL, VARLEN>(p, w, sched);
+        const Work wk = get_work<CAUSAL, VARLEN>(p, r, sched);
         if (wk.n_kv_max == 0) continue;
         if (!(ok = ptx::warp_all(ptx::bar_wait(bar(S::kQFull), wi & 1, abort_flag, p.timeout_ns)))) break;
+        if (wi == 0 && leader) ptx::bar_arrive(bar(S::kFirstQ));  // releases the V producer's ring fill
         {
             const uint32_t ks = it % S::kKStages;
             if (!(ok = ptx::warp_all(ptx::bar_wait(bar(S::kKFull + ks), (it / S::kKStages) & 1, abort_flag, p.timeout_ns))))
@@ -379,6 +446,10 @@ __device__ void fwd_mma(const FwdParams &p, uint32_t sbase, uint32_t tmem, volat
                 }
             }
             if (leader) ptx::mma_commit(bar(S::kKEmpty + ks));  // K tile 0 has all its readers
+            // Q is read by Q K^T only: once an item's last Q K^T is issued, the
+            // producer may load the next item's Q pair, which then lands while
+            // this item's last P V products run.
+            if (wk.n_kv_max == 1 && leader) ptx::mma_commit(bar(S::kQEmpty));
         }
         for (int j = 0; j < wk.n_kv_max && ok; ++j) {
             const uint32_t itj = it + j;
@@ -425,10 +496,10 @@ __device__ void fwd_mma(const FwdParams &p, uint32_t sbase, uint32_t tmem, volat
             if (leader) {
                 ptx::mma_commit(bar(S::kVEmpty + vs));                 // V tile j: both P V products issued
                 if (k_next_used) ptx::mma_commit(bar(S::kKEmpty + kn));  // K tile j+1: both Q K^T issued
+                if (j + 2 == wk.n_kv_max) ptx::mma_commit(bar(S::kQEmpty));  // the item's last Q K^T issued
             }
         }
         if (!ok) break;
-        if (leader) ptx::mma_commit(bar(S::kQEmpty));
         it += wk.n_kv_max;
         ++wi;
     }
@@ -451,6 +522,7 @@ __device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, i
     const uint32_t tS = tmem + lane_base + S::kTmemS + t * 128;
     const uint32_t tO = tmem + lane_base + S::kTmemO + t * D;
     const float scale_log2 = p.scale_log2;
+    const uint64_t stream_pol = ptx::l2_policy_evict_first();
     constexpr unsigned kFull = 0xffffffffu;
     uint32_t cnt = 0;    // S tiles consumed by this warpgroup
     uint32_t items = 0;  // work items finished by this warpgroup
@@ -459,7 +531,7 @@ __device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, i
     for (int r = 0; ok; ++r) {
         const int w = work_index(r);
         if (w >= num_items<VARLEN>(p, sched)) break;
-        const Work wk = get_work<CAUSAL, VARLEN>(p, w, sched);
+        const Work wk = get_work<CAUSAL, VARLEN>(p, r, sched);
         if (wk.rows[t] == 0) continue;
         const int q_row = wk.q_start[t] + row;
         const bool row_valid = row < wk.rows[t];
@@ -602,16 +674,20 @@ __device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, i
             for (int i = 0; i < 16; ++i)
                 pk[i] = ptx::pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
             if (row_valid) {
+                // O and LSE are written once: evict them first, keep L2 for K and V
                 uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                for (int i = 0; i < 4; ++i)
+                    ptx::st_global_v4_hint(dst + i, pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3], stream_pol);
             }
         }
         if (row_valid) {
             if constexpr (VARLEN)
-                p.lse[static_cast<size_t>(wk.h) * p.total_q + wk.seq_q0 + q_row] = lse;
+                ptx::st_global_f32_hint(p.lse + static_cast<size_t>(wk.h) * p.total_q + wk.seq_q0 + q_row, lse,
+                                        stream_pol);
             else
-                p.lse[static_cast<size_t>(wk.b * p.H + wk.h) * p.Sq + q_row] = lse;
+                ptx::st_global_f32_hint(p.lse + static_cast<size_t>(wk.b * p.H + wk.h) * p.Sq + q_row, lse,
+                                        stream_pol);
         }
     }
 }
@@ -658,6 +734,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (!varlen_offsets_ok(p)) {
             if (threadIdx.x == 0) {
                 sch[VarlenSched::kItems] = 0;
+                sch[VarlenSched::kRecs] = 0;
                 sch[VarlenSched::kOn] = 1;
             }
         } else if (nb <= kSchedSeqs && np <= kSchedPairs) {
@@ -680,9 +757,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     off += sch[VarlenSched::kCount + q] * p.H;
                 }
                 sch[VarlenSched::kItems] = off;
+                sch[VarlenSched::kRecs] = 0;
                 sch[VarlenSched::kOn] = 1;
             }
+            __syncthreads();
+            // This CTA's own items, one thread per round, resolved while the
+            // table is intact; then written over it as records (when every
+            // CTA's rounds fit: the decision is the same in every CTA).
+            const int items = sch[VarlenSched::kItems];
+            const int rounds = (items + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+            const int r = static_cast<int>(threadIdx.x);
+            const bool mine = rounds <= VarlenSched::kMaxRecs && r < rounds && work_index(r) < items;
+            int pair = 0;
+            Work wk{};
+            if (mine) wk = resolve_work<CAUSAL, VARLEN>(p, work_index(r), sbase + S::kOffSched, &pair);
+            __syncthreads();
+            if (mine) {
+                int *rec = sch + VarlenSched::kRec0 + VarlenSched::kRecInts * r;
+                rec[0] = wk.b;
+                rec[1] = wk.h;
+                rec[2] = pair;
+                rec[3] = wk.seq_q0;
+                rec[4] = wk.seq_k0;
+                rec[5] = wk.Lq;
+                rec[6] = wk.Lk;
+            }
+            if (threadIdx.x == 0 && rounds <= VarlenSched::kMaxRecs) sch[VarlenSched::kRecs] = rounds;
         } else if (threadIdx.x == 0) {
+            sch[VarlenSched::kRecs] = 0;
             sch[VarlenSched::kOn] = 0;
         }
     }

@@ -116,6 +116,38 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// L2 eviction-priority policy for data read or written once (streamed past
+// the cache): lines it touches are the first candidates for eviction, which
+// leaves L2 to the data that is read again.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_load_3d with an L2 cache-policy hint (from l2_policy_evict_first).
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap, uint32_t bar, int x, int y, int z,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
+        : "memory");
+}
+
+// 16-byte global store with an L2 cache-policy hint.
+__device__ __forceinline__ void st_global_v4_hint(void *ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                                  uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(a), "r"(b), "r"(c),
+                 "r"(d), "l"(policy)
+                 : "memory");
+}
+
+// 4-byte global store with an L2 cache-policy hint.
+__device__ __forceinline__ void st_global_f32_hint(float *ptr, float v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(policy) : "memory");
+}
+
 // 3-D tiled bulk reduction: global[tile at (x, y, z)] += shared[src] element-wise
 // (element type and layout from the tensor map). Tracked by the bulk-group
 // mechanism of the issuing thread (bulk_commit / bulk_wait_*).

@@ -147,3 +147,18 @@ def test_varlen_schedule_table_and_fallback(num_seqs):
         ro, rl = oracle.attention_varlen(q, k, v, cu, cu, causal, 0.125)
         assert_close(o, ro, O_TOL, f"varlen O {num_seqs} causal={causal}")
         assert_close(lse, rl, LSE_TOL, f"varlen LSE {num_seqs} causal={causal}")
+
+
+def test_varlen_more_items_per_cta_than_cached_records():
+    """Each CTA keeps at most 48 of its work items as cached records; with
+    8000 items (200 short sequences x 40 heads) a CTA has more rounds than
+    that on any GPU of up to 166 SMs, and the kernel resolves every item from
+    the schedule table instead. Both forms must give the oracle's result."""
+    g = torch.Generator().manual_seed(41)
+    lengths = torch.randint(1, 257, (200,), generator=g)
+    _, cu, q, k, v = inputs.make_varlen(200, 0, 0, 40, 64, torch.bfloat16, seed=42, lengths=lengths.tolist())
+    for causal in (True, False):
+        o, lse = run_varlen(q, k, v, cu, causal, 0.125)
+        ro, rl = oracle.attention_varlen(q, k, v, cu, cu, causal, 0.125)
+        assert_close(o, ro, O_TOL, f"many-item varlen O causal={causal}")
+        assert_close(lse, rl, LSE_TOL, f"many-item varlen LSE causal={causal}")

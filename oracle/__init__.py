@@ -172,6 +172,30 @@ class Oracle:
             lse[:, q0:q1] = li
         return o, lse
 
+    def attention_bwd_varlen(self, q, k, v, dout, cu_seqlens_q, cu_seqlens_k, causal: bool, scale: float,
+                             nthreads: int | None = None):
+        """Gradients of packed variable-length attention (attention_varlen)
+        with respect to q, k, v for the upstream gradient dout ("Adaptive
+        High-Performance Attention Kernels in CUDA", Advanced Production
+        Features 2 and 3). Each sequence is an independent exact attention over
+        its own keys, so its gradients are those of its own block, computed by
+        attention_bwd; causal positions count from each sequence's start.
+        Tokens laid out [total, H, D]; returns float64 dq [total_q, H, D] and
+        dk, dv [total_k, H, D]. Keys of a sequence without queries, and queries
+        of a sequence without keys, get zero gradients."""
+        q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+        cq = [int(x) for x in np.asarray(cu_seqlens_q).tolist()]
+        ck = [int(x) for x in np.asarray(cu_seqlens_k).tolist()]
+        dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+        for i in range(len(cq) - 1):
+            q0, q1, k0, k1 = cq[i], cq[i + 1], ck[i], ck[i + 1]
+            if q1 == q0 or k1 == k0:
+                continue
+            g = self.attention_bwd(*(x.transpose(1, 0, 2) for x in (q[q0:q1], k[k0:k1], v[k0:k1], dout[q0:q1])),
+                                   causal, scale, nthreads=nthreads)
+            dq[q0:q1], dk[k0:k1], dv[k0:k1] = (x.transpose(1, 0, 2) for x in g)
+        return dq, dk, dv
+
     def splitkv_partials(self, q, k, v, num_splits: int, scale: float):
         """Split-K decoding phase 1 for q [..., 1, D] (or [..., D]) and k, v [..., Sk, D].
 
@@ -296,3 +320,7 @@ def decode_paged(*a, **kw):
 
 def attention_bwd(*a, **kw):
     return get().attention_bwd(*a, **kw)
+
+
+def attention_bwd_varlen(*a, **kw):
+    return get().attention_bwd_varlen(*a, **kw)

@@ -334,7 +334,39 @@ def pin_bwd_invariants(orc):
         _close(dv2, dv, 1e-11, f"dv under key shift causal={causal}")
 
 
+def pin_bwd_varlen_block_diag(orc):
+    """Packed-sequence gradients equal torch fp64 autograd through SDPA over
+    the whole packed stream with a block-diagonal mask (top-left causal inside
+    each block), with query and key lengths that differ per sequence so that
+    positions counted from the wrong start would show; a sequence with no
+    queries gets zero key gradients."""
+    Lq, Lk = [3, 2, 0, 4, 1], [5, 2, 3, 6, 1]
+    H, D = 2, 4
+    cq = np.concatenate([[0], np.cumsum(Lq)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(Lk)]).astype(np.int32)
+    Tq, Tk = sum(Lq), sum(Lk)
+    q, do = _rand((Tq, H, D), 131), _rand((Tq, H, D), 132)
+    k, v = _rand((Tk, H, D), 133), _rand((Tk, H, D), 134)
+    scale = 0.55
+    seg_q = torch.repeat_interleave(torch.arange(len(Lq)), torch.tensor(Lq))
+    seg_k = torch.repeat_interleave(torch.arange(len(Lk)), torch.tensor(Lk))
+    pos_q = torch.cat([torch.arange(n) for n in Lq])
+    pos_k = torch.cat([torch.arange(n) for n in Lk])
+    for causal in (False, True):
+        got = orc.attention_bwd_varlen(q, k, v, do, cq, ck, causal, scale)
+        keep = seg_q[:, None] == seg_k[None, :]
+        if causal:
+            keep &= pos_k[None, :] <= pos_q[:, None]
+        qh, kh, vh = (x.transpose(0, 1).clone().requires_grad_(True) for x in (q, k, v))
+        o = F.scaled_dot_product_attention(qh, kh, vh, attn_mask=keep, scale=scale)
+        (o * do.transpose(0, 1)).sum().backward()
+        for name, a, b in zip(("dq", "dk", "dv"), got, (qh.grad, kh.grad, vh.grad)):
+            _close(a, b.transpose(0, 1).numpy(), 1e-11, f"varlen {name} causal={causal}")
+        # sequence 2 has keys [ck[2], ck[3]) and no queries: no gradient reaches them
+        assert np.all(got[1][ck[2]:ck[3]] == 0) and np.all(got[2][ck[2]:ck[3]] == 0)
+
+
 PINS = [pin_sdpa, pin_rows_sum_to_one, pin_single_key, pin_equal_scores, pin_causal_row0,
         pin_two_keys, pin_shift, pin_permutation, pin_rows_subset, pin_partials_definition,
         pin_merge_identity, pin_varlen_block_diag, pin_paged_gather, pin_bwd_autograd,
-        pin_bwd_finite_differences, pin_bwd_invariants]
+        pin_bwd_finite_differences, pin_bwd_invariants, pin_bwd_varlen_block_diag]

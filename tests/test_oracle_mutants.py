@@ -70,3 +70,46 @@ def test_pins_reject_mutant(name, old, new, tmp_path):
         except (AssertionError, ValueError):
             caught.append(pin.__name__)
     assert caught, f"no pin rejects the mutant '{name}'"
+
+
+class _VarlenBwdMutant:
+    """The committed oracle with one mistake planted in its packed-sequence
+    backward (which composes per-sequence calls in Python, not C)."""
+
+    def __init__(self, base, kind):
+        self.base, self.kind = base, kind
+
+    def __getattr__(self, name):
+        return getattr(self.base, name)
+
+    def attention_bwd_varlen(self, q, k, v, dout, cq, ck, causal, scale, nthreads=None):
+        import numpy as np
+        q, k, v, dout = (oracle._f64(x) for x in (q, k, v, dout))
+        if self.kind == "one block":  # sequences not separated
+            g = self.base.attention_bwd(*(x.transpose(1, 0, 2) for x in (q, k, v, dout)), causal, scale)
+            return tuple(x.transpose(1, 0, 2) for x in g)
+        cq, ck = [int(x) for x in cq], [int(x) for x in ck]
+        dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+        for i in range(len(cq) - 1):
+            q0, q1, k0, k1 = cq[i], cq[i + 1], ck[i], ck[i + 1]
+            if q1 == q0 or k1 == k0:
+                continue
+            if self.kind == "keys at query offsets":
+                k0, k1 = q0, min(q0 + (k1 - k0), k.shape[0])
+            g = self.base.attention_bwd(*(x.transpose(1, 0, 2) for x in (q[q0:q1], k[k0:k1], v[k0:k1], dout[q0:q1])),
+                                        causal, scale)
+            g = [x.transpose(1, 0, 2) for x in g]
+            dq[q0:q1] = g[0]
+            if self.kind == "key gradients at query offsets":
+                n = min(k1 - k0, dk.shape[0] - q0)
+                dk[q0:q0 + n], dv[q0:q0 + n] = g[1][:n], g[2][:n]
+            else:
+                dk[k0:k1], dv[k0:k1] = g[1], g[2]
+        return dq, dk, dv
+
+
+@pytest.mark.parametrize("kind", ["one block", "keys at query offsets", "key gradients at query offsets"])
+def test_varlen_bwd_pin_rejects_mutant(kind):
+    from oracle_pins import pin_bwd_varlen_block_diag
+    with pytest.raises(AssertionError):
+        pin_bwd_varlen_block_diag(_VarlenBwdMutant(oracle.get(), kind))

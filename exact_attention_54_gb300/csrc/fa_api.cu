@@ -437,6 +437,11 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
     p.n_qtiles = (Sq + 127) / 128;
     p.n_ktiles = static_cast<int>(n_kt);
     p.Sq_pad = p.n_qtiles * 128;
+    // heads per group: the group's Q, dO and fp32 dQ accumulator (8 Sq D
+    // bytes per head) within 32 MB, a quarter of L2
+    const long long per_head = 8LL * Sq * D;
+    const long long hpg = (32LL << 20) / per_head;
+    p.heads_per_group = static_cast<int>(hpg < 1 ? 1 : (hpg > BH ? BH : hpg));
     p.dq_acc = workspace;
     p.lse2 = workspace + static_cast<size_t>(BH) * Sq * D;
     p.delta = p.lse2 + static_cast<size_t>(BH) * p.Sq_pad;

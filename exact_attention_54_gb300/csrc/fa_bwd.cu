@@ -177,6 +177,21 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float *__restrict_
 
 // ------------------------------------------------------------ main kernel --
 
+// Work item of this CTA: key tile kt of head bh. Heads are taken a group at a
+// time, and within a group the heavy causal key tiles (low kt) come first.
+// Every CTA of a head re-reads its Q and dO and adds into its dQ accumulator,
+// so running a few heads at once keeps that set (8 Sq D bytes per head)
+// within L2 instead of streaming every head's through it at once.
+__device__ __forceinline__ void bwd_work(const BwdParams &p, int &kt, int &bh) {
+    const int per_group = p.heads_per_group * p.n_ktiles;
+    const int g = static_cast<int>(blockIdx.x) / per_group;
+    const int i = static_cast<int>(blockIdx.x) % per_group;
+    const int rest = p.BH - g * p.heads_per_group;
+    const int g_heads = rest < p.heads_per_group ? rest : p.heads_per_group;
+    kt = i / g_heads;
+    bh = g * p.heads_per_group + i % g_heads;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -210,8 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     // work item: key tile kt of head bh; heavy causal tiles (small kt) first
-    const int kt = static_cast<int>(blockIdx.x) / p.BH;
-    const int bh = static_cast<int>(blockIdx.x) % p.BH;
+    int kt, bh;
+    bwd_work(p, kt, bh);
     const int k0 = kt * kBlock;
     const int qt0 = CAUSAL ? kt : 0;  // first query tile that sees any of these keys
     const int n = p.n_qtiles > qt0 ? p.n_qtiles - qt0 : 0;
@@ -471,6 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
             const bool row_valid = key < p.Sk;
             const size_t row_g = (static_cast<size_t>(bh) * p.Sk + key) * D + h * (D / 2);
+            const uint64_t once = ptx::l2_policy_evict_first();
 #pragma unroll 1
             for (int t = 0; t < 2; ++t) {
                 const float f = t == 0 ? 1.f : p.scale;
@@ -492,10 +508,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < 16; ++k)
                         pk[k] = ptx::pack2<BF16>(__uint_as_float(w[2 * k]) * f, __uint_as_float(w[2 * k + 1]) * f);
                     if (row_valid) {
+                        // written once: evict first
                         uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                            ptx::st_global_v4_hint(d4 + k, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3],
+                                                   once);
                     }
                 }
             }
@@ -630,8 +648,8 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
 
     // work item: key tile kt of head bh, heavy causal tiles first; sub-steps of
     // 64 queries from the first query that sees any of these keys
-    const int kt = static_cast<int>(blockIdx.x) / p.BH;
-    const int bh = static_cast<int>(blockIdx.x) % p.BH;
+    int kt, bh;
+    bwd_work(p, kt, bh);
     const int k0 = kt * kBlock;
     const int qs0 = CAUSAL ? k0 : 0;
     const int n = p.Sq > qs0 ? (p.Sq - qs0 + S::kQ - 1) / S::kQ : 0;
@@ -668,10 +686,15 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
         // ---- TMA producer ----
         const bool leader = ptx::elect_one();
         if (leader) {
+            // K and V are read by this CTA only: evict them first, keep L2 for
+            // the Q, dO and dQ accumulator rows the head's other CTAs reuse
+            const uint64_t once = ptx::l2_policy_evict_first();
             ptx::bar_arrive_expect_tx(bar(S::kKVFull), 2 * S::kKTileBytes);
             for (int c = 0; c < 2; ++c) {
-                ptx::tma_load_3d(sbase + S::kOffK + c * S::kKBoxBytes, &tm_k, bar(S::kKVFull), c * 64, k0, bh);
-                ptx::tma_load_3d(sbase + S::kOffV + c * S::kKBoxBytes, &tm_v, bar(S::kKVFull), c * 64, k0, bh);
+                ptx::tma_load_3d_hint(sbase + S::kOffK + c * S::kKBoxBytes, &tm_k, bar(S::kKVFull), c * 64, k0, bh,
+                                      once);
+                ptx::tma_load_3d_hint(sbase + S::kOffV + c * S::kKBoxBytes, &tm_v, bar(S::kKVFull), c * 64, k0, bh,
+                                      once);
             }
         }
         int nq = 0, nl = 0;  // Q/dO and row-value loads issued
@@ -879,6 +902,7 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
         if (ok) {
             const bool row_valid = key < p.Sk;
             const size_t row_g = (static_cast<size_t>(bh) * p.Sk + key) * D + h * (D / 2);
+            const uint64_t once = ptx::l2_policy_evict_first();
 #pragma unroll 1
             for (int t = 0; t < 2; ++t) {
                 const float f = t == 0 ? 1.f : p.scale;
@@ -900,10 +924,12 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
                     for (int k = 0; k < 16; ++k)
                         pk[k] = ptx::pack2<BF16>(__uint_as_float(w[2 * k]) * f, __uint_as_float(w[2 * k + 1]) * f);
                     if (row_valid) {
+                        // written once: evict first
                         uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                            ptx::st_global_v4_hint(d4 + k, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3],
+                                                   once);
                     }
                 }
             }

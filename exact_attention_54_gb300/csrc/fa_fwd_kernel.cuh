@@ -731,19 +731,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // empty (nothing is read or written, the error word says why)
         int *sch = reinterpret_cast<int *>(smem + S::kOffSched);
         const int nb = p.B, np = p.n_pairs;
-        if (!varlen_offsets_ok(p)) {
+        const bool table = nb <= kSchedSeqs && np <= kSchedPairs;
+        // one pass over the offsets: checked, and (for the table) each
+        // sequence's pair count
+        bool bad = false;
+        for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+            const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
+            bad |= varlen_seq_bad(p, q0, q1, p.cu_k[b], p.cu_k[b + 1]);
+            if (table) {
+                const int len = q1 - q0;
+                const int tiles = len > 0 ? (len + kBlockM - 1) / kBlockM : 0;
+                sch[VarlenSched::kPairs + b] = (tiles + 1) / 2;
+            }
+        }
+        if (__syncthreads_or(bad)) {
             if (threadIdx.x == 0) {
+                atomicExch(p.err, kDeviceErrSeqLens);
                 sch[VarlenSched::kItems] = 0;
                 sch[VarlenSched::kRecs] = 0;
                 sch[VarlenSched::kOn] = 1;
             }
-        } else if (nb <= kSchedSeqs && np <= kSchedPairs) {
-            for (int b = threadIdx.x; b < nb; b += blockDim.x) {
-                const int len = p.cu_q[b + 1] - p.cu_q[b];
-                const int tiles = len > 0 ? (len + kBlockM - 1) / kBlockM : 0;
-                sch[VarlenSched::kPairs + b] = (tiles + 1) / 2;
-            }
-            __syncthreads();
+        } else if (table) {
             for (int q = threadIdx.x; q < np; q += blockDim.x) {
                 int c = 0;
                 for (int b = 0; b < nb; ++b) c += sch[VarlenSched::kPairs + b] > q ? 1 : 0;

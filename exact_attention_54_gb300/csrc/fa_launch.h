@@ -41,17 +41,20 @@ struct FwdParams {
 
 int fwd_smem_bytes(int D);
 
+// A packed sequence whose offsets [q0, q1) and [k0, k1) do not lie inside the
+// tensors (0 <= begin <= end <= total), or whose query length exceeds p.Sq
+// (the max_seqlen_q the launch was sized for).
+__device__ __forceinline__ bool varlen_seq_bad(const FwdParams &p, int q0, int q1, int k0, int k1) {
+    return q0 < 0 || q1 < q0 || q1 > p.total_q || q1 - q0 > p.Sq || k0 < 0 || k1 < k0 || k1 > p.total_k;
+}
+
 // Packed-sequence offsets check, run by every thread of a CTA (all must call
-// it): true when 0 <= cu[0] <= ... <= cu[B] <= total for queries and keys and
-// no query sequence is longer than p.Sq (the max_seqlen_q the launch was
-// sized for). Every CTA reaches the same answer; thread 0 of each CTA that
-// finds a fault records it in the device error word.
+// it): true when no sequence is bad. Every CTA reaches the same answer;
+// thread 0 of each CTA that finds a fault records it in the device error word.
 __device__ __forceinline__ bool varlen_offsets_ok(const FwdParams &p) {
     bool bad = false;
-    for (int b = static_cast<int>(threadIdx.x); b < p.B; b += static_cast<int>(blockDim.x)) {
-        const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1], k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
-        bad |= q0 < 0 || q1 < q0 || q1 > p.total_q || q1 - q0 > p.Sq || k0 < 0 || k1 < k0 || k1 > p.total_k;
-    }
+    for (int b = static_cast<int>(threadIdx.x); b < p.B; b += static_cast<int>(blockDim.x))
+        bad |= varlen_seq_bad(p, p.cu_q[b], p.cu_q[b + 1], p.cu_k[b], p.cu_k[b + 1]);
     bad = __syncthreads_or(bad) != 0;
     if (bad && threadIdx.x == 0) atomicExch(p.err, kDeviceErrSeqLens);
     return !bad;
@@ -86,6 +89,7 @@ struct BwdParams {
     int BH, Sq, Sk;
     int Sq_pad;            // Sq rounded up to whole 128-row tiles
     int n_qtiles, n_ktiles;
+    int heads_per_group;   // CTAs run head group by head group (see bwd_work)
     float scale, scale_log2;
     int *err;              // device error word
     unsigned long long timeout_ns;

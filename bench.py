@@ -55,7 +55,7 @@ KERNEL_SOURCES = {
     "fa_fwd_d256_kernel": [_CSRC + "fa_fwd_d256.cuh", _CSRC + "sm103_ptx.cuh", _CSRC + "fa_launch.h"],
     "fa_fwd_d256_kernel_d512": [_CSRC + "fa_fwd_d256.cuh", _CSRC + "sm103_ptx.cuh", _CSRC + "fa_launch.h"],
     "fa_fwd_d256_kernel_d1024": [_CSRC + "fa_fwd_d256.cuh", _CSRC + "sm103_ptx.cuh", _CSRC + "fa_launch.h"],
-    "fa_bwd_kernel": [_CSRC + "fa_bwd.cu", _CSRC + "sm103_ptx.cuh", _CSRC + "fa_launch.h"],
+    "fa_bwd_kernel": [_CSRC + "fa_bwd.cuh", _CSRC + "sm103_ptx.cuh", _CSRC + "fa_launch.h"],
 }
 
 
@@ -73,7 +73,7 @@ def parse_args(argv=None):
                     help="kernel seconds of the back-to-back prefill leg (0 skips it)")
     ap.add_argument("--parts", default="prefill,decode",
                     help="comma list of the path parts to run (profiling runs may isolate one: prefill, decode, "
-                         "backward, d256, splitd, varlen, shapes)")
+                         "backward, d256, splitd, varlen, varlen_backward, shapes)")
     return ap.parse_args(argv)
 
 
@@ -359,7 +359,7 @@ def run_gpu(args, rank, world, local):
     pf_flops = attention_flops(wp.B, wp.H, wp.Sq, wp.Sk, wp.D, wp.causal)
     dc_bytes = decode_bytes(wd.B, wd.H, wd.Sk, wd.D)
 
-    if parts & {"backward", "d256", "splitd", "varlen", "shapes"} and not (run_pf or run_dc):
+    if parts & {"backward", "d256", "splitd", "varlen", "varlen_backward", "shapes"} and not (run_pf or run_dc):
         # profiling run of the backward pass or of the large-head forwards alone
         rec = {"part": args.parts, "steps": args.steps}
         if "backward" in parts:
@@ -372,6 +372,8 @@ def run_gpu(args, rank, world, local):
         if "varlen" in parts:
             rec["varlen_prefill"] = run_varlen(args, fa, torch, dev, stream, flush, world)
             rec["small_prefill"] = run_wide_head(args, fa, torch, dev, stream, flush, world, "small")
+        if "varlen_backward" in parts:
+            rec["varlen_backward"] = run_varlen_bwd(args, fa, torch, dev, stream, flush, world)
         if "shapes" in parts:
             rec["shapes"] = run_shapes(args, fa, torch, dev, stream, flush, world)
         if rank == 0:
@@ -440,6 +442,7 @@ def run_gpu(args, rank, world, local):
     varlen = run_varlen(args, fa, torch, dev, stream, flush, world)
     small = run_wide_head(args, fa, torch, dev, stream, flush, world, "small")
     bwd = run_bwd(args, fa, torch, stream, dev, flush, world, (q, k, v), o, lse, wp)
+    varlen_bwd = run_varlen_bwd(args, fa, torch, dev, stream, flush, world)
     paged = run_paged(args, fa, torch, stream, dev, flush, world)
     sustained = (None if args.sustained_seconds <= 0 else
                  run_sustained(args, fa, torch, stream, flush, world, local, (q, k, v), o, lse, wp,
@@ -486,6 +489,7 @@ def run_gpu(args, rank, world, local):
         "varlen_prefill": varlen,
         "small_prefill": small,
         "backward": bwd,
+        "varlen_backward": varlen_bwd,
         "gpu_launches": 2 * K,
         "clocks": clock,
         "wall_ms_per_step": 1e3 * wall / K,
@@ -727,6 +731,46 @@ def run_varlen(args, fa, torch, dev, stream, flush, world):
     return {"workload": w.name, "value": tf, "unit": "TFLOPS", "ms_per_launch": ms, "steps": n,
             "kernel": "fa_fwd_kernel<128,bf16,causal,varlen>", "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
             "per_launch_flops": flops, "total_tokens": int(q.shape[0]), "max_seqlen": max_len}
+
+
+def run_varlen_bwd(args, fa, torch, dev, stream, flush, world):
+    """Backward pass over the packed-sequence workload (16 sequences of
+    64-2048 tokens, H16 D128 bf16, causal), dO seeded like the inputs; the
+    three launches of fa_bwd_varlen timed together with the same L2 flush.
+    FLOPs: 2.5x the forward's count (five products of its size)."""
+    from exact_attention_54_gb300 import inputs
+    from exact_attention_54_gb300.metrics import varlen_flops
+    w = inputs.WORKLOADS["varlen"]
+    lengths, cu, q, k, v = inputs.make_workload(w)
+    do = inputs.make_varlen(w.num_seqs, 0, 0, w.H, w.D, w.dtype, seed=w.seed + 100, lengths=lengths.tolist())[2]
+    q, k, v, do, cu = (t.to(dev) for t in (q, k, v, do, cu))
+    mx = int(lengths.max())
+    o, lse = fa.flash_attention_varlen(q, k, v, cu, cu, mx, causal=w.causal, scale=w.scale, stream=stream)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_varlen_workspace_bytes(q.shape[0], w.H, w.D) // 4, dtype=torch.float32, device=dev)
+    n = max(1, min(args.steps, 300))
+
+    def step(evs=None):
+        flush.fill_(float(1.0))
+        if evs:
+            evs[0].record(stream)
+        fa.fa_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, ws, cu, cu, mx, mx, w.causal, w.scale, stream)
+        if evs:
+            evs[1].record(stream)
+
+    for _ in range(3):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        step(evs[i])
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    ms = aggregate_max([sum(e[0].elapsed_time(e[1]) for e in evs) / n], world)[0]
+    flops = 2.5 * varlen_flops(lengths.tolist(), lengths.tolist(), w.H, w.D, w.causal)
+    peaks, _ = load_peaks()
+    tf = world * flops / (ms * 1e-3) / 1e12
+    return {"workload": w.name, "value": tf, "unit": "TFLOPS", "ms_per_call": ms, "steps": n,
+            "launches_per_call": 3, "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "per_call_flops": flops}
 
 
 def run_paged(args, fa, torch, stream, dev, flush, world):

@@ -22,9 +22,9 @@ import torch
 
 __all__ = ["FAError", "fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_decode_paged_splitkv", "fa_splitkv_merge",
            "fa_decode_splitkv_fused", "fa_decode_paged_splitkv_fused", "fa_bwd", "fa_bwd_workspace_bytes",
-           "fa_check_device_error", "fa_status_string", "flash_attention", "flash_attention_varlen",
-           "flash_attention_bwd", "flash_decode", "flash_decode_paged", "library_path", "load_library",
-           "EXPORTED_SYMBOLS"]
+           "fa_bwd_varlen", "fa_bwd_varlen_workspace_bytes", "fa_check_device_error", "fa_status_string",
+           "flash_attention", "flash_attention_varlen", "flash_attention_bwd", "flash_attention_varlen_bwd",
+           "flash_decode", "flash_decode_paged", "library_path", "load_library", "EXPORTED_SYMBOLS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libfa.so")
@@ -35,7 +35,8 @@ FA_FP16, FA_BF16 = 0, 1
 FA_MAX_SPLITS = 1024
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_decode_paged_splitkv", "fa_splitkv_merge",
                     "fa_decode_splitkv_fused", "fa_decode_paged_splitkv_fused", "fa_bwd", "fa_bwd_workspace_bytes",
-                    "fa_check_device_error", "fa_status_string", "fa_version")
+                    "fa_bwd_varlen", "fa_bwd_varlen_workspace_bytes", "fa_check_device_error", "fa_status_string",
+                    "fa_version")
 
 
 class FAError(RuntimeError):
@@ -73,6 +74,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.fa_bwd.restype = ctypes.c_int
         lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
         lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp, vp, i, i, i, i, i,
+                                      i, i, i, f, i, vp]
+        lib.fa_bwd_varlen.restype = ctypes.c_int
+        lib.fa_bwd_varlen_workspace_bytes.argtypes = [i, i, i]
+        lib.fa_bwd_varlen_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_check_device_error.argtypes = [vp]
         lib.fa_status_string.argtypes = [i]
         lib.fa_status_string.restype = ctypes.c_char_p
@@ -241,6 +247,30 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal: bool, scale: fl
     _check("fa_bwd", st)
 
 
+def fa_bwd_varlen_workspace_bytes(total_q: int, H: int, D: int) -> int:
+    return int(load_library().fa_bwd_varlen_workspace_bytes(total_q, H, D))
+
+
+def fa_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, workspace, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                  max_seqlen_k: int, causal: bool, scale: float | None = None, stream=None):
+    """Backward pass over packed sequences: q, o, dout, dq [total_q,H,D]; k, v,
+    dk, dv [total_k,H,D]; lse [H,total_q] fp32 from fa_fwd_varlen;
+    cu_seqlens_* int32 CUDA tensors of length num_seqs+1; workspace a CUDA
+    tensor of at least fa_bwd_varlen_workspace_bytes(total_q, H, D) bytes."""
+    Tq, H, D = q.shape
+    Tk = k.shape[0]
+    _need_contig(q, k, v, o, dout, lse, dq, dk, dv, workspace, cu_seqlens_q, cu_seqlens_k)
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    st = load_library().fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                                      _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), cu_seqlens_q.numel() - 1, Tq, Tk,
+                                      int(max_seqlen_q), int(max_seqlen_k), H, D, int(bool(causal)), float(scale),
+                                      _dtype_code(q), _stream(stream))
+    _check("fa_bwd_varlen", st)
+
+
 def fa_check_device_error(stream=None):
     """Synchronise the stream and raise if a kernel abandoned a barrier wait."""
     _check("fa_check_device_error", load_library().fa_check_device_error(_stream(stream)))
@@ -266,6 +296,19 @@ def flash_attention_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: floa
         workspace = torch.empty(fa_bwd_workspace_bytes(B, H, Sq, D) // 4, dtype=torch.float32, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal, scale, stream)
+    return dq, dk, dv
+
+
+def flash_attention_varlen_bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                               max_seqlen_k: int, causal: bool = False, scale: float | None = None, stream=None,
+                               workspace=None):
+    """Returns (dq, dk, dv) for packed sequences, given fa_fwd_varlen's o and lse."""
+    Tq, H, D = q.shape
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_varlen_workspace_bytes(Tq, H, D) // 4, dtype=torch.float32, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, workspace, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                  max_seqlen_k, causal, scale, stream)
     return dq, dk, dv
 
 

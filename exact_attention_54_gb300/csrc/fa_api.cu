@@ -81,18 +81,30 @@ bool encode_map(CUtensorMap *m, bool bf16, const void *base, uint64_t d0, uint64
     return r == CUDA_SUCCESS;
 }
 
-// 3-D map over the fp32 dQ accumulator [B*H][Sq][D] with 32 x rows x 1 boxes
-// and 128-byte swizzle: the target of the backward pass's bulk reductions.
-bool encode_map_f32(CUtensorMap *m, void *base, uint64_t D, uint64_t Sq, uint64_t BH, uint32_t rows) {
+// 3-D map over an fp32 dQ accumulator with 32-column boxes and 128-byte
+// swizzle: the target of the backward pass's bulk reductions. Dense
+// [B*H][Sq][D]: dims {D, Sq, B*H}, boxes 32 x rows x 1; packed [T][H][D]:
+// dims {D, H, T}, boxes 32 x 1 x rows.
+bool encode_map_f32(CUtensorMap *m, void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
+                    uint64_t stride2_bytes, uint32_t box1, uint32_t box2) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
-    const cuuint64_t dims[3] = {D, Sq, BH};
-    const cuuint64_t strides[2] = {D * 4, D * 4 * Sq};
-    const cuuint32_t box[3] = {32, rows, 1};
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    const cuuint32_t box[3] = {32, box1, box2};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Work units per group of the backward's CTA order: the group's Q, dO and fp32
+// dQ accumulator rows (8 L D bytes per unit of L query rows) within 32 MB, a
+// quarter of L2.
+int bwd_units_per_group(long long units, long long rows, int D) {
+    const long long per_unit = 8LL * (rows > 0 ? rows : 1) * D;
+    const long long g = (32LL << 20) / per_unit;
+    return static_cast<int>(g < 1 ? 1 : (g > units ? units : g));
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -425,7 +437,7 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
         !encode_map(&maps[1], bf16, k, D, Sk, BH, row, row * Sk, 128, 1) ||
         !encode_map(&maps[2], bf16, v, D, Sk, BH, row, row * Sk, 128, 1) ||
         !encode_map(&maps[3], bf16, dout, D, Sq, BH, row, row * Sq, q_rows, 1) ||
-        !encode_map_f32(&maps[4], workspace, D, Sq, BH, q_rows))
+        !encode_map_f32(&maps[4], workspace, D, Sq, BH, D * 4, D * 4 * static_cast<uint64_t>(Sq), q_rows, 1))
         return FA_ERR_CUDA;
     int *err = device_error_word();
     if (err == nullptr) return FA_ERR_CUDA;
@@ -437,11 +449,7 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
     p.n_qtiles = (Sq + 127) / 128;
     p.n_ktiles = static_cast<int>(n_kt);
     p.Sq_pad = p.n_qtiles * 128;
-    // heads per group: the group's Q, dO and fp32 dQ accumulator (8 Sq D
-    // bytes per head) within 32 MB, a quarter of L2
-    const long long per_head = 8LL * Sq * D;
-    const long long hpg = (32LL << 20) / per_head;
-    p.heads_per_group = static_cast<int>(hpg < 1 ? 1 : (hpg > BH ? BH : hpg));
+    p.heads_per_group = bwd_units_per_group(BH, Sq, D);
     p.dq_acc = workspace;
     p.lse2 = workspace + static_cast<size_t>(BH) * Sq * D;
     p.delta = p.lse2 + static_cast<size_t>(BH) * p.Sq_pad;
@@ -451,8 +459,82 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
     p.scale_log2 = scale * kLog2e;
     p.err = err;
     p.timeout_ns = fa::kWaitTimeoutNs;
-    const cudaError_t e = fa::launch_bwd(D, bf16, causal != 0, maps, o, dout, lse, dq, p,
+    const cudaError_t e = fa::launch_bwd_dense(D, bf16, causal != 0, maps, o, dout, lse, dq, p,
                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_varlen_workspace_bytes(int total_q, int H, int D) {
+    if (total_q < 1 || H < 1 || total_q > kMaxLen || (D != 64 && D != 128)) return 0;
+    const long long TH = static_cast<long long>(total_q) * H;
+    if (TH > INT_MAX) return 0;
+    return static_cast<size_t>(TH * D + 2 * TH) * sizeof(float);
+}
+
+fa_status_t fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                          const float *lse, void *dq, void *dk, void *dv, float *workspace, size_t workspace_bytes,
+                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int num_seqs, int total_q,
+                          int total_k, int max_seqlen_q, int max_seqlen_k, int H, int D, int causal, float scale,
+                          fa_dtype_t dtype, void *stream) {
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace || !cu_seqlens_q || !cu_seqlens_k)
+        return FA_ERR_NULL;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+    if (D != 64 && D != 128) return FA_ERR_HEADDIM;
+    if (num_seqs < 1 || total_q < 1 || total_k < 1 || max_seqlen_q < 1 || max_seqlen_k < 1 || H < 1 ||
+        total_q > kMaxLen || total_k > kMaxLen || max_seqlen_q > kMaxLen || max_seqlen_k > kMaxLen)
+        return FA_ERR_SHAPE;
+    const long long units = static_cast<long long>(num_seqs) * H;
+    const long long n_kt = (max_seqlen_k + 127) / 128;
+    if (units > INT_MAX || units * n_kt > INT_MAX || static_cast<long long>(total_q) * H > INT_MAX ||
+        static_cast<long long>(total_k) * H > INT_MAX)
+        return FA_ERR_SHAPE;
+    if (!scale_ok(scale)) return FA_ERR_SCALE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned4(lse) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) || !aligned4(cu_seqlens_q) ||
+        !aligned4(cu_seqlens_k))
+        return FA_ERR_ALIGN;
+    const size_t need = fa_bwd_varlen_workspace_bytes(total_q, H, D);
+    if (need == 0) return FA_ERR_SHAPE;
+    if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+
+    const bool bf16 = dtype == FA_BF16;
+    CUtensorMap maps[5];
+    const uint64_t row = static_cast<uint64_t>(D) * 2;
+    const uint64_t tok = row * H;
+    const uint32_t q_rows = D == 128 ? 64 : 128;  // query rows per step of the kernel that runs
+    if (!encode_map(&maps[0], bf16, q, D, H, total_q, row, tok, 1, q_rows) ||
+        !encode_map(&maps[1], bf16, k, D, H, total_k, row, tok, 1, 128) ||
+        !encode_map(&maps[2], bf16, v, D, H, total_k, row, tok, 1, 128) ||
+        !encode_map(&maps[3], bf16, dout, D, H, total_q, row, tok, 1, q_rows) ||
+        !encode_map_f32(&maps[4], workspace, D, H, total_q, D * 4, D * 4 * static_cast<uint64_t>(H), 1, q_rows))
+        return FA_ERR_CUDA;
+    int *err = device_error_word();
+    if (err == nullptr) return FA_ERR_CUDA;
+
+    fa::BwdParams p{};
+    p.BH = static_cast<int>(units);
+    p.Sq = max_seqlen_q;
+    p.Sk = max_seqlen_k;
+    p.n_qtiles = (max_seqlen_q + 127) / 128;
+    p.n_ktiles = static_cast<int>(n_kt);
+    p.Sq_pad = 0;
+    p.heads_per_group = bwd_units_per_group(units, max_seqlen_q, D);
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.H = H;
+    p.total_q = total_q;
+    p.total_k = total_k;
+    p.dq_acc = workspace;
+    p.lse2 = workspace + static_cast<size_t>(total_q) * H * D;
+    p.delta = p.lse2 + static_cast<size_t>(total_q) * H;
+    p.dk = dk;
+    p.dv = dv;
+    p.scale = scale;
+    p.scale_log2 = scale * kLog2e;
+    p.err = err;
+    p.timeout_ns = fa::kWaitTimeoutNs;
+    const cudaError_t e = fa::launch_bwd_varlen(D, bf16, causal != 0, maps, o, dout, lse, dq, p,
+                                                static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

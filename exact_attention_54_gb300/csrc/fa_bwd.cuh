@@ -44,6 +44,8 @@
 // writes that column half of dK and dV at the end. P^T of half h sits in S^T
 // columns [64h, 64h+32). TMEM columns: S^T [0,128), dP^T and then dQ_t
 // [128,256), dV [256, 256+D), dK [256+D, 256+2D).
+#pragma once
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -114,25 +116,38 @@ __device__ __forceinline__ float to_f32(uint16_t x) {
 
 // One warp per (head, padded row): D_i = sum_d dO_id O_id, LSE in base 2, and
 // the zeroed dQ accumulator row. Rows past Sq get D = 0 and LSE = +inf.
-template <int D, bool BF16>
+// Packed sequences: one warp per (head, token) row of the [H][total_q] row
+// arrays, with O, dO and the accumulator laid out [total_q][H][D]; no padding
+// (the main kernel fills rows past a sequence itself).
+template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(256)
     fa_bwd_prep_kernel(const uint16_t *__restrict__ o, const uint16_t *__restrict__ dout,
                        const float *__restrict__ lse, const BwdParams p) {
     constexpr int E = D / 32;  // elements per lane
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;
-    if (row >= static_cast<long long>(p.BH) * p.Sq_pad) return;
-    const int bh = static_cast<int>(row / p.Sq_pad);
-    const int r = static_cast<int>(row % p.Sq_pad);
-    const size_t srow = static_cast<size_t>(bh) * p.Sq_pad + r;
-    if (r >= p.Sq) {
-        if (lane == 0) {
-            p.delta[srow] = 0.f;
-            p.lse2[srow] = CUDART_INF_F;
+    size_t srow, off, lrow;
+    if constexpr (VARLEN) {
+        if (row >= static_cast<long long>(p.H) * p.total_q) return;
+        const int h = static_cast<int>(row / p.total_q);
+        const int t = static_cast<int>(row % p.total_q);
+        srow = lrow = static_cast<size_t>(row);
+        off = (static_cast<size_t>(t) * p.H + h) * D + lane * E;
+    } else {
+        if (row >= static_cast<long long>(p.BH) * p.Sq_pad) return;
+        const int bh = static_cast<int>(row / p.Sq_pad);
+        const int r = static_cast<int>(row % p.Sq_pad);
+        srow = static_cast<size_t>(bh) * p.Sq_pad + r;
+        if (r >= p.Sq) {
+            if (lane == 0) {
+                p.delta[srow] = 0.f;
+                p.lse2[srow] = CUDART_INF_F;
+            }
+            return;
         }
-        return;
+        lrow = static_cast<size_t>(bh) * p.Sq + r;
+        off = lrow * D + lane * E;
     }
-    const size_t off = (static_cast<size_t>(bh) * p.Sq + r) * D + lane * E;
     // E = 2 or 4 consecutive 16-bit values per lane: one 4- or 8-byte load
     // each from O and dO, one 8- or 16-byte store of zeros
     uint16_t ov[E], gv[E];
@@ -154,7 +169,7 @@ __global__ void __launch_bounds__(256)
     for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
     if (lane == 0) {
         p.delta[srow] = acc;
-        p.lse2[srow] = lse[static_cast<size_t>(bh) * p.Sq + r] * 1.4426950408889634f;
+        p.lse2[srow] = lse[lrow] * 1.4426950408889634f;
     }
 }
 
@@ -192,6 +207,78 @@ __device__ __forceinline__ void bwd_work(const BwdParams &p, int &kt, int &bh) {
     bh = g * p.heads_per_group + i % g_heads;
 }
 
+// This CTA's key tile and what it needs of its unit: the unit's index (dense
+// tensor maps), head, first query and key token and lengths (packed). A packed
+// unit whose offsets do not lie inside the tensors, or whose lengths exceed
+// the launch's maxima, is not ok.
+struct BwdUnit {
+    int kt;
+    int z;         // dense: B*H index of the unit
+    int hh;        // packed: head
+    int tq0, tk0;  // packed: first query and key token of the sequence
+    int Lq, Lk;
+    bool ok;
+};
+
+template <bool VARLEN>
+__device__ __forceinline__ BwdUnit bwd_unit(const BwdParams &p) {
+    BwdUnit u;
+    int unit;
+    bwd_work(p, u.kt, unit);
+    if constexpr (VARLEN) {
+        const int b = unit / p.H;
+        u.z = 0;
+        u.hh = unit % p.H;
+        const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1], k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
+        u.ok = !(q0 < 0 || q1 < q0 || q1 > p.total_q || q1 - q0 > p.Sq || k0 < 0 || k1 < k0 || k1 > p.total_k ||
+                 k1 - k0 > p.Sk);
+        u.tq0 = q0;
+        u.tk0 = k0;
+        u.Lq = u.ok ? q1 - q0 : 0;
+        u.Lk = u.ok ? k1 - k0 : 0;
+    } else {
+        u.z = unit;
+        u.hh = 0;
+        u.tq0 = u.tk0 = 0;
+        u.Lq = p.Sq;
+        u.Lk = p.Sk;
+        u.ok = true;
+    }
+    return u;
+}
+
+// Tensor-map coordinates (y, z) of row `row` of the unit's queries or keys:
+// dense maps are {D, S, B*H}, packed maps {D, H, tokens}.
+template <bool VARLEN>
+__device__ __forceinline__ void unit_coords(const BwdUnit &u, bool keys, int row, int &y, int &z) {
+    if constexpr (VARLEN) {
+        y = u.hh;
+        z = (keys ? u.tk0 : u.tq0) + row;
+    } else {
+        y = row;
+        z = u.z;
+    }
+}
+
+// Packed sequences: the per-row values (base-2 LSE, D_i) of query rows
+// [q0, q0 + n) of the unit, read by the calling warp into shared memory at
+// `dst` (LSE at dst, D_i at dst + n floats); rows past the sequence get
+// LSE = +inf and D_i = 0, which zero P and dS there. Then one arrival on `bar`.
+template <int n>
+__device__ __forceinline__ void load_rows_packed(const BwdParams &p, const BwdUnit &u, int q0, float *dst,
+                                                 uint32_t bar, bool leader) {
+    const float *l = p.lse2 + static_cast<size_t>(u.hh) * p.total_q + u.tq0;
+    const float *d = p.delta + static_cast<size_t>(u.hh) * p.total_q + u.tq0;
+#pragma unroll
+    for (int i = threadIdx.x % 32; i < n; i += 32) {
+        const int r = q0 + i;
+        dst[i] = r < u.Lq ? l[r] : CUDART_INF_F;
+        dst[n + i] = r < u.Lq ? d[r] : 0.f;
+    }
+    __syncwarp();
+    if (leader) ptx::bar_arrive(bar);
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -203,7 +290,7 @@ __device__ __forceinline__ void load_tile(const CUtensorMap *tm, uint32_t dst, u
     for (int c = 0; c < D / 64; ++c) ptx::tma_load_3d(dst + c * Shape<D>::kBoxBytes, tm, bar, c * 64, row0, bh);
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -224,12 +311,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         return __all_sync(0xffffffffu, ptx::bar_wait(bar(i), parity, abort_flag, p.timeout_ns));
     };
 
-    // work item: key tile kt of head bh; heavy causal tiles (small kt) first
-    int kt, bh;
-    bwd_work(p, kt, bh);
+    // work item: key tile kt of a head (dense) or of a sequence's head (packed)
+    const BwdUnit u = bwd_unit<VARLEN>(p);
+    if constexpr (VARLEN) {
+        // packed: offsets outside the tensors are reported and skipped; a
+        // key tile past the sequence's keys has nothing to compute or write
+        if (!u.ok) {
+            if (threadIdx.x == 0) atomicExch(p.err, kDeviceErrSeqLens);
+            return;
+        }
+        if (u.kt * kBlock >= u.Lk) return;
+    }
+    const int kt = u.kt;
     const int k0 = kt * kBlock;
     const int qt0 = CAUSAL ? kt : 0;  // first query tile that sees any of these keys
-    const int n = p.n_qtiles > qt0 ? p.n_qtiles - qt0 : 0;
+    const int n_qt = (u.Lq + kBlock - 1) / kBlock;
+    const int n = n_qt > qt0 ? n_qt - qt0 : 0;
+    // 128 rows of the unit's queries (keys = false) or keys, every 64-column box
+    auto load_rows = [&](const CUtensorMap *tm, uint32_t dst, uint32_t bar_addr, int row0, bool keys) {
+        int y, z;
+        unit_coords<VARLEN>(u, keys, row0, y, z);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) ptx::tma_load_3d(dst + c * S::kBoxBytes, tm, bar_addr, c * 64, y, z);
+    };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S::kNumBars; ++i) {
@@ -262,8 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool leader = ptx::elect_one();
         if (leader) {
             ptx::bar_arrive_expect_tx(bar(S::kKVFull), 2 * S::kTileBytes);
-            load_tile<D>(&tm_k, sbase + S::kOffK, bar(S::kKVFull), k0, bh);
-            load_tile<D>(&tm_v, sbase + S::kOffV, bar(S::kKVFull), k0, bh);
+            load_rows(&tm_k, sbase + S::kOffK, bar(S::kKVFull), k0, true);
+            load_rows(&tm_v, sbase + S::kOffV, bar(S::kKVFull), k0, true);
         }
         int nq = 0, nl = 0;  // Q/dO steps and row-value steps loaded
         for (int it = 0; it < n; ++it) {
@@ -273,8 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int q0 = (qt0 + it) * kBlock;
             if (leader) {
                 ptx::bar_arrive_expect_tx(bar(S::kQFull + s), 2 * S::kTileBytes);
-                load_tile<D>(&tm_q, sbase + S::kOffQ + s * S::kTileBytes, bar(S::kQFull + s), q0, bh);
-                load_tile<D>(&tm_do, sbase + S::kOffDO + s * S::kTileBytes, bar(S::kQFull + s), q0, bh);
+                load_rows(&tm_q, sbase + S::kOffQ + s * S::kTileBytes, bar(S::kQFull + s), q0, false);
+                load_rows(&tm_do, sbase + S::kOffDO + s * S::kTileBytes, bar(S::kQFull + s), q0, false);
             }
             ++nq;
             // the single row-value buffer is free once every compute warp has
@@ -284,8 +388,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 4 && got; ++c) got = wait(S::kPChunk + c, (it - 1) & 1);
                 if (!got) break;
             }
-            if (leader) {
-                const size_t ro = static_cast<size_t>(bh) * p.Sq_pad + q0;
+            if constexpr (VARLEN) {
+                load_rows_packed<128>(p, u, q0, reinterpret_cast<float *>(smem_raw + S::kOffRows), bar(S::kLFull),
+                                      leader);
+            } else if (leader) {
+                const size_t ro = static_cast<size_t>(u.z) * p.Sq_pad + q0;
                 ptx::bar_arrive_expect_tx(bar(S::kLFull), 2 * 128 * 4);
                 ptx::bulk_load(ssmall + S::kOffRows, p.lse2 + ro, 128 * 4, bar(S::kLFull));
                 ptx::bulk_load(ssmall + S::kOffRows + 128 * 4, p.delta + ro, 128 * 4, bar(S::kLFull));
@@ -408,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::reg_fence(sv);
                 ptx::reg_fence(dpv);
                 const int qc = q0 + 32 * c;
-                const bool need_mask = (CAUSAL && key > qc) || key >= p.Sk;
+                const bool need_mask = (CAUSAL && key > qc) || key >= u.Lk;
                 uint32_t pp[16], dd[16];
                 const float4 *lq = reinterpret_cast<const float4 *>(rows_lse + 32 * c);
                 const float4 *dq4 = reinterpret_cast<const float4 *>(rows_lse + 128 + 32 * c);
@@ -421,8 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float e0 = ptx::ex2(fmaf(__uint_as_float(sv[j]), p.scale_log2, -l0));
                     float e1 = ptx::ex2(fmaf(__uint_as_float(sv[j + 1]), p.scale_log2, -l1));
                     if (need_mask) {
-                        if ((CAUSAL && key > qc + j) || key >= p.Sk) e0 = 0.f;
-                        if ((CAUSAL && key > qc + j + 1) || key >= p.Sk) e1 = 0.f;
+                        if ((CAUSAL && key > qc + j) || key >= u.Lk) e0 = 0.f;
+                        if ((CAUSAL && key > qc + j + 1) || key >= u.Lk) e1 = 0.f;
                     }
                     pp[j / 2] = ptx::pack2<BF16>(e0, e1);
                     dd[j / 2] = ptx::pack2<BF16>(e0 * (__uint_as_float(dpv[j]) - d0),
@@ -484,8 +591,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The TMEM loads are warp-collective (.sync.aligned): every lane runs
         // them; only the global stores are limited to keys that exist.
         if (ok) {
-            const bool row_valid = key < p.Sk;
-            const size_t row_g = (static_cast<size_t>(bh) * p.Sk + key) * D + h * (D / 2);
+            const bool row_valid = key < u.Lk;
+            const size_t row_g = (VARLEN ? (static_cast<size_t>(u.tk0) + key) * p.H + u.hh
+                                         : static_cast<size_t>(u.z) * p.Sk + key) * D + h * (D / 2);
             const uint64_t once = ptx::l2_policy_evict_first();
 #pragma unroll 1
             for (int t = 0; t < 2; ++t) {
@@ -530,7 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < D / 32; ++c) {
                     const uint32_t box = sbase + (c < D / 64 ? S::kOffQ + s * S::kTileBytes + c * S::kBoxBytes
                                                              : S::kOffDO + s * S::kTileBytes + (c - D / 64) * S::kBoxBytes);
-                    ptx::tma_reduce_add_3d(&tm_dq, box, 32 * c, q0, bh);  // rows past Sq are clipped
+                    int y, z;
+                    unit_coords<VARLEN>(u, false, q0, y, z);
+                    ptx::tma_reduce_add_3d(&tm_dq, box, 32 * c, y, z);  // rows past the tensor are clipped
                 }
                 ptx::bulk_commit();
                 ptx::bulk_wait_read_all();  // the stage may be refilled now
@@ -626,7 +736,7 @@ struct ShapeQ64 {
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
-template <bool BF16, bool CAUSAL>
+template <bool BF16, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kThreadsQ64, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -646,13 +756,23 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
         return __all_sync(0xffffffffu, ptx::bar_wait(bar(i), parity, abort_flag, p.timeout_ns));
     };
 
-    // work item: key tile kt of head bh, heavy causal tiles first; sub-steps of
-    // 64 queries from the first query that sees any of these keys
-    int kt, bh;
-    bwd_work(p, kt, bh);
+    // work item: key tile kt of a head (dense) or of a sequence's head (packed),
+    // heavy causal tiles first; sub-steps of 64 queries from the first query
+    // that sees any of these keys
+    const BwdUnit u = bwd_unit<VARLEN>(p);
+    if constexpr (VARLEN) {
+        // packed: offsets outside the tensors are reported and skipped; a
+        // key tile past the sequence's keys has nothing to compute or write
+        if (!u.ok) {
+            if (threadIdx.x == 0) atomicExch(p.err, kDeviceErrSeqLens);
+            return;
+        }
+        if (u.kt * kBlock >= u.Lk) return;
+    }
+    const int kt = u.kt;
     const int k0 = kt * kBlock;
     const int qs0 = CAUSAL ? k0 : 0;
-    const int n = p.Sq > qs0 ? (p.Sq - qs0 + S::kQ - 1) / S::kQ : 0;
+    const int n = u.Lq > qs0 ? (u.Lq - qs0 + S::kQ - 1) / S::kQ : 0;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S::kNumBars; ++i) {
@@ -690,10 +810,12 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             // the Q, dO and dQ accumulator rows the head's other CTAs reuse
             const uint64_t once = ptx::l2_policy_evict_first();
             ptx::bar_arrive_expect_tx(bar(S::kKVFull), 2 * S::kKTileBytes);
+            int ky, kz;
+            unit_coords<VARLEN>(u, true, k0, ky, kz);
             for (int c = 0; c < 2; ++c) {
-                ptx::tma_load_3d_hint(sbase + S::kOffK + c * S::kKBoxBytes, &tm_k, bar(S::kKVFull), c * 64, k0, bh,
+                ptx::tma_load_3d_hint(sbase + S::kOffK + c * S::kKBoxBytes, &tm_k, bar(S::kKVFull), c * 64, ky, kz,
                                       once);
-                ptx::tma_load_3d_hint(sbase + S::kOffV + c * S::kKBoxBytes, &tm_v, bar(S::kKVFull), c * 64, k0, bh,
+                ptx::tma_load_3d_hint(sbase + S::kOffV + c * S::kKBoxBytes, &tm_v, bar(S::kKVFull), c * 64, ky, kz,
                                       once);
             }
         }
@@ -706,18 +828,24 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             if (leader) {
                 const uint32_t qb = sbase + S::kOffQ + st * S::kStageBytes;
                 ptx::bar_arrive_expect_tx(bar(S::kQFull + st), S::kStageBytes);
+                int qy, qz;
+                unit_coords<VARLEN>(u, false, q0, qy, qz);
                 for (int c = 0; c < 2; ++c) {
-                    ptx::tma_load_3d(qb + c * S::kQBoxBytes, &tm_q, bar(S::kQFull + st), c * 64, q0, bh);
+                    ptx::tma_load_3d(qb + c * S::kQBoxBytes, &tm_q, bar(S::kQFull + st), c * 64, qy, qz);
                     ptx::tma_load_3d(qb + S::kQTileBytes + c * S::kQBoxBytes, &tm_do, bar(S::kQFull + st), c * 64,
-                                     q0, bh);
+                                     qy, qz);
                 }
             }
             ++nq;
             // row buffer b is free once the key-row warps are done with sub-step j-2
             if (j >= 2 && !wait(S::kPFull + b, ((j - 2) >> 1) & 1)) break;
-            if (leader) {
+            if constexpr (VARLEN) {
+                load_rows_packed<S::kQ>(p, u, q0,
+                                        reinterpret_cast<float *>(smem_raw + S::kOffRows + b * 2 * S::kQ * 4),
+                                        bar(S::kLFull + b), leader);
+            } else if (leader) {
                 const uint32_t rows = ssmall + S::kOffRows + b * 2 * S::kQ * 4;
-                const size_t ro = static_cast<size_t>(bh) * p.Sq_pad + q0;
+                const size_t ro = static_cast<size_t>(u.z) * p.Sq_pad + q0;
                 ptx::bar_arrive_expect_tx(bar(S::kLFull + b), 2 * S::kQ * 4);
                 ptx::bulk_load(rows, p.lse2 + ro, S::kQ * 4, bar(S::kLFull + b));
                 ptx::bulk_load(rows + S::kQ * 4, p.delta + ro, S::kQ * 4, bar(S::kLFull + b));
@@ -855,7 +983,7 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             ptx::tmem_ld_wait();
             ptx::reg_fence(sv);
             ptx::reg_fence(dpv);
-            const bool need_mask = (CAUSAL && key > qc) || key >= p.Sk;
+            const bool need_mask = (CAUSAL && key > qc) || key >= u.Lk;
             const float *rows = reinterpret_cast<const float *>(smem_raw + S::kOffRows + b * 2 * S::kQ * 4);
             const float4 *lq = reinterpret_cast<const float4 *>(rows + 32 * h);
             const float4 *dq4 = reinterpret_cast<const float4 *>(rows + S::kQ + 32 * h);
@@ -868,8 +996,8 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
                 float e0 = ptx::ex2(fmaf(__uint_as_float(sv[i]), p.scale_log2, -l0));
                 float e1 = ptx::ex2(fmaf(__uint_as_float(sv[i + 1]), p.scale_log2, -l1));
                 if (need_mask) {
-                    if ((CAUSAL && key > qc + i) || key >= p.Sk) e0 = 0.f;
-                    if ((CAUSAL && key > qc + i + 1) || key >= p.Sk) e1 = 0.f;
+                    if ((CAUSAL && key > qc + i) || key >= u.Lk) e0 = 0.f;
+                    if ((CAUSAL && key > qc + i + 1) || key >= u.Lk) e1 = 0.f;
                 }
                 pp[i / 2] = ptx::pack2<BF16>(e0, e1);
                 dd[i / 2] = ptx::pack2<BF16>(e0 * (__uint_as_float(dpv[i]) - d0),
@@ -900,8 +1028,9 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
         // The TMEM loads are warp-collective (.sync.aligned): every lane runs
         // them; only the global stores are limited to keys that exist.
         if (ok) {
-            const bool row_valid = key < p.Sk;
-            const size_t row_g = (static_cast<size_t>(bh) * p.Sk + key) * D + h * (D / 2);
+            const bool row_valid = key < u.Lk;
+            const size_t row_g = (VARLEN ? (static_cast<size_t>(u.tk0) + key) * p.H + u.hh
+                                         : static_cast<size_t>(u.z) * p.Sk + key) * D + h * (D / 2);
             const uint64_t once = ptx::l2_policy_evict_first();
 #pragma unroll 1
             for (int t = 0; t < 2; ++t) {
@@ -978,8 +1107,10 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
                 const int q0 = qs0 + j * S::kQ;
                 const uint32_t tile = sbase + S::kOffQ + st * S::kStageBytes;
 #pragma unroll
+                int y, z;
+                unit_coords<VARLEN>(u, false, q0, y, z);
                 for (int c = 0; c < D / 32; ++c)
-                    ptx::tma_reduce_add_3d(&tm_dq, tile + c * S::kDQBoxBytes, 32 * c, q0, bh);
+                    ptx::tma_reduce_add_3d(&tm_dq, tile + c * S::kDQBoxBytes, 32 * c, y, z);
                 ptx::bulk_commit();
                 ptx::bulk_wait_read_all();  // the stage may be refilled now
                 ptx::bar_arrive(bar(S::kStageFree + st));
@@ -1000,16 +1131,16 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
     if (threadIdx.x == 0 && *abort_flag) atomicExch(p.err, kDeviceErrTimeout);
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 cudaError_t launch_t(const CUtensorMap *maps, const void *o, const void *dout, const float *lse, void *dq,
                      const BwdParams &p, cudaStream_t st) {
-    const long long rows = static_cast<long long>(p.BH) * p.Sq_pad;
-    fa_bwd_prep_kernel<D, BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+    const long long rows = VARLEN ? static_cast<long long>(p.H) * p.total_q : static_cast<long long>(p.BH) * p.Sq_pad;
+    fa_bwd_prep_kernel<D, BF16, VARLEN><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
         static_cast<const uint16_t *>(o), static_cast<const uint16_t *>(dout), lse, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // D = 64: 128-query steps; D = 128: 64-query sub-steps, double-buffered in TMEM
-    auto kern = D == 64 ? fa_bwd_d64_kernel<64, BF16, CAUSAL> : fa_bwd_kernel<BF16, CAUSAL>;
+    auto kern = D == 64 ? fa_bwd_d64_kernel<64, BF16, CAUSAL, VARLEN> : fa_bwd_kernel<BF16, CAUSAL, VARLEN>;
     constexpr int kSmem = D == 64 ? Shape<64>::kSmemBytes : ShapeQ64::kSmemBytes;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
@@ -1017,22 +1148,12 @@ cudaError_t launch_t(const CUtensorMap *maps, const void *o, const void *dout, c
         maps[0], maps[1], maps[2], maps[3], maps[4], p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const long long n8 = static_cast<long long>(p.BH) * p.Sq * D / 8;
+    const long long n8 = (VARLEN ? static_cast<long long>(p.total_q) * p.H : static_cast<long long>(p.BH) * p.Sq) * D / 8;
     fa_bwd_dq_kernel<BF16><<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, st>>>(
         p.dq_acc, static_cast<uint16_t *>(dq), n8, p.scale);
     return cudaGetLastError();
 }
 
 }  // namespace bwd
-
-cudaError_t launch_bwd(int D, bool bf16, bool causal, const CUtensorMap *maps, const void *o, const void *dout,
-                       const float *lse, void *dq, const BwdParams &p, cudaStream_t stream) {
-#define FA_BWD(DD, BB, CC) \
-    if (D == DD && bf16 == BB && causal == CC) return bwd::launch_t<DD, BB, CC>(maps, o, dout, lse, dq, p, stream);
-    FA_BWD(64, false, false) FA_BWD(64, false, true) FA_BWD(64, true, false) FA_BWD(64, true, true)
-    FA_BWD(128, false, false) FA_BWD(128, false, true) FA_BWD(128, true, false) FA_BWD(128, true, true)
-#undef FA_BWD
-    return cudaErrorInvalidValue;
-}
 
 }  // namespace fa

@@ -80,24 +80,34 @@ struct DecodeParams {
     int *counters;               // fused: [B*H] finished partitions per head, zero between calls
 };
 
-// Parameters of the backward pass (dense [B,H,S,D] layout).
+// Parameters of the backward pass: dense [B,H,S,D] or packed [T,H,D] layout.
+// A work unit is a head (dense) or a (sequence, head) pair (packed).
 struct BwdParams {
-    float *lse2;           // [B*H][Sq_pad] forward LSE * log2(e); +inf past Sq
-    float *delta;          // [B*H][Sq_pad] D_i = sum_d dO_id O_id; 0 past Sq
-    float *dq_acc;         // [B*H][Sq][D] fp32 accumulator of dS K
-    void *dk, *dv;         // [B*H][Sk][D] outputs (input dtype)
-    int BH, Sq, Sk;
-    int Sq_pad;            // Sq rounded up to whole 128-row tiles
+    float *lse2;           // dense [B*H][Sq_pad], +inf past Sq | packed [H][total_q]: forward LSE * log2(e)
+    float *delta;          // same layout: D_i = sum_d dO_id O_id (0 past Sq, dense)
+    float *dq_acc;         // dense [B*H][Sq][D] | packed [total_q][H][D]: fp32 accumulator of dS K
+    void *dk, *dv;         // dense [B*H][Sk][D] | packed [total_k][H][D] outputs (input dtype)
+    int BH;                // work units: B*H (dense), num_seqs*H (packed)
+    int Sq, Sk;            // dense: lengths; packed: max_seqlen_q, max_seqlen_k
+    int Sq_pad;            // dense: Sq rounded up to whole 128-row tiles
     int n_qtiles, n_ktiles;
-    int heads_per_group;   // CTAs run head group by head group (see bwd_work)
+    int heads_per_group;   // CTAs run work units group by group (see bwd_work)
+    const int *cu_q;       // packed: int32[num_seqs + 1]
+    const int *cu_k;       // packed: int32[num_seqs + 1]
+    int H;                 // packed: heads
+    int total_q, total_k;  // packed: tokens
     float scale, scale_log2;
     int *err;              // device error word
     unsigned long long timeout_ns;
 };
 
-// maps: {Q, K, V, dO, dQ accumulator (fp32)}; lse [B*H][Sq]; dq output (input dtype).
-cudaError_t launch_bwd(int D, bool bf16, bool causal, const CUtensorMap *maps, const void *o, const void *dout,
-                       const float *lse, void *dq, const BwdParams &p, cudaStream_t stream);
+// maps: {Q, K, V, dO, dQ accumulator (fp32)}; lse dense [B*H][Sq] | packed
+// [H][total_q]; dq output (input dtype). Dense maps are 3-D {D, S, B*H},
+// packed maps {D, H, tokens}.
+cudaError_t launch_bwd_dense(int D, bool bf16, bool causal, const CUtensorMap *maps, const void *o,
+                             const void *dout, const float *lse, void *dq, const BwdParams &p, cudaStream_t stream);
+cudaError_t launch_bwd_varlen(int D, bool bf16, bool causal, const CUtensorMap *maps, const void *o,
+                              const void *dout, const float *lse, void *dq, const BwdParams &p, cudaStream_t stream);
 
 // maps: {Q, K, V} tensor maps (see fa_api.cu for their geometry).
 cudaError_t launch_fwd_dense(int D, bool bf16, bool causal, const CUtensorMap *maps,

@@ -281,12 +281,56 @@ FA_API fa_status_t fa_bwd(const void *q, const void *k, const void *v, const voi
                           float scale, fa_dtype_t dtype, void *stream);
 
 /*
+ * fa_bwd_varlen_workspace_bytes - bytes of fp32 workspace fa_bwd_varlen needs:
+ * 4 * (total_q*H*D + 2*H*total_q); 0 for an invalid shape.
+ */
+FA_API size_t fa_bwd_varlen_workspace_bytes(int total_q, int H, int D);
+
+/*
+ * fa_bwd_varlen - the backward pass over packed sequences of different lengths.
+ *
+ * Defined by "Adaptive High-Performance Attention Kernels in CUDA" (Advanced
+ * Production Features 2, Custom CUDA Backward Pass, and 3, Ragged / Variable-
+ * Length Sequences): the gradients of fa_fwd_varlen. Each sequence is an
+ * independent attention over its own keys, so its gradients are those of
+ * fa_bwd on that sequence alone; causal positions count from each sequence's
+ * start (top-left, as in fa_fwd_varlen).
+ *
+ *   q, o, dout    [total_q,H,D]  fp16/bf16   k, v [total_k,H,D]  same dtype
+ *   lse           [H,total_q] fp32, as written by fa_fwd_varlen
+ *   dq [total_q,H,D], dk and dv [total_k,H,D]: outputs in the input dtype;
+ *                 rows of tokens outside every sequence are left unwritten in
+ *                 dk and dv, and dq rows outside every sequence are zero
+ *   cu_seqlens_q, cu_seqlens_k   device int32[num_seqs+1], as in fa_fwd_varlen
+ *   max_seqlen_q, max_seqlen_k   >= every query / key length (size the launch)
+ *   workspace     caller-owned device memory of at least
+ *                 fa_bwd_varlen_workspace_bytes(total_q, H, D) bytes, 16-byte
+ *                 aligned; its contents on entry do not matter. Calls sharing
+ *                 a workspace must not overlap on the GPU.
+ *   D             64 or 128.
+ * Keys of a sequence without queries get dK = dV = 0. Three launches on
+ * `stream`; dQ's fp32 additions make its rounding run-dependent, dK and dV are
+ * deterministic. The offsets are checked on the device: a sequence whose
+ * offsets lie outside the tensors, or that is longer than max_seqlen_q /
+ * max_seqlen_k, is skipped (its gradients are not written) and the next
+ * fa_check_device_error returns FA_ERR_DEVICE_SEQLENS.
+ * Errors: FA_ERR_NULL, FA_ERR_SHAPE, FA_ERR_HEADDIM, FA_ERR_DTYPE,
+ * FA_ERR_ALIGN, FA_ERR_SCALE, FA_ERR_WORKSPACE, FA_ERR_CUDA.
+ */
+FA_API fa_status_t fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                                 const float *lse, void *dq, void *dk, void *dv, float *workspace,
+                                 size_t workspace_bytes, const int32_t *cu_seqlens_q,
+                                 const int32_t *cu_seqlens_k, int num_seqs, int total_q, int total_k,
+                                 int max_seqlen_q, int max_seqlen_k, int H, int D, int causal, float scale,
+                                 fa_dtype_t dtype, void *stream);
+
+/*
  * fa_check_device_error - synchronise `stream`, then read and clear the
  * current device's error word. Kernels bound every wait on an on-chip barrier;
  * a wait that runs out sets the word, releases what the CTA holds and returns.
  * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT, FA_ERR_DEVICE_INDEX (an out-of-range
  * block-table entry was skipped), FA_ERR_DEVICE_SEQLENS (a packed-sequence
- * launch found inconsistent cu_seqlens and computed nothing), or FA_ERR_CUDA
+ * launch found inconsistent cu_seqlens: see fa_fwd_varlen, fa_bwd_varlen), or FA_ERR_CUDA
  * when the runtime itself reports an error.
  */
 FA_API fa_status_t fa_check_device_error(void *stream);

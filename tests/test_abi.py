@@ -193,6 +193,30 @@ def test_bwd_validation(lib):
     assert lib.fa_bwd_workspace_bytes(1, 2, 200, 96) == 0
 
 
+def _bwd_varlen(lib, q=A, k=A, v=A, o=A, do=A, lse=A, dq=A, dk=A, dv=A, ws=A, wsb=1 << 30, cq=A, ck=A, nseq=3,
+                Tq=500, Tk=600, mq=300, mk=320, H=2, D=128, causal=1, scale=0.1, dtype=1):
+    return lib.fa_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, ws, wsb, cq, ck, nseq, Tq, Tk, mq, mk, H, D, causal,
+                             scale, dtype, None)
+
+
+def test_bwd_varlen_validation(lib):
+    for kw in ("q", "k", "v", "o", "do", "lse", "dq", "dk", "dv", "ws", "cq", "ck"):
+        assert _bwd_varlen(lib, **{kw: None}) == NULL, kw
+    assert _bwd_varlen(lib, dtype=2) == DTYPE
+    assert _bwd_varlen(lib, D=256) == HEADDIM
+    for kw in ({"nseq": 0}, {"Tq": 0}, {"Tk": 0}, {"mq": 0}, {"mk": 0}, {"H": 0}, {"Tq": (1 << 30) + 1},
+               {"nseq": 1 << 20, "H": 1 << 12}):
+        assert _bwd_varlen(lib, **kw) == SHAPE, kw
+    assert _bwd_varlen(lib, scale=-1.0) == SCALE
+    for kw in ("q", "dk", "ws"):
+        assert _bwd_varlen(lib, **{kw: MIS}) == ALIGN, kw
+    assert _bwd_varlen(lib, cq=A + 2) == ALIGN
+    need = lib.fa_bwd_varlen_workspace_bytes(500, 2, 128)
+    assert need == 4 * (500 * 2 * 128 + 2 * 2 * 500)
+    assert _bwd_varlen(lib, wsb=need - 4) == -12
+    assert lib.fa_bwd_varlen_workspace_bytes(500, 2, 80) == 0
+
+
 def test_merge_validation(lib):
     m = lib.fa_splitkv_merge
     assert m(None, A, A, A, A, 2, 2, 128, 8, 1, None) == NULL

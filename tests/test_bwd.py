@@ -7,19 +7,15 @@ of a few 2^-9 of the magnitudes that meet in its sum; the check is
 max |g - ref| <= 2e-2 * max(1, max |ref|) per tensor, plus
 ||g - ref|| <= 1e-2 * max(||ref||, sqrt(n)). Bookkeeping is exact: keys no query can see get
 dK = dV = 0 bit for bit, and dK, dV are bitwise repeatable."""
-import numpy as np
 import pytest
 import torch
 
 import exact_attention_54_gb300 as fa
 import oracle
 from exact_attention_54_gb300 import inputs
-from gpu_helpers import dev
+from gpu_helpers import assert_grad_close, dev
 
 pytestmark = pytest.mark.gpu
-
-GRAD_TOL = 2e-2
-FRO_TOL = 1e-2
 
 
 def grads(q, k, v, do, causal, scale):
@@ -29,20 +25,6 @@ def grads(q, k, v, do, causal, scale):
     torch.cuda.synchronize()
     fa.fa_check_device_error()
     return dq.cpu(), dk.cpu(), dv.cpu()
-
-
-def assert_grad_close(got, ref, what):
-    g = got.double().numpy() if hasattr(got, "numpy") else np.asarray(got, np.float64)
-    r = np.asarray(ref, np.float64)
-    assert g.shape == r.shape, (what, g.shape, r.shape)
-    assert np.all(np.isfinite(g)), f"{what}: non-finite values"
-    err = float(np.max(np.abs(g - r)))
-    bound = GRAD_TOL * max(1.0, float(np.max(np.abs(r))))
-    # Frobenius error relative to the reference, floored (like the max bound)
-    # at an O(1) scale per element: an exactly zero reference (one key) only
-    # meets rounding noise
-    fro = float(np.linalg.norm(g - r) / max(np.linalg.norm(r), np.sqrt(r.size)))
-    assert err <= bound and fro <= FRO_TOL, f"{what}: max err {err:.3e} (bound {bound:.3e}), rel fro {fro:.3e}"
 
 
 def check(B, H, Sq, Sk, D, dtype, causal, seed, scale=None):

@@ -393,19 +393,23 @@ def run_gpu(args, rank, world, local):
         if evs:
             evs[2].record(stream)
 
-    for _ in range(args.warmup):
-        step()
+    # one untimed pass checks the device error word before anything is timed
+    step()
     torch.cuda.synchronize()
     fa.fa_check_device_error()
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)  # nvidia-smi start-up; samples before t_begin are discarded
+    # the W warm-up steps run right before the timed ones, so that the timed
+    # region does not start on a GPU that has just idled for the sampler
+    for _ in range(args.warmup):
+        step()
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)  # nvidia-smi start-up; samples before t_begin are discarded
     t_begin = time.time()
     t0 = time.perf_counter()
     for i in range(args.steps):

@@ -658,27 +658,39 @@ __device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, i
             orow = static_cast<Elem *>(p.o) + (static_cast<size_t>(wk.seq_q0 + q_row) * p.H + wk.h) * D;
         else
             orow = static_cast<Elem *>(p.o) + (static_cast<size_t>(wk.b * p.H + wk.h) * p.Sq + q_row) * D;
+        uint32_t o[D / 32][32];
+        if (nkv > 0) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(tO + c * 32, o[c]);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) ptx::reg_fence(o[c]);
+        } else {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[c][i] = 0u;
+        }
+        // One wait for all of O's TMEM loads; rows go out in 32-byte stores
+        // when O is 32-byte aligned (every row then is: a row is D * 2 bytes).
+        const bool v8 = (reinterpret_cast<uintptr_t>(p.o) & 31) == 0;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            if (nkv > 0) {
-                ptx::tmem_ld32(tO + c * 32, o);
-                ptx::tmem_ld_wait();
-                ptx::reg_fence(o);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = 0u;
-            }
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-                pk[i] = ptx::pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+                pk[i] = ptx::pack2<BF16>(__uint_as_float(o[c][2 * i]) * inv_l, __uint_as_float(o[c][2 * i + 1]) * inv_l);
             if (row_valid) {
                 // O and LSE are written once: evict them first, keep L2 for K and V
                 uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                if (v8) {
+                    ptx::st_global_v8_hint(dst, pk, stream_pol);
+                    ptx::st_global_v8_hint(dst + 2, pk + 8, stream_pol);
+                } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    ptx::st_global_v4_hint(dst + i, pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3], stream_pol);
+                    for (int i = 0; i < 4; ++i)
+                        ptx::st_global_v4_hint(dst + i, pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3], stream_pol);
+                }
             }
         }
         if (row_valid) {

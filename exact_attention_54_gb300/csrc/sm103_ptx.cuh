@@ -143,6 +143,14 @@ __device__ __forceinline__ void st_global_v4_hint(void *ptr, uint32_t a, uint32_
                  : "memory");
 }
 
+// 32-byte global store with an L2 cache-policy hint (the address must be
+// 32-byte aligned).
+__device__ __forceinline__ void st_global_v8_hint(void *ptr, const uint32_t *v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(ptr), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "l"(policy)
+                 : "memory");
+}
+
 // 4-byte global store with an L2 cache-policy hint.
 __device__ __forceinline__ void st_global_f32_hint(float *ptr, float v, uint64_t policy) {
     asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(policy) : "memory");

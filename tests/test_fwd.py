@@ -176,6 +176,35 @@ def test_outputs_do_not_spill_past_the_buffer(D):
     assert torch.all(l_buf[B * H * Sq:] == 7.0)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_output_aligned_to_16_bytes_only(D):
+    """O may start 16 bytes past a 32-byte boundary (the entry point asks for
+    16-byte alignment); its rows are then written with 16-byte stores instead
+    of 32-byte ones. The values must be bit-identical to those written into
+    an aligned buffer, nothing outside the view may change, and O must match
+    the oracle."""
+    B, H, Sq = 1, 2, 200
+    q, k, v = inputs.make_dense(B, H, Sq, Sq, D, torch.bfloat16, seed=17)
+    qd, kd, vd = dev(q, k, v)
+    n = B * H * Sq * D
+    o_buf = torch.full((n + 64,), 1.5, dtype=torch.bfloat16, device="cuda")
+    o = o_buf[8: 8 + n].view(B, H, Sq, D)
+    assert o.data_ptr() % 32 == 16
+    lse = torch.empty(B, H, Sq, dtype=torch.float32, device="cuda")
+    fa.fa_fwd(qd, kd, vd, o, lse, True, 0.1)
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    assert torch.all(o_buf[:8] == 1.5) and torch.all(o_buf[8 + n:] == 1.5)
+    o_al, l_al = fa.flash_attention(qd, kd, vd, causal=True, scale=0.1)
+    torch.cuda.synchronize()
+    assert o_al.data_ptr() % 32 == 0
+    assert torch.equal(o.view(torch.int16), o_al.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), l_al.view(torch.int32))
+    ro, rl = oracle.attention(q, k, v, True, 0.1)
+    assert_close(o.cpu(), ro, O_TOL, "O at a 16-byte offset")
+    assert_close(lse.cpu(), rl, LSE_TOL, "LSE")
+
+
 def test_repeatable_bitwise():
     q, k, v = inputs.make_dense(2, 4, 512, 512, 128, torch.bfloat16, seed=15)
     o1, l1 = run(q, k, v, True, 0.09)

@@ -516,6 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::reg_fence(dpv);
                 const int qc = q0 + 32 * c;
                 const bool need_mask = (CAUSAL && key > qc) || key >= u.Lk;
+                // queries j < lo of the chunk do not see this key (causal: a
+                // key is seen from its own position on; a key past Lk by none)
+                const int lo = key >= u.Lk ? 32 : (CAUSAL ? key - qc : 0);
                 uint32_t pp[16], dd[16];
                 const float4 *lq = reinterpret_cast<const float4 *>(rows_lse + 32 * c);
                 const float4 *dq4 = reinterpret_cast<const float4 *>(rows_lse + 128 + 32 * c);
@@ -528,8 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float e0 = ptx::ex2(fmaf(__uint_as_float(sv[j]), p.scale_log2, -l0));
                     float e1 = ptx::ex2(fmaf(__uint_as_float(sv[j + 1]), p.scale_log2, -l1));
                     if (need_mask) {
-                        if ((CAUSAL && key > qc + j) || key >= u.Lk) e0 = 0.f;
-                        if ((CAUSAL && key > qc + j + 1) || key >= u.Lk) e1 = 0.f;
+                        if (j < lo) e0 = 0.f;
+                        if (j + 1 < lo) e1 = 0.f;
                     }
                     pp[j / 2] = ptx::pack2<BF16>(e0, e1);
                     dd[j / 2] = ptx::pack2<BF16>(e0 * (__uint_as_float(dpv[j]) - d0),
@@ -984,6 +987,7 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             ptx::reg_fence(sv);
             ptx::reg_fence(dpv);
             const bool need_mask = (CAUSAL && key > qc) || key >= u.Lk;
+            const int lo = key >= u.Lk ? 32 : (CAUSAL ? key - qc : 0);  // queries i < lo do not see the key
             const float *rows = reinterpret_cast<const float *>(smem_raw + S::kOffRows + b * 2 * S::kQ * 4);
             const float4 *lq = reinterpret_cast<const float4 *>(rows + 32 * h);
             const float4 *dq4 = reinterpret_cast<const float4 *>(rows + S::kQ + 32 * h);
@@ -996,8 +1000,8 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
                 float e0 = ptx::ex2(fmaf(__uint_as_float(sv[i]), p.scale_log2, -l0));
                 float e1 = ptx::ex2(fmaf(__uint_as_float(sv[i + 1]), p.scale_log2, -l1));
                 if (need_mask) {
-                    if ((CAUSAL && key > qc + i) || key >= u.Lk) e0 = 0.f;
-                    if ((CAUSAL && key > qc + i + 1) || key >= u.Lk) e1 = 0.f;
+                    if (i < lo) e0 = 0.f;
+                    if (i + 1 < lo) e1 = 0.f;
                 }
                 pp[i / 2] = ptx::pack2<BF16>(e0, e1);
                 dd[i / 2] = ptx::pack2<BF16>(e0 * (__uint_as_float(dpv[i]) - d0),

@@ -420,12 +420,12 @@ __device__ void softmax_role(const FwdParams &p, uint32_t sbase, uint32_t tmem, 
             const int k0 = i * kBlockN;
             const bool need_mask = (k0 + kBlockN > wk.Lk) || (CAUSAL && k0 + kBlockN - 1 > wk.q_start);
             if (need_mask) {
+                // the row sees columns c < lim: the sequence's end and, causal, its own position
+                int lim = wk.Lk - k0;
+                if (CAUSAL) lim = min(lim, q_row + 1 - k0);
 #pragma unroll
-                for (int c = 0; c < kBlockN; ++c) {
-                    const int key = k0 + c;
-                    const bool vis = key < wk.Lk && (!CAUSAL || key <= q_row);
-                    if (!vis) s[c / 32][c % 32] = 0xff800000u;  // -inf
-                }
+                for (int c = 0; c < kBlockN; ++c)
+                    if (c >= lim) s[c / 32][c % 32] = 0xff800000u;  // -inf
             }
             float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll

@@ -553,15 +553,18 @@ __device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, i
             ptx::tmem_ld32(tS + 64, s[2]);
             ptx::tmem_ld32(tS + 96, s[3]);
 
+            // The keys of this tile that the row sees are the columns c < lim:
+            // the sequence ends at Lk and, causal, the row sees keys up to its
+            // own position. Tiles inside both limits (need_mask false, the
+            // same for the whole warpgroup) are not tested.
             const int k0 = j * kBlockN;
             const bool need_mask = (k0 + kBlockN > wk.Lk) || (CAUSAL && k0 + kBlockN - 1 > wk.q_start[t]);
+            int lim = wk.Lk - k0;
+            if (CAUSAL) lim = min(lim, q_row + 1 - k0);
             auto mask_half = [&](int h) {
 #pragma unroll
-                for (int c = 64 * h; c < 64 * h + 64; ++c) {
-                    const int key = k0 + c;
-                    const bool vis = key < wk.Lk && (!CAUSAL || key <= q_row);
-                    if (!vis) s[c / 32][c % 32] = 0xff800000u;  // -inf
-                }
+                for (int c = 64 * h; c < 64 * h + 64; ++c)
+                    if (c >= lim) s[c / 32][c % 32] = 0xff800000u;  // -inf
             };
             // row maximum of the raw scores: four chains of three-input max
             float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};

@@ -23,6 +23,7 @@ import torch
 __all__ = ["FAError", "fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_decode_paged_splitkv", "fa_splitkv_merge",
            "fa_decode_splitkv_fused", "fa_decode_paged_splitkv_fused", "fa_bwd", "fa_bwd_workspace_bytes",
            "fa_bwd_varlen", "fa_bwd_varlen_workspace_bytes", "fa_check_device_error", "fa_status_string",
+           "fa_test_withhold_load",
            "flash_attention", "flash_attention_varlen", "flash_attention_bwd", "flash_attention_varlen_bwd",
            "flash_decode", "flash_decode_paged", "library_path", "load_library", "EXPORTED_SYMBOLS"]
 
@@ -36,7 +37,7 @@ FA_MAX_SPLITS = 1024
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_decode_paged_splitkv", "fa_splitkv_merge",
                     "fa_decode_splitkv_fused", "fa_decode_paged_splitkv_fused", "fa_bwd", "fa_bwd_workspace_bytes",
                     "fa_bwd_varlen", "fa_bwd_varlen_workspace_bytes", "fa_check_device_error", "fa_status_string",
-                    "fa_version")
+                    "fa_version", "fa_test_withhold_load")
 
 
 class FAError(RuntimeError):
@@ -71,6 +72,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.fa_decode_paged_splitkv_fused.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i,
                                                       f, i, vp]
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, i, f, i, vp]
+        lib.fa_test_withhold_load.argtypes = [i, ctypes.c_ulonglong]
         lib.fa_bwd.restype = ctypes.c_int
         lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
         lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
@@ -269,6 +271,13 @@ def fa_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, workspace, cu_seqlens_q, cu
                                       int(max_seqlen_q), int(max_seqlen_k), H, D, int(bool(causal)), float(scale),
                                       _dtype_code(q), _stream(stream))
     _check("fa_bwd_varlen", st)
+
+
+def fa_test_withhold_load(load: int, wait_limit_ns: int = 0):
+    """Test support: make CTA 0 of later prefill launches withhold one tile
+    load so that their bounded wait runs out (see include/fa.h); (0, 0) turns
+    it off."""
+    _check("fa_test_withhold_load", load_library().fa_test_withhold_load(int(load), int(wait_limit_ns)))
 
 
 def fa_check_device_error(stream=None):

@@ -8,6 +8,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 
 #include "fa.h"
@@ -20,6 +21,11 @@ __device__ int g_device_error_word = 0;
 constexpr int kMaxDevices = 64;
 
 // Address of the error word on the current device (looked up once per device).
+// Test support (fa_test_withhold_load): the load to withhold and the wait
+// limit every launch uses.
+std::atomic<int> g_withhold{0};
+std::atomic<unsigned long long> g_wait_limit_ns{fa::kWaitTimeoutNs};
+
 int *device_error_word() {
     static std::mutex mu;
     static int *cache[kMaxDevices] = {};
@@ -191,7 +197,8 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *
     p.num_work = static_cast<int>(n_work);
     p.scale_log2 = scale * kLog2e;
     p.err = err;
-    p.timeout_ns = fa::kWaitTimeoutNs;
+    p.timeout_ns = g_wait_limit_ns.load();
+    p.withhold = g_withhold.load();
     const int grid = p.num_work < sms ? p.num_work : sms;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     const cudaError_t e = D > 256    ? fa::launch_fwd_splitd(D, bf16, causal != 0, false, maps, p, grid, st)
@@ -246,7 +253,8 @@ fa_status_t fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, 
     p.num_work = static_cast<int>(n_work);
     p.scale_log2 = scale * kLog2e;
     p.err = err;
-    p.timeout_ns = fa::kWaitTimeoutNs;
+    p.timeout_ns = g_wait_limit_ns.load();
+    p.withhold = g_withhold.load();
     const int grid = p.num_work < sms ? p.num_work : sms;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     const cudaError_t e = D > 256    ? fa::launch_fwd_splitd(D, bf16, causal != 0, true, maps, p, grid, st)
@@ -458,7 +466,8 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
     p.err = err;
-    p.timeout_ns = fa::kWaitTimeoutNs;
+    p.timeout_ns = g_wait_limit_ns.load();
+    p.withhold = g_withhold.load();
     const cudaError_t e = fa::launch_bwd_dense(D, bf16, causal != 0, maps, o, dout, lse, dq, p,
                                          static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -532,7 +541,8 @@ fa_status_t fa_bwd_varlen(const void *q, const void *k, const void *v, const voi
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
     p.err = err;
-    p.timeout_ns = fa::kWaitTimeoutNs;
+    p.timeout_ns = g_wait_limit_ns.load();
+    p.withhold = g_withhold.load();
     const cudaError_t e = fa::launch_bwd_varlen(D, bf16, causal != 0, maps, o, dout, lse, dq, p,
                                                 static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -553,6 +563,13 @@ fa_status_t fa_splitkv_merge(const float *o_part, const float *m_part, const flo
                                                    static_cast<int>(BH), num_splits,
                                                    static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status_t fa_test_withhold_load(int load, unsigned long long wait_limit_ns) {
+    if (load < 0) return FA_ERR_SHAPE;
+    g_withhold.store(load);
+    g_wait_limit_ns.store(wait_limit_ns == 0 ? fa::kWaitTimeoutNs : wait_limit_ns);
+    return FA_OK;
 }
 
 fa_status_t fa_check_device_error(void *stream) {

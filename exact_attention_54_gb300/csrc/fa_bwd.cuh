@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // stage s is free once the bulk reduction of step it-2 has read it
             if (it >= 2 && !wait(S::kStageFree + s, ((it >> 1) - 1) & 1)) break;
             const int q0 = (qt0 + it) * kBlock;
-            if (leader) {
+            if (leader && !withheld(p.withhold, static_cast<uint32_t>(it))) {
                 ptx::bar_arrive_expect_tx(bar(S::kQFull + s), 2 * S::kTileBytes);
                 load_rows(&tm_q, sbase + S::kOffQ + s * S::kTileBytes, bar(S::kQFull + s), q0, false);
                 load_rows(&tm_do, sbase + S::kOffDO + s * S::kTileBytes, bar(S::kQFull + s), q0, false);
@@ -828,7 +828,7 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             // the stage held sub-step j-4's staged dQ_t until its reductions read it
             if (j >= S::kStages && !wait(S::kStageFree + st, ((j / S::kStages) - 1) & 1)) break;
             const int q0 = qs0 + j * S::kQ;
-            if (leader) {
+            if (leader && !withheld(p.withhold, static_cast<uint32_t>(j))) {
                 const uint32_t qb = sbase + S::kOffQ + st * S::kStageBytes;
                 ptx::bar_arrive_expect_tx(bar(S::kQFull + st), S::kStageBytes);
                 int qy, qz;

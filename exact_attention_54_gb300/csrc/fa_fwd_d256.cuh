@@ -270,7 +270,7 @@ __device__ void producer_v(const CUtensorMap *tv, const FwdParams &p, uint32_t s
                 !(ok = ptx::warp_all(ptx::bar_wait(bar(S::kVEmpty + stage), ((it / S::kVStages) - 1) & 1, abort_flag,
                                      p.timeout_ns))))
                 break;
-            if (leader) {
+            if (leader && !withheld(p.withhold, it)) {
                 ptx::bar_arrive_expect_tx(bar(S::kVFull + stage), S::kKVTileBytes);
                 load_rows<S::kColBlocks, VARLEN>(tv, sbase + S::kOffV + stage * S::kKVTileBytes, S::kKVBoxBytes,
                                                  bar(S::kVFull + stage), wk, wk.seq_k0, j * kBlockN, p.H,

@@ -365,7 +365,7 @@ __device__ void fwd_producer_v(const CUtensorMap *tv, const FwdParams &p, uint32
                 !(ok = ptx::warp_all(ptx::bar_wait(bar(S::kVEmpty + stage), ((it / S::kVStages) - 1) & 1, abort_flag,
                                      p.timeout_ns))))
                 break;
-            if (leader) {
+            if (leader && !withheld(p.withhold, it)) {
                 ptx::bar_arrive_expect_tx(bar(S::kVFull + stage), S::kTileBytes);
                 load_kv_tile<D, VARLEN>(tv, sbase + S::kOffV + stage * S::kTileBytes, bar(S::kVFull + stage), wk, j,
                                         p.H);

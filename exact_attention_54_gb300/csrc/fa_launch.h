@@ -37,6 +37,7 @@ struct FwdParams {
     float scale_log2;      // scale * log2(e)
     int *err;              // device error word
     unsigned long long timeout_ns;
+    int withhold;          // test support, 0 = off: CTA 0 never issues its V tile load number withhold - 1
 };
 
 int fwd_smem_bytes(int D);
@@ -99,7 +100,15 @@ struct BwdParams {
     float scale, scale_log2;
     int *err;              // device error word
     unsigned long long timeout_ns;
+    int withhold;          // test support, 0 = off: CTA 0 never issues its Q/dO load number withhold - 1
 };
+
+// Test support: a launch that withholds one load (see FwdParams::withhold)
+// leaves a wait that nothing completes, so the kernel's bounded wait runs
+// out and its abort path (drain, TMEM release, error word) runs.
+__device__ __forceinline__ bool withheld(int withhold, uint32_t load) {
+    return withhold > 0 && blockIdx.x == 0 && load + 1 == static_cast<uint32_t>(withhold);
+}
 
 // maps: {Q, K, V, dO, dQ accumulator (fp32)}; lse dense [B*H][Sq] | packed
 // [H][total_q]; dq output (input dtype). Dense maps are 3-D {D, S, B*H},

@@ -13,7 +13,8 @@
  * Common rules
  *   - Every tensor pointer is a DEVICE pointer owned by the caller. The library
  *     allocates no memory and keeps no state between calls, apart from one
- *     device-resident error word per GPU (see fa_check_device_error).
+ *     device-resident error word per GPU (see fa_check_device_error) and the
+ *     test setting of fa_test_withhold_load (off unless a test turns it on).
  *   - Calls are asynchronous: work is enqueued on `stream` (a cudaStream_t
  *     passed as void*, NULL = the legacy default stream) and the call returns
  *     after the launch. Inputs must stay valid until the work completes.
@@ -334,6 +335,22 @@ FA_API fa_status_t fa_bwd_varlen(const void *q, const void *k, const void *v, co
  * when the runtime itself reports an error.
  */
 FA_API fa_status_t fa_check_device_error(void *stream);
+
+/*
+ * fa_test_withhold_load - test support for the failure path of the prefill
+ * kernels (fa_fwd, fa_fwd_varlen, fa_bwd, fa_bwd_varlen). With load = n > 0,
+ * CTA 0 of every later launch of those kernels never issues one of its tile
+ * loads (the forward's V tile n - 1, the backward's Q/dO step n - 1), so the
+ * wait for it cannot complete: the kernel's bounded wait runs out after
+ * `wait_limit_ns`, its CTAs drain the copies they issued, release tensor
+ * memory and stop, and fa_check_device_error returns FA_ERR_DEVICE_TIMEOUT.
+ * Outputs of such a launch are undefined. `wait_limit_ns` (0 = the default,
+ * one second) bounds every on-chip wait of every launch of those kernels.
+ * load = 0 and wait_limit_ns = 0 restore normal operation. The setting is
+ * process-wide; it is not meant to be changed while other threads launch.
+ * Returns FA_OK, or FA_ERR_SHAPE for a negative load.
+ */
+FA_API fa_status_t fa_test_withhold_load(int load, unsigned long long wait_limit_ns);
 
 /*
  * fa_decode_noalloc - split-KV decoding (phase 1 and phase 2 in one call) that

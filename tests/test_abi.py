@@ -227,6 +227,12 @@ def test_merge_validation(lib):
     assert m(A, A, A, MIS, A, 2, 2, 128, 8, 1, None) == ALIGN
 
 
+def test_withhold_setting_validation(lib):
+    """The failure-path test setting takes no negative load and resets with (0, 0)."""
+    assert lib.fa_test_withhold_load(-1, 0) == SHAPE
+    assert lib.fa_test_withhold_load(0, 0) == 0
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         fa.load_library(os.path.join(tmp_path, "missing.so"))

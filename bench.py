@@ -73,7 +73,7 @@ def parse_args(argv=None):
                     help="kernel seconds of the back-to-back prefill leg (0 skips it)")
     ap.add_argument("--parts", default="prefill,decode",
                     help="comma list of the path parts to run (profiling runs may isolate one: prefill, decode, "
-                         "backward, d256, splitd, varlen, varlen_backward, shapes)")
+                         "backward, d256, splitd, varlen, varlen_backward, shapes, decode_two)")
     return ap.parse_args(argv)
 
 
@@ -346,7 +346,7 @@ def run_gpu(args, rank, world, local):
         q, k, v = (t.to(dev) for t in inputs.make_workload(wp))
         o = torch.empty_like(q)
         lse = torch.empty(wp.B, wp.H, wp.Sq, dtype=torch.float32, device=dev)
-    if run_dc:
+    if run_dc or "decode_two" in parts:
         dq, dk, dv = (t.to(dev) for t in inputs.make_workload(wd))
         S = wd.num_splits
         ws = (torch.empty(wd.B, wd.H, S, wd.D, dtype=torch.float32, device=dev),
@@ -359,7 +359,7 @@ def run_gpu(args, rank, world, local):
     pf_flops = attention_flops(wp.B, wp.H, wp.Sq, wp.Sk, wp.D, wp.causal)
     dc_bytes = decode_bytes(wd.B, wd.H, wd.Sk, wd.D)
 
-    if parts & {"backward", "d256", "splitd", "varlen", "varlen_backward", "shapes"} and not (run_pf or run_dc):
+    if parts & {"backward", "d256", "splitd", "varlen", "varlen_backward", "shapes", "decode_two"} and not (run_pf or run_dc):
         # profiling run of the backward pass or of the large-head forwards alone
         rec = {"part": args.parts, "steps": args.steps}
         if "backward" in parts:
@@ -376,6 +376,9 @@ def run_gpu(args, rank, world, local):
             rec["varlen_backward"] = run_varlen_bwd(args, fa, torch, dev, stream, flush, world)
         if "shapes" in parts:
             rec["shapes"] = run_shapes(args, fa, torch, dev, stream, flush, world)
+        if "decode_two" in parts:
+            rec["decode_two_launch"] = run_two_launch(args, fa, torch, stream, flush, world, (dq, dk, dv), ws, do,
+                                                      dlse, wd)
         if rank == 0:
             print(json.dumps(rec), flush=True)
         return None

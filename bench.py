@@ -832,63 +832,94 @@ def run_paged(args, fa, torch, stream, dev, flush, world):
 
 def run_e2e(args, fa, torch, stream, dev, wp, wd, pre, dec, world):
     """Same metrics through the public API from pinned host buffers: every step
-    copies its inputs host->device, runs the kernels and reads the outputs back."""
+    copies its inputs host->device, runs the kernels and reads the outputs back.
+    Steps are pipelined the way a serving loop would run them: two sets of
+    device and host buffers, the host->device copies on one stream, the
+    kernel on `stream`, the device->host copies on a third, ordered by events
+    so that step i's inputs land while step i-1 computes and step i-2's
+    outputs drain. Every step's copies are inside the timed region."""
     from exact_attention_54_gb300.metrics import attention_flops, decode_bytes
     n = max(1, min(args.e2e_steps, args.steps))
-    hq, hk, hv = (t.cpu().pin_memory() for t in pre)
-    ho = torch.empty(wp.B, wp.H, wp.Sq, wp.D, dtype=wp.dtype).pin_memory()
-    hl = torch.empty(wp.B, wp.H, wp.Sq, dtype=torch.float32).pin_memory()
-    q, k, v = (torch.empty_like(t, device=dev) for t in pre)
-    o = torch.empty_like(q)
-    lse = torch.empty(wp.B, wp.H, wp.Sq, dtype=torch.float32, device=dev)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     S = wd.num_splits
-    gq, gk, gv = (t.cpu().pin_memory() for t in dec)
-    dq, dk, dv = (torch.empty_like(t, device=dev) for t in dec)
-    ws = (torch.empty(wd.B, wd.H, S, wd.D, dtype=torch.float32, device=dev),
-          torch.empty(wd.B, wd.H, S, dtype=torch.float32, device=dev),
-          torch.empty(wd.B, wd.H, S, dtype=torch.float32, device=dev))
-    counters = torch.zeros(wd.B * wd.H, dtype=torch.int32, device=dev)
-    do = torch.empty(wd.B, wd.H, 1, wd.D, dtype=wd.dtype, device=dev)
-    dlse = torch.empty(wd.B, wd.H, dtype=torch.float32, device=dev)
-    hdo = torch.empty(wd.B, wd.H, 1, wd.D, dtype=wd.dtype).pin_memory()
-    hdl = torch.empty(wd.B, wd.H, dtype=torch.float32).pin_memory()
 
-    def pre_step():
-        for d, h in ((q, hq), (k, hk), (v, hv)):
-            d.copy_(h, non_blocking=True)
-        fa.fa_fwd(q, k, v, o, lse, wp.causal, wp.scale, stream)
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
-
-    def dec_step():
-        for d, h in ((dq, gq), (dk, gk), (dv, gv)):
-            d.copy_(h, non_blocking=True)
-        fa.fa_decode_splitkv_fused(dq, dk, dv, do, dlse, *ws, counters, S, wd.scale, stream)
-        hdo.copy_(do, non_blocking=True)
-        hdl.copy_(dlse, non_blocking=True)
+    def buffers(kind):
+        if kind == "prefill":
+            host_in = [t.cpu().pin_memory() for t in pre]
+            sets = []
+            for _ in range(2):
+                q, k, v = (torch.empty_like(t, device=dev) for t in pre)
+                sets.append({"in": (q, k, v), "o": torch.empty_like(q),
+                             "lse": torch.empty(wp.B, wp.H, wp.Sq, dtype=torch.float32, device=dev),
+                             "ho": torch.empty(wp.B, wp.H, wp.Sq, wp.D, dtype=wp.dtype).pin_memory(),
+                             "hl": torch.empty(wp.B, wp.H, wp.Sq, dtype=torch.float32).pin_memory()})
+            return host_in, sets
+        host_in = [t.cpu().pin_memory() for t in dec]
+        sets = []
+        for _ in range(2):
+            q, k, v = (torch.empty_like(t, device=dev) for t in dec)
+            sets.append({"in": (q, k, v),
+                         "ws": (torch.empty(wd.B, wd.H, S, wd.D, dtype=torch.float32, device=dev),
+                                torch.empty(wd.B, wd.H, S, dtype=torch.float32, device=dev),
+                                torch.empty(wd.B, wd.H, S, dtype=torch.float32, device=dev)),
+                         "counters": torch.zeros(wd.B * wd.H, dtype=torch.int32, device=dev),
+                         "o": torch.empty(wd.B, wd.H, 1, wd.D, dtype=wd.dtype, device=dev),
+                         "lse": torch.empty(wd.B, wd.H, dtype=torch.float32, device=dev),
+                         "ho": torch.empty(wd.B, wd.H, 1, wd.D, dtype=wd.dtype).pin_memory(),
+                         "hl": torch.empty(wd.B, wd.H, dtype=torch.float32).pin_memory()})
+        return host_in, sets
 
     out = {}
-    for name, fn in (("prefill", pre_step), ("decode", dec_step)):
-        for _ in range(2):
-            fn()
+    for name in ("prefill", "decode"):
+        host_in, sets = buffers(name)
+        ev = [{k: torch.cuda.Event() for k in ("in", "run", "out")} for _ in range(2)]
+        started = [False, False]
+
+        def step(i):
+            b, e = sets[i % 2], ev[i % 2]
+            with torch.cuda.stream(s_in):
+                if started[i % 2]:
+                    s_in.wait_event(e["run"])  # the previous kernel on this set has read its inputs
+                for d, h in zip(b["in"], host_in):
+                    d.copy_(h, non_blocking=True)
+                e["in"].record(s_in)
+            stream.wait_event(e["in"])
+            if started[i % 2]:
+                stream.wait_event(e["out"])  # the previous read-back of this set's outputs is done
+            q, k, v = b["in"]
+            if name == "prefill":
+                fa.fa_fwd(q, k, v, b["o"], b["lse"], wp.causal, wp.scale, stream)
+            else:
+                fa.fa_decode_splitkv_fused(q, k, v, b["o"], b["lse"], *b["ws"], b["counters"], S, wd.scale, stream)
+            e["run"].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(e["run"])
+                b["ho"].copy_(b["o"], non_blocking=True)
+                b["hl"].copy_(b["lse"], non_blocking=True)
+                e["out"].record(s_out)
+            started[i % 2] = True
+
+        for i in range(2):
+            step(i)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for _ in range(n):
-            fn()
+        for i in range(n):
+            step(i)
         torch.cuda.synchronize()
         dt = aggregate_max([time.perf_counter() - t0], world)[0]
+        fa.fa_check_device_error()
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sets[0]["ho"].numel() * sets[0]["ho"].element_size() + sets[0]["hl"].numel() * sets[0]["hl"].element_size()
         if name == "prefill":
             val = world * attention_flops(wp.B, wp.H, wp.Sq, wp.Sk, wp.D, wp.causal) * n / dt / 1e12
-            h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-            d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
-            out[name] = {"value": val, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                         "steps": n, "ms_per_step": 1e3 * dt / n}
+            unit = "TFLOPS"
         else:
             val = world * decode_bytes(wd.B, wd.H, wd.Sk, wd.D) * n / dt / 1e9
-            h2d = sum(t.numel() * t.element_size() for t in (gq, gk, gv))
-            d2h = hdo.numel() * hdo.element_size() + hdl.numel() * hdl.element_size()
-            out[name] = {"value": val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                         "steps": n, "ms_per_step": 1e3 * dt / n}
+            unit = "GB/s"
+        out[name] = {"value": val, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                     "steps": n, "ms_per_step": 1e3 * dt / n, "copy_gbs": (h2d + d2h) * n / dt / 1e9,
+                     "pipelined": "inputs of step i land while step i-1 computes; outputs drain on a third stream"}
+        del sets, host_in
     return out
 
 

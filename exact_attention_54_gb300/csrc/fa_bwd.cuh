@@ -598,6 +598,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const size_t row_g = (VARLEN ? (static_cast<size_t>(u.tk0) + key) * p.H + u.hh
                                          : static_cast<size_t>(u.z) * p.Sk + key) * D + h * (D / 2);
             const uint64_t once = ptx::l2_policy_evict_first();
+            // 32-byte stores when both outputs are 32-byte aligned
+            const bool v8 = ((reinterpret_cast<uintptr_t>(p.dk) | reinterpret_cast<uintptr_t>(p.dv)) & 31) == 0;
 #pragma unroll 1
             for (int t = 0; t < 2; ++t) {
                 const float f = t == 0 ? 1.f : p.scale;
@@ -621,10 +623,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (row_valid) {
                         // written once: evict first
                         uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
+                        if (v8) {
+                            ptx::st_global_v8_hint(d4, pk, once);
+                            ptx::st_global_v8_hint(d4 + 2, pk + 8, once);
+                        } else {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            ptx::st_global_v4_hint(d4 + k, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3],
-                                                   once);
+                            for (int k = 0; k < 4; ++k)
+                                ptx::st_global_v4_hint(d4 + k, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2],
+                                                       pk[4 * k + 3], once);
+                        }
                     }
                 }
             }
@@ -1036,33 +1043,46 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             const size_t row_g = (VARLEN ? (static_cast<size_t>(u.tk0) + key) * p.H + u.hh
                                          : static_cast<size_t>(u.z) * p.Sk + key) * D + h * (D / 2);
             const uint64_t once = ptx::l2_policy_evict_first();
+            // one TMEM wait per tensor; 32-byte stores when both outputs are
+            // 32-byte aligned (every row then is: a row is D * 2 bytes)
+            const bool v8 = ((reinterpret_cast<uintptr_t>(p.dk) | reinterpret_cast<uintptr_t>(p.dv)) & 31) == 0;
 #pragma unroll 1
             for (int t = 0; t < 2; ++t) {
                 const float f = t == 0 ? 1.f : p.scale;
                 uint16_t *dst = static_cast<uint16_t *>(t == 0 ? p.dv : p.dk) + row_g;
-#pragma unroll 1
-                for (int c = 0; c < D / 64; ++c) {
-                    uint32_t w[32];
-                    if (n > 0) {
-                        ptx::tmem_ld32(tmem + lane_base + (t == 0 ? S::kTmemDV : S::kTmemDK) + h * (D / 2) + 32 * c,
-                                       w);
-                        ptx::tmem_ld_wait();
-                        ptx::reg_fence(w);
-                    } else {
+                uint32_t w[D / 64][32];
+                if (n > 0) {
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) w[k] = 0u;
-                    }
+                    for (int c = 0; c < D / 64; ++c)
+                        ptx::tmem_ld32(tmem + lane_base + (t == 0 ? S::kTmemDV : S::kTmemDK) + h * (D / 2) + 32 * c,
+                                       w[c]);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) ptx::reg_fence(w[c]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) w[c][k] = 0u;
+                }
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
-                        pk[k] = ptx::pack2<BF16>(__uint_as_float(w[2 * k]) * f, __uint_as_float(w[2 * k + 1]) * f);
+                        pk[k] = ptx::pack2<BF16>(__uint_as_float(w[c][2 * k]) * f, __uint_as_float(w[c][2 * k + 1]) * f);
                     if (row_valid) {
                         // written once: evict first
                         uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
+                        if (v8) {
+                            ptx::st_global_v8_hint(d4, pk, once);
+                            ptx::st_global_v8_hint(d4 + 2, pk + 8, once);
+                        } else {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            ptx::st_global_v4_hint(d4 + k, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3],
-                                                   once);
+                            for (int k = 0; k < 4; ++k)
+                                ptx::st_global_v4_hint(d4 + k, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2],
+                                                       pk[4 * k + 3], once);
+                        }
                     }
                 }
             }

@@ -78,6 +78,36 @@ def test_unreachable_keys_get_exact_zero_and_dk_dv_repeat_bitwise():
     assert_grad_close(dk1[:, :, :200], rk[:, :, :200], "dk")
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_dk_dv_aligned_to_16_bytes_only(D):
+    """dK and dV may start 16 bytes past a 32-byte boundary (the entry point
+    asks for 16-byte alignment); their rows are then written with 16-byte
+    stores. The values must equal, bit for bit, those written into aligned
+    buffers, and nothing outside the views may change."""
+    B, H, S = 1, 2, 300
+    q, k, v = inputs.make_dense(B, H, S, S, D, torch.bfloat16, seed=63 + D)
+    do = inputs.make_dense(B, H, S, S, D, torch.bfloat16, seed=64 + D)[0]
+    qd, kd, vd, dod = dev(q, k, v, do)
+    o, lse = fa.flash_attention(qd, kd, vd, causal=True, scale=0.1)
+    dq_al, dk_al, dv_al = fa.flash_attention_bwd(qd, kd, vd, o, lse, dod, causal=True, scale=0.1)
+    n = B * H * S * D
+    bufs = [torch.full((n + 64,), 1.5, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    dk, dv = (b[8: 8 + n].view(B, H, S, D) for b in bufs)
+    assert dk.data_ptr() % 32 == 16 and dv.data_ptr() % 32 == 16
+    dq = torch.empty_like(qd)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, S, D) // 4, dtype=torch.float32, device="cuda")
+    fa.fa_bwd(qd, kd, vd, o, dod, lse, dq, dk, dv, ws, True, 0.1)
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    for b in bufs:
+        assert torch.all(b[:8] == 1.5) and torch.all(b[8 + n:] == 1.5)
+    assert torch.equal(dk.view(torch.int16), dk_al.view(torch.int16))
+    assert torch.equal(dv.view(torch.int16), dv_al.view(torch.int16))
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, True, 0.1)
+    assert_grad_close(dk.cpu(), rk, "dk at a 16-byte offset")
+    assert_grad_close(dv.cpu(), rv, "dv at a 16-byte offset")
+
+
 def test_bwd_llama_prefill_full_size_two_heads():
     """The LLaMA-7B prefill shape (1,32,4096,4096,128, causal, bf16) through
     the full kernel; two heads compared against the oracle (about a minute of

@@ -279,6 +279,13 @@ __device__ __forceinline__ void load_rows_packed(const BwdParams &p, const BwdUn
     if (leader) ptx::bar_arrive(bar);
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -1039,17 +1046,17 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
         // The TMEM loads are warp-collective (.sync.aligned): every lane runs
         // them; only the global stores are limited to keys that exist.
         if (ok) {
-            const bool row_valid = key < u.Lk;
-            const size_t row_g = (VARLEN ? (static_cast<size_t>(u.tk0) + key) * p.H + u.hh
-                                         : static_cast<size_t>(u.z) * p.Sk + key) * D + h * (D / 2);
             const uint64_t once = ptx::l2_policy_evict_first();
-            // one TMEM wait per tensor; 32-byte stores when both outputs are
-            // 32-byte aligned (every row then is: a row is D * 2 bytes)
-            const bool v8 = ((reinterpret_cast<uintptr_t>(p.dk) | reinterpret_cast<uintptr_t>(p.dv)) & 31) == 0;
+            // dV, then scale * dK. Each warp stages its 32 key rows (64 head
+            // columns, 128 bytes a row) in its own 4 KB of the dS^T buffers,
+            // free once the last products are done, and writes them back four
+            // whole rows (full 128-byte lines) per store instruction instead
+            // of pieces of 32 rows, which took the LSU ~8x the transactions.
+            const uint32_t stage = sbase + S::kOffDS + static_cast<uint32_t>(warp - 4) * 4096u;
+            const uint32_t my_row = stage + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll 1
             for (int t = 0; t < 2; ++t) {
                 const float f = t == 0 ? 1.f : p.scale;
-                uint16_t *dst = static_cast<uint16_t *>(t == 0 ? p.dv : p.dk) + row_g;
                 uint32_t w[D / 64][32];
                 if (n > 0) {
 #pragma unroll
@@ -1065,26 +1072,34 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
 #pragma unroll
                         for (int k = 0; k < 32; ++k) w[c][k] = 0u;
                 }
+                // row `lane` of the block: 16-byte chunk q at (q ^ (row & 7)) * 16
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
                         pk[k] = ptx::pack2<BF16>(__uint_as_float(w[c][2 * k]) * f, __uint_as_float(w[c][2 * k + 1]) * f);
-                    if (row_valid) {
-                        // written once: evict first
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
-                        if (v8) {
-                            ptx::st_global_v8_hint(d4, pk, once);
-                            ptx::st_global_v8_hint(d4 + 2, pk + 8, once);
-                        } else {
 #pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                ptx::st_global_v4_hint(d4 + k, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2],
-                                                       pk[4 * k + 3], once);
-                        }
+                    for (int m = 0; m < 4; ++m)
+                        st_shared_v4(my_row + static_cast<uint32_t>(((4 * c + m) ^ (lane & 7)) * 16), pk[4 * m],
+                                     pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]);
+                }
+                __syncwarp();
+                uint16_t *out = static_cast<uint16_t *>(t == 0 ? p.dv : p.dk);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int rr = 4 * k + (lane >> 3), q = lane & 7;  // row of the block, 16-byte chunk
+                    const uint4 val = ld_shared_v4(stage + static_cast<uint32_t>(rr * 128 + ((q ^ (rr & 7)) * 16)));
+                    const int key_r = k0 + wq * 32 + rr;
+                    if (key_r < u.Lk) {
+                        // written once: evict first
+                        const size_t row_g = (VARLEN ? (static_cast<size_t>(u.tk0) + key_r) * p.H + u.hh
+                                                     : static_cast<size_t>(u.z) * p.Sk + key_r) * D + h * (D / 2);
+                        ptx::st_global_v4_hint(reinterpret_cast<uint4 *>(out + row_g) + q, val.x, val.y, val.z,
+                                               val.w, once);
                     }
                 }
+                __syncwarp();  // the block is rewritten for the next tensor
             }
         }
     } else if (warp >= 12 && n > 0) {
@@ -1130,7 +1145,6 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             if (leader) {
                 const int q0 = qs0 + j * S::kQ;
                 const uint32_t tile = sbase + S::kOffQ + st * S::kStageBytes;
-#pragma unroll
                 int y, z;
                 unit_coords<VARLEN>(u, false, q0, y, z);
                 for (int c = 0; c < D / 32; ++c)

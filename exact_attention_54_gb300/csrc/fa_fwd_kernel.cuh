@@ -543,44 +543,37 @@ __device__ void fwd_softmax(const FwdParams &p, uint32_t sbase, uint32_t tmem, i
             ok = ptx::bar_wait(bar(S::kSFull + t), cnt & 1, abort_flag, p.timeout_ns);
             if (!__all_sync(kFull, ok)) { ok = false; break; }
             ptx::tc_fence_after();
-            // S row in two halves: the second TMEM load overlaps the first half's max.
-            uint32_t s[4][32];
-            ptx::tmem_ld32(tS, s[0]);
-            ptx::tmem_ld32(tS + 32, s[1]);
-            ptx::tmem_ld_wait();
-            ptx::reg_fence(s[0]);
-            ptx::reg_fence(s[1]);
-            ptx::tmem_ld32(tS + 64, s[2]);
-            ptx::tmem_ld32(tS + 96, s[3]);
-
             // The keys of this tile that the row sees are the columns c < lim:
             // the sequence ends at Lk and, causal, the row sees keys up to its
             // own position. Tiles inside both limits (need_mask false, the
             // same for the whole warpgroup) are not tested.
             const int k0 = j * kBlockN;
             const bool need_mask = (k0 + kBlockN > wk.Lk) || (CAUSAL && k0 + kBlockN - 1 > wk.q_start[t]);
-            int lim = wk.Lk - k0;
-            if (CAUSAL) lim = min(lim, q_row + 1 - k0);
-            auto mask_half = [&](int h) {
+            // The row maximum comes with the loads (one wait for all four).
+            uint32_t s[4][32];
+            float mx4[4];
 #pragma unroll
-                for (int c = 64 * h; c < 64 * h + 64; ++c)
+            for (int c = 0; c < 4; ++c) ptx::tmem_ld32_max(tS + 32 * c, s[c], mx4[c]);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                ptx::reg_fence(s[c]);
+                asm volatile("" : "+f"(mx4[c]));
+            }
+            if (need_mask) {
+                // masked tile: the maximum is taken again after the mask
+                int lim = wk.Lk - k0;
+                if (CAUSAL) lim = min(lim, q_row + 1 - k0);
+#pragma unroll
+                for (int c = 0; c < kBlockN; ++c)
                     if (c >= lim) s[c / 32][c % 32] = 0xff800000u;  // -inf
-            };
-            // row maximum of the raw scores: four chains of three-input max
-            float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
-            auto max_half = [&](int h) {
 #pragma unroll
-                for (int c = 64 * h; c < 64 * h + 64; c += 2)
+                for (int c = 0; c < 4; ++c) mx4[c] = -CUDART_INF_F;
+#pragma unroll
+                for (int c = 0; c < kBlockN; c += 2)
                     mx4[(c / 2) % 4] = ptx::fmax3(mx4[(c / 2) % 4], __uint_as_float(s[c / 32][c % 32]),
                                                   __uint_as_float(s[(c + 1) / 32][(c + 1) % 32]));
-            };
-            if (need_mask) mask_half(0);
-            max_half(0);
-            ptx::tmem_ld_wait();
-            ptx::reg_fence(s[2]);
-            ptx::reg_fence(s[3]);
-            if (need_mask) mask_half(1);
-            max_half(1);
+            }
             const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
             const float m_cand = mx * scale_log2;
             const bool need = m_cand > m_used + kRescaleThreshold;

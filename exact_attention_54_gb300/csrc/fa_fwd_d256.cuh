@@ -410,15 +410,20 @@ __device__ void softmax_role(const FwdParams &p, uint32_t sbase, uint32_t tmem, 
             if (!(ok = wait(S::kSFull + b, (g >> 1) & 1))) break;
             ptx::tc_fence_after();
             const uint32_t tS = tmem + lane_base + S::kTmemS + b * kBlockN;
+            // the row maximum comes with the loads (tcgen05.ld.red); a masked
+            // tile takes it again after the mask
             uint32_t s[2][32];
-            ptx::tmem_ld32(tS, s[0]);
-            ptx::tmem_ld32(tS + 32, s[1]);
+            float mr[2];
+            ptx::tmem_ld32_max(tS, s[0], mr[0]);
+            ptx::tmem_ld32_max(tS + 32, s[1], mr[1]);
             ptx::tmem_ld_wait();
             ptx::reg_fence(s[0]);
             ptx::reg_fence(s[1]);
+            asm volatile("" : "+f"(mr[0]), "+f"(mr[1]));
 
             const int k0 = i * kBlockN;
             const bool need_mask = (k0 + kBlockN > wk.Lk) || (CAUSAL && k0 + kBlockN - 1 > wk.q_start);
+            float mx = fmaxf(mr[0], mr[1]);
             if (need_mask) {
                 // the row sees columns c < lim: the sequence's end and, causal, its own position
                 int lim = wk.Lk - k0;
@@ -426,13 +431,13 @@ __device__ void softmax_role(const FwdParams &p, uint32_t sbase, uint32_t tmem, 
 #pragma unroll
                 for (int c = 0; c < kBlockN; ++c)
                     if (c >= lim) s[c / 32][c % 32] = 0xff800000u;  // -inf
-            }
-            float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+                float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-            for (int c = 0; c < kBlockN; c += 2)
-                mx4[(c / 2) % 4] = ptx::fmax3(mx4[(c / 2) % 4], __uint_as_float(s[c / 32][c % 32]),
-                                              __uint_as_float(s[(c + 1) / 32][(c + 1) % 32]));
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                for (int c = 0; c < kBlockN; c += 2)
+                    mx4[(c / 2) % 4] = ptx::fmax3(mx4[(c / 2) % 4], __uint_as_float(s[c / 32][c % 32]),
+                                                  __uint_as_float(s[(c + 1) / 32][(c + 1) % 32]));
+                mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            }
             const float m_cand = mx * scale_log2;
             const bool need = m_cand > m_used + kRescaleThreshold;
             float alpha = 1.f;

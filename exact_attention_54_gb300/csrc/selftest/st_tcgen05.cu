@@ -9,6 +9,9 @@
 //                        like any 128-row tile and read by the MMA as an
 //                        MN-major A operand (the backward pass's dQ = dS K
 //                        reads dS^T this way), Y as an MN-major B operand
+//   fa_selftest_ldmax    x[128x32] fp32 written to TMEM and read back with the
+//                        reducing load (tcgen05.ld.red max): the values and
+//                        each row's maximum, as the forward's softmax uses it
 //   fa_selftest_watchdog a bounded wait on a barrier nobody arrives at; the
 //                        kernel must give up, release TMEM and report it
 // Each kernel writes 0 (done) or 1 (a wait timed out) to *status.
@@ -252,6 +255,37 @@ __global__ void __launch_bounds__(128, 1)
     if (threadIdx.x == 0) *status = *abort_flag ? 1 : 0;
 }
 
+// Writes x[128][32] into 32 TMEM columns (row r in lane r) and reads it back
+// with tmem_ld32_max: y gets the values, mx each row's maximum.
+__global__ void __launch_bounds__(128, 1) st_ldmax_kernel(const float *x, float *y, float *mx) {
+    __shared__ uint32_t slot;
+    const int warp = threadIdx.x / 32;
+    if (warp == 0) {
+        ptx::tmem_alloc(ptx::smem_addr(&slot), 32);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t taddr = slot + (static_cast<uint32_t>(warp * 32) << 16);
+    uint32_t w[32];
+    for (int c = 0; c < 32; ++c) w[c] = __float_as_uint(x[threadIdx.x * 32 + c]);
+    ptx::tmem_st32(taddr, w);
+    ptx::tmem_st_wait();
+    float m;
+    ptx::tmem_ld32_max(taddr, w, m);
+    ptx::tmem_ld_wait();
+    ptx::reg_fence(w);
+    for (int c = 0; c < 32; ++c) y[threadIdx.x * 32 + c] = __uint_as_float(w[c]);
+    mx[threadIdx.x] = m;
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(slot, 32);
+    }
+}
+
 // Waits on a barrier that never completes, while holding TMEM, and must come
 // back on its own after timeout_ns with the TMEM released.
 __global__ void __launch_bounds__(128, 1) st_watchdog_kernel(int *status, unsigned long long timeout_ns) {
@@ -385,6 +419,12 @@ __attribute__((visibility("default"))) int fa_selftest_tn(const void *x, const v
 __attribute__((visibility("default"))) int fa_selftest_watchdog(int *status, unsigned long long timeout_ns,
                                                                 void *stream) {
     st_watchdog_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(status, timeout_ns);
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+__attribute__((visibility("default"))) int fa_selftest_ldmax(const float *x, float *y, float *mx, void *stream) {
+    if (!x || !y || !mx) return -1;
+    st_ldmax_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(x, y, mx);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

@@ -21,6 +21,7 @@ def st():
     lib.fa_selftest_pv.argtypes = [vp, vp, vp, i, i, vp, u64, vp]
     lib.fa_selftest_tn.argtypes = [vp, vp, vp, i, i, vp, u64, vp]
     lib.fa_selftest_watchdog.argtypes = [vp, u64, vp]
+    lib.fa_selftest_ldmax.argtypes = [vp, vp, vp, vp]
     return lib
 
 
@@ -93,6 +94,25 @@ def test_transposed_a_mma(st, D, dtype):
     err = float((c - ref).abs().max())
     hyps = {"X^T Y": ref, "X Y": x.float() @ y.float()}
     assert err < 1e-3, {k: float((c - v).abs().max()) for k, v in hyps.items()}
+
+
+def test_reducing_tmem_load_returns_values_and_row_max(st):
+    """The forward's softmax takes each row's maximum from the TMEM loads
+    (tcgen05.ld.red max): values must come back unchanged and the maximum
+    must be exact, including very large and very negative entries."""
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn(128, 32, generator=g) * 30
+    x[5, 7] = 1e30
+    x[9, :] = -torch.arange(32, dtype=torch.float32) - 1e20
+    x[17, :] = float("-inf")
+    x[17, 31] = -2.5
+    xd = x.cuda()
+    y = torch.full_like(xd, float("nan"))
+    mx = torch.full((128,), float("nan"), device="cuda")
+    assert st.fa_selftest_ldmax(xd.data_ptr(), y.data_ptr(), mx.data_ptr(), _stream()) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(y.cpu(), x)
+    assert torch.equal(mx.cpu(), x.max(dim=1).values)
 
 
 def test_watchdog_gives_up_and_gpu_stays_usable(st):

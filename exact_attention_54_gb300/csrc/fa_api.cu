@@ -416,7 +416,8 @@ size_t fa_bwd_workspace_bytes(int B, int H, int Sq, int D) {
     const long long BH = static_cast<long long>(B) * H;
     if (BH > INT_MAX) return 0;
     const long long pad = (static_cast<long long>(Sq) + 127) / 128 * 128;
-    return static_cast<size_t>(BH * Sq * D + 2 * BH * pad) * sizeof(float);
+    // + 16 bytes: the main kernel's work counter
+    return static_cast<size_t>(BH * Sq * D + 2 * BH * pad) * sizeof(float) + 16;
 }
 
 fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse,
@@ -461,6 +462,10 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
     p.dq_acc = workspace;
     p.lse2 = workspace + static_cast<size_t>(BH) * Sq * D;
     p.delta = p.lse2 + static_cast<size_t>(BH) * p.Sq_pad;
+    p.work_counter = reinterpret_cast<int *>(p.delta + static_cast<size_t>(BH) * p.Sq_pad);
+    p.total_units = static_cast<int>(BH * n_kt);
+    p.grid = num_sms();
+    if (p.grid <= 0) return FA_ERR_CUDA;
     p.dk = dk;
     p.dv = dv;
     p.scale = scale;
@@ -477,7 +482,7 @@ size_t fa_bwd_varlen_workspace_bytes(int total_q, int H, int D) {
     if (total_q < 1 || H < 1 || total_q > kMaxLen || (D != 64 && D != 128)) return 0;
     const long long TH = static_cast<long long>(total_q) * H;
     if (TH > INT_MAX) return 0;
-    return static_cast<size_t>(TH * D + 2 * TH) * sizeof(float);
+    return static_cast<size_t>(TH * D + 2 * TH) * sizeof(float) + 16;  // + the work counter
 }
 
 fa_status_t fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const void *dout,
@@ -536,6 +541,10 @@ fa_status_t fa_bwd_varlen(const void *q, const void *k, const void *v, const voi
     p.dq_acc = workspace;
     p.lse2 = workspace + static_cast<size_t>(total_q) * H * D;
     p.delta = p.lse2 + static_cast<size_t>(total_q) * H;
+    p.work_counter = reinterpret_cast<int *>(p.delta + static_cast<size_t>(total_q) * H);
+    p.total_units = p.BH * p.n_ktiles;
+    p.grid = num_sms();
+    if (p.grid <= 0) return FA_ERR_CUDA;
     p.dk = dk;
     p.dv = dv;
     p.scale = scale;

@@ -125,6 +125,8 @@ __global__ void __launch_bounds__(256)
                        const float *__restrict__ lse, const BwdParams p) {
     constexpr int E = D / 32;  // elements per lane
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    // the main kernel's work counter starts every call at zero
+    if (blockIdx.x == 0 && threadIdx.x == 0 && p.work_counter != nullptr) *p.work_counter = 0;
     const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;
     size_t srow, off, lrow;
     if constexpr (VARLEN) {
@@ -197,14 +199,19 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float *__restrict_
 // Every CTA of a head re-reads its Q and dO and adds into its dQ accumulator,
 // so running a few heads at once keeps that set (8 Sq D bytes per head)
 // within L2 instead of streaming every head's through it at once.
-__device__ __forceinline__ void bwd_work(const BwdParams &p, int &kt, int &bh) {
+__device__ __forceinline__ void bwd_work_at(const BwdParams &p, int w, int &kt, int &bh) {
     const int per_group = p.heads_per_group * p.n_ktiles;
-    const int g = static_cast<int>(blockIdx.x) / per_group;
-    const int i = static_cast<int>(blockIdx.x) % per_group;
+    const int g = w / per_group;
+    const int i = w % per_group;
     const int rest = p.BH - g * p.heads_per_group;
     const int g_heads = rest < p.heads_per_group ? rest : p.heads_per_group;
     kt = i / g_heads;
     bh = g * p.heads_per_group + i % g_heads;
+}
+
+// The unit of this CTA (one unit per CTA, in block order).
+__device__ __forceinline__ void bwd_work(const BwdParams &p, int &kt, int &bh) {
+    bwd_work_at(p, static_cast<int>(blockIdx.x), kt, bh);
 }
 
 // This CTA's key tile and what it needs of its unit: the unit's index (dense
@@ -221,10 +228,10 @@ struct BwdUnit {
 };
 
 template <bool VARLEN>
-__device__ __forceinline__ BwdUnit bwd_unit(const BwdParams &p) {
+__device__ __forceinline__ BwdUnit bwd_unit_at(const BwdParams &p, int w) {
     BwdUnit u;
     int unit;
-    bwd_work(p, u.kt, unit);
+    bwd_work_at(p, w, u.kt, unit);
     if constexpr (VARLEN) {
         const int b = unit / p.H;
         u.z = 0;
@@ -245,6 +252,11 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams &p) {
         u.ok = true;
     }
     return u;
+}
+
+template <bool VARLEN>
+__device__ __forceinline__ BwdUnit bwd_unit(const BwdParams &p) {
+    return bwd_unit_at<VARLEN>(p, static_cast<int>(blockIdx.x));
 }
 
 // Tensor-map coordinates (y, z) of row `row` of the unit's queries or keys:
@@ -740,10 +752,18 @@ struct ShapeQ64 {
     static constexpr int kTeardown = 27;
     static constexpr int kPTFree = 28;     // +b: dV of the buffer done, its S^T columns free (MMA commit)
     static constexpr int kLFull = 30;      // +b: the sub-step's LSE and D values landed (bulk copy)
-    static constexpr int kNumBars = 32;
+    static constexpr int kKVEmpty = 32;    // the unit's last products done: K and V may be replaced (MMA commit)
+    static constexpr int kRing = 4;        // unit slots
+    static constexpr int kUnitReady = 33;  // +slot: a unit published (warp 0)
+    static constexpr int kUnitFree = 37;   // +slot: every role has read it (15 warps)
+    // a unit's dK/dV written out of every key-row warp's staging block (8 warps)
+    static constexpr int kStagingFree = 41;
+    static constexpr int kNumBars = 42;
     static constexpr int kOffMisc = kNumBars * 8;
     static constexpr int kOffRows = 384;   // + b * 512: float lse2[64], delta[64]
-    static constexpr int kSmallBytes = kOffRows + 2 * 2 * kQ * 4;
+    // + slot * 32: int {live, kt, z, hh, tq0, tk0, Lq, Lk} of a published unit
+    static constexpr int kOffUnits = kOffRows + 2 * 2 * kQ * 4;
+    static constexpr int kSmallBytes = kOffUnits + kRing * 32;
     static_assert(kOffMisc + 16 <= kOffRows, "small region layout");
     static constexpr int kSmemBytes = kSmallBytes + 1024 + kTilesBytes;
     static constexpr uint32_t kTmemDV = 0;
@@ -773,31 +793,23 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
         return __all_sync(0xffffffffu, ptx::bar_wait(bar(i), parity, abort_flag, p.timeout_ns));
     };
 
-    // work item: key tile kt of a head (dense) or of a sequence's head (packed),
-    // heavy causal tiles first; sub-steps of 64 queries from the first query
-    // that sees any of these keys
-    const BwdUnit u = bwd_unit<VARLEN>(p);
-    if constexpr (VARLEN) {
-        // packed: offsets outside the tensors are reported and skipped; a
-        // key tile past the sequence's keys has nothing to compute or write
-        if (!u.ok) {
-            if (threadIdx.x == 0) atomicExch(p.err, kDeviceErrSeqLens);
-            return;
-        }
-        if (u.kt * kBlock >= u.Lk) return;
-    }
-    const int kt = u.kt;
-    const int k0 = kt * kBlock;
-    const int qs0 = CAUSAL ? k0 : 0;
-    const int n = u.Lq > qs0 ? (u.Lq - qs0 + S::kQ - 1) / S::kQ : 0;
-
+    // Persistent: each CTA takes work units (key tile kt of a head, dense, or
+    // of a sequence's head, packed; heavy causal tiles first) from a counter
+    // until none is left. Warp 0 fetches a unit and publishes it in a ring of
+    // unit slots that every role reads in turn; ring stages and buffers keep
+    // their phases across units through one running sub-step count J, and
+    // the next unit's K and V are loaded while the current unit's dK and dV
+    // are written out. tests/test_bwd_barrier_protocol.py models this
+    // protocol.
     if (threadIdx.x == 0) {
         for (int i = 0; i < S::kNumBars; ++i) {
-            uint32_t count = 1;  // MMA commits, TMA, the reduction thread
+            uint32_t count = 1;  // MMA commits, TMA, the reduction thread, warp 0
             if (i >= S::kPFull && i < S::kPFull + 2) count = 2 * kBlock / 32;  // the key-row warps
             if ((i >= S::kBufFree && i < S::kBufFree + 2) || (i >= S::kStageReady && i < S::kStageReady + S::kStages))
                 count = kBlock / 32;  // dQ warps
             if (i == S::kTeardown) count = 2;  // one commit per MMA-issuing warp
+            if (i >= S::kUnitFree && i < S::kUnitFree + S::kRing) count = kThreadsQ64 / 32 - 1;  // every warp but 0
+            if (i == S::kStagingFree) count = 2 * kBlock / 32;  // the key-row warps
             ptx::bar_init(bar(i), count);
         }
         *abort_flag = 0;
@@ -819,58 +831,135 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0 && n > 0) {
-        // ---- TMA producer ----
+    // A published unit as every role sees it; n: its 64-query sub-steps from
+    // the first query that sees any of its keys.
+    struct UnitView {
+        bool live;  // false: no unit is left
+        BwdUnit u;
+        int k0, qs0, n;
+    };
+    // Unit slot i of this CTA: waits until warp 0 has published it, copies it
+    // and releases the slot. False when the wait gave up.
+    auto read_unit = [&](int i, UnitView &uv) -> bool {
+        const int s = i % S::kRing;
+        if (!wait(S::kUnitReady + s, (i / S::kRing) & 1)) return false;
+        const volatile int *e = reinterpret_cast<const volatile int *>(smem_raw + S::kOffUnits + s * 32);
+        uv.live = e[0] != 0;
+        uv.u.kt = e[1];
+        uv.u.z = e[2];
+        uv.u.hh = e[3];
+        uv.u.tq0 = e[4];
+        uv.u.tk0 = e[5];
+        uv.u.Lq = e[6];
+        uv.u.Lk = e[7];
+        uv.u.ok = true;
+        uv.k0 = uv.u.kt * kBlock;
+        uv.qs0 = CAUSAL ? uv.k0 : 0;
+        uv.n = uv.u.Lq > uv.qs0 ? (uv.u.Lq - uv.qs0 + S::kQ - 1) / S::kQ : 0;
+        __syncwarp();
+        if (lane == 0) ptx::bar_arrive(bar(S::kUnitFree + s));
+        return true;
+    };
+
+    if (warp == 0) {
+        // ---- unit fetch and TMA producer ----
         const bool leader = ptx::elect_one();
-        if (leader) {
-            // K and V are read by this CTA only: evict them first, keep L2 for
-            // the Q, dO and dQ accumulator rows the head's other CTAs reuse
-            const uint64_t once = ptx::l2_policy_evict_first();
-            ptx::bar_arrive_expect_tx(bar(S::kKVFull), 2 * S::kKTileBytes);
-            int ky, kz;
-            unit_coords<VARLEN>(u, true, k0, ky, kz);
-            for (int c = 0; c < 2; ++c) {
-                ptx::tma_load_3d_hint(sbase + S::kOffK + c * S::kKBoxBytes, &tm_k, bar(S::kKVFull), c * 64, ky, kz,
-                                      once);
-                ptx::tma_load_3d_hint(sbase + S::kOffV + c * S::kKBoxBytes, &tm_v, bar(S::kKVFull), c * 64, ky, kz,
-                                      once);
-            }
-        }
+        // K and V are read by this CTA only: evict them first, keep L2 for
+        // the Q, dO and dQ accumulator rows the head's other CTAs reuse
+        const uint64_t once = ptx::l2_policy_evict_first();
+        int J = 0, wi = 0;   // sub-steps and units with work so far
         int nq = 0, nl = 0;  // Q/dO and row-value loads issued
-        for (int j = 0; j < n; ++j) {
-            const int st = j % S::kStages, b = j & 1;
-            // the stage held sub-step j-4's staged dQ_t until its reductions read it
-            if (j >= S::kStages && !wait(S::kStageFree + st, ((j / S::kStages) - 1) & 1)) break;
-            const int q0 = qs0 + j * S::kQ;
-            if (leader && !withheld(p.withhold, static_cast<uint32_t>(j))) {
-                const uint32_t qb = sbase + S::kOffQ + st * S::kStageBytes;
-                ptx::bar_arrive_expect_tx(bar(S::kQFull + st), S::kStageBytes);
-                int qy, qz;
-                unit_coords<VARLEN>(u, false, q0, qy, qz);
+        bool ok = true;
+        for (int i = 0; ok; ++i) {
+            const int s = i % S::kRing;
+            // slot s held unit i - kRing until every role had read it
+            if (i >= S::kRing && !(ok = wait(S::kUnitFree + s, ((i / S::kRing) - 1) & 1))) break;
+            // the next unit with keys to handle; offsets outside the tensors
+            // (packed) are reported and skipped
+            BwdUnit u{};
+            int w;
+            for (;;) {
+                int got = 0;
+                if (lane == 0) got = atomicAdd(p.work_counter, 1);
+                w = __shfl_sync(0xffffffffu, got, 0);
+                if (w >= p.total_units) break;
+                u = bwd_unit_at<VARLEN>(p, w);
+                if constexpr (VARLEN) {
+                    if (!u.ok) {
+                        if (lane == 0) atomicExch(p.err, kDeviceErrSeqLens);
+                        continue;
+                    }
+                    if (u.kt * kBlock >= u.Lk) continue;  // a key tile past the sequence's keys
+                }
+                break;
+            }
+            const bool live = w < p.total_units;
+            if (lane == 0) {
+                volatile int *e = reinterpret_cast<volatile int *>(smem_raw + S::kOffUnits + s * 32);
+                e[0] = live ? 1 : 0;
+                e[1] = u.kt;
+                e[2] = u.z;
+                e[3] = u.hh;
+                e[4] = u.tq0;
+                e[5] = u.tk0;
+                e[6] = u.Lq;
+                e[7] = u.Lk;
+                ptx::bar_arrive(bar(S::kUnitReady + s));
+            }
+            __syncwarp();
+            if (!live) break;
+            const int k0 = u.kt * kBlock, qs0 = CAUSAL ? k0 : 0;
+            const int n = u.Lq > qs0 ? (u.Lq - qs0 + S::kQ - 1) / S::kQ : 0;
+            if (n == 0) continue;  // no query sees these keys: zero dK and dV only
+            // K and V of the unit once the previous unit's products are done with theirs
+            if (wi >= 1 && !(ok = wait(S::kKVEmpty, (wi - 1) & 1))) break;
+            if (leader) {
+                ptx::bar_arrive_expect_tx(bar(S::kKVFull), 2 * S::kKTileBytes);
+                int ky, kz;
+                unit_coords<VARLEN>(u, true, k0, ky, kz);
                 for (int c = 0; c < 2; ++c) {
-                    ptx::tma_load_3d(qb + c * S::kQBoxBytes, &tm_q, bar(S::kQFull + st), c * 64, qy, qz);
-                    ptx::tma_load_3d(qb + S::kQTileBytes + c * S::kQBoxBytes, &tm_do, bar(S::kQFull + st), c * 64,
-                                     qy, qz);
+                    ptx::tma_load_3d_hint(sbase + S::kOffK + c * S::kKBoxBytes, &tm_k, bar(S::kKVFull), c * 64, ky,
+                                          kz, once);
+                    ptx::tma_load_3d_hint(sbase + S::kOffV + c * S::kKBoxBytes, &tm_v, bar(S::kKVFull), c * 64, ky,
+                                          kz, once);
                 }
             }
-            ++nq;
-            // row buffer b is free once the key-row warps are done with sub-step j-2
-            if (j >= 2 && !wait(S::kPFull + b, ((j - 2) >> 1) & 1)) break;
-            if constexpr (VARLEN) {
-                load_rows_packed<S::kQ>(p, u, q0,
-                                        reinterpret_cast<float *>(smem_raw + S::kOffRows + b * 2 * S::kQ * 4),
-                                        bar(S::kLFull + b), leader);
-            } else if (leader) {
-                const uint32_t rows = ssmall + S::kOffRows + b * 2 * S::kQ * 4;
-                const size_t ro = static_cast<size_t>(u.z) * p.Sq_pad + q0;
-                ptx::bar_arrive_expect_tx(bar(S::kLFull + b), 2 * S::kQ * 4);
-                ptx::bulk_load(rows, p.lse2 + ro, S::kQ * 4, bar(S::kLFull + b));
-                ptx::bulk_load(rows + S::kQ * 4, p.delta + ro, S::kQ * 4, bar(S::kLFull + b));
+            ++wi;
+            for (int j = 0; j < n; ++j, ++J) {
+                const int st = J % S::kStages, b = J & 1;
+                // the stage held sub-step J-4's staged dQ_t until its reductions read it
+                if (J >= S::kStages && !(ok = wait(S::kStageFree + st, ((J / S::kStages) - 1) & 1))) break;
+                const int q0 = qs0 + j * S::kQ;
+                if (leader && !withheld(p.withhold, static_cast<uint32_t>(J))) {
+                    const uint32_t qb = sbase + S::kOffQ + st * S::kStageBytes;
+                    ptx::bar_arrive_expect_tx(bar(S::kQFull + st), S::kStageBytes);
+                    int qy, qz;
+                    unit_coords<VARLEN>(u, false, q0, qy, qz);
+                    for (int c = 0; c < 2; ++c) {
+                        ptx::tma_load_3d(qb + c * S::kQBoxBytes, &tm_q, bar(S::kQFull + st), c * 64, qy, qz);
+                        ptx::tma_load_3d(qb + S::kQTileBytes + c * S::kQBoxBytes, &tm_do, bar(S::kQFull + st),
+                                         c * 64, qy, qz);
+                    }
+                }
+                ++nq;
+                // row buffer b is free once the key-row warps are done with sub-step J-2
+                if (J >= 2 && !(ok = wait(S::kPFull + b, ((J - 2) >> 1) & 1))) break;
+                if constexpr (VARLEN) {
+                    load_rows_packed<S::kQ>(p, u, q0,
+                                            reinterpret_cast<float *>(smem_raw + S::kOffRows + b * 2 * S::kQ * 4),
+                                            bar(S::kLFull + b), leader);
+                } else if (leader) {
+                    const uint32_t rows = ssmall + S::kOffRows + b * 2 * S::kQ * 4;
+                    const size_t ro = static_cast<size_t>(u.z) * p.Sq_pad + q0;
+                    ptx::bar_arrive_expect_tx(bar(S::kLFull + b), 2 * S::kQ * 4);
+                    ptx::bulk_load(rows, p.lse2 + ro, S::kQ * 4, bar(S::kLFull + b));
+                    ptx::bulk_load(rows + S::kQ * 4, p.delta + ro, S::kQ * 4, bar(S::kLFull + b));
+                }
+                ++nl;
             }
-            ++nl;
         }
         // never leave with copies in flight
-        ptx::bar_wait(bar(S::kKVFull), 0, nullptr, p.timeout_ns);
+        if (wi > 0) ptx::bar_wait(bar(S::kKVFull), (wi - 1) & 1, nullptr, p.timeout_ns);
         for (int st = 0; st < S::kStages && st < nq; ++st) {
             const int last = (nq - 1) - ((nq - 1 - st) % S::kStages);
             ptx::bar_wait(bar(S::kQFull + st), (last / S::kStages) & 1, nullptr, p.timeout_ns);
@@ -879,7 +968,7 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             const int last = (nl - 1) - ((nl - 1 - b) % 2);
             ptx::bar_wait(bar(S::kLFull + b), (last >> 1) & 1, nullptr, p.timeout_ns);
         }
-    } else if ((warp == 1 || warp == 3) && n > 0) {
+    } else if (warp == 1 || warp == 3) {
         // ---- MMA issuers: warp 1 forms S^T and dP^T of each sub-step, warp 3
         // the products of the sub-step before it. A warp blocks in
         // tcgen05.mma while the tensor core's queue (a few MMAs) is full, so
@@ -891,20 +980,27 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
         constexpr uint32_t kIdQ = ptx::idesc_f16(BF16, D, S::kQ, true, true);       // dQ_t^T: A, B MN-major
         constexpr uint64_t kKBox16 = S::kKBoxBytes >> 4, kQBox16 = S::kQBoxBytes >> 4;
         constexpr uint64_t kStage16 = S::kStageBytes >> 4, kDS16 = S::kDSBytes >> 4, kRows16 = 2048 >> 4;
-        bool ok = wait(S::kKVFull, 0);
+        int J = 0, wi = 0;  // sub-steps and units with work so far
+        bool ok = true;
         if (warp == 1) {
             const uint64_t k_kmaj = ptx::smem_desc_sw128(sbase + S::kOffK, 16, 1024);
             const uint64_t v_kmaj = ptx::smem_desc_sw128(sbase + S::kOffV, 16, 1024);
             const uint64_t q_kmaj = ptx::smem_desc_sw128(sbase + S::kOffQ, 16, 1024);
             const uint64_t do_kmaj = ptx::smem_desc_sw128(sbase + S::kOffQ + S::kQTileBytes, 16, 1024);
-            for (int j = 0; j < n && ok; ++j) {
-                const int st = j % S::kStages, b = j & 1;
-                // S^T: Q_j landed and the buffer's P^T of sub-step j-2 consumed by its dV
-                const bool ready = ptx::bar_try_wait(bar(S::kQFull + st), (j / S::kStages) & 1) &&
-                                   (j < 2 || ptx::bar_try_wait(bar(S::kPTFree + b), ((j - 2) >> 1) & 1));
+            for (int i = 0; ok; ++i) {
+              UnitView uv;
+              if (!(ok = read_unit(i, uv)) || !uv.live) break;
+              if (uv.n == 0) continue;
+              if (!(ok = wait(S::kKVFull, wi & 1))) break;
+              ++wi;
+              for (int j = 0; j < uv.n && ok; ++j, ++J) {
+                const int st = J % S::kStages, b = J & 1;
+                // S^T: Q_J landed and the buffer's P^T of sub-step J-2 consumed by its dV
+                const bool ready = ptx::bar_try_wait(bar(S::kQFull + st), (J / S::kStages) & 1) &&
+                                   (J < 2 || ptx::bar_try_wait(bar(S::kPTFree + b), ((J - 2) >> 1) & 1));
                 if (!__all_sync(0xffffffffu, ready)) {
-                    if (!(ok = wait(S::kQFull + st, (j / S::kStages) & 1))) break;
-                    if (j >= 2 && !(ok = wait(S::kPTFree + b, ((j - 2) >> 1) & 1))) break;
+                    if (!(ok = wait(S::kQFull + st, (J / S::kStages) & 1))) break;
+                    if (J >= 2 && !(ok = wait(S::kPTFree + b, ((J - 2) >> 1) & 1))) break;
                 }
                 ptx::tc_fence_after();
                 const uint64_t so = static_cast<uint64_t>(st) * kStage16;
@@ -917,8 +1013,8 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
                         ptx::mma_ss(tb, k_kmaj + ka, q_kmaj + so + qa, kIdS, kk > 0);
                     }
                 }
-                // dP^T: the buffer's dQ_t^T of sub-step j-2 read out
-                if (j >= 2 && !(ok = wait(S::kBufFree + b, ((j - 2) >> 1) & 1))) break;
+                // dP^T: the buffer's dQ_t^T of sub-step J-2 read out
+                if (J >= 2 && !(ok = wait(S::kBufFree + b, ((J - 2) >> 1) & 1))) break;
                 ptx::tc_fence_after();
                 if (leader) {
 #pragma unroll
@@ -930,6 +1026,7 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
                     ptx::mma_commit(bar(S::kSFull + b));
                 }
                 __syncwarp();
+              }
             }
         } else {
             const uint64_t k_mn = ptx::smem_desc_sw128(sbase + S::kOffK, S::kKBoxBytes, 1024);
@@ -937,9 +1034,16 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             const uint64_t do_mn = ptx::smem_desc_sw128(sbase + S::kOffQ + S::kQTileBytes, S::kQBoxBytes, 1024);
             const uint64_t ds_kmaj = ptx::smem_desc_sw128(sbase + S::kOffDS, 16, 1024);
             const uint64_t ds_mn = ptx::smem_desc_sw128(sbase + S::kOffDS, S::kDSBytes, 1024);
-            for (int j = 0; j < n && ok; ++j) {
-                const int st = j % S::kStages, b = j & 1;
-                if (!(ok = wait(S::kPFull + b, (j >> 1) & 1))) break;
+            for (int i = 0; ok; ++i) {
+              UnitView uv;
+              if (!(ok = read_unit(i, uv)) || !uv.live) break;
+              if (uv.n == 0) continue;
+              // dQ_t^T reads K: the unit's K and V must have landed
+              if (!(ok = wait(S::kKVFull, wi & 1))) break;
+              ++wi;
+              for (int j = 0; j < uv.n && ok; ++j, ++J) {
+                const int st = J % S::kStages, b = J & 1;
+                if (!(ok = wait(S::kPFull + b, (J >> 1) & 1))) break;
                 ptx::tc_fence_after();
                 if (leader) {
                     const uint64_t so = static_cast<uint64_t>(st) * kStage16;
@@ -962,10 +1066,15 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
                     for (int kk = 0; kk < S::kQ / 16; ++kk)
                         ptx::mma_ss(tmem + S::kTmemDK, ds_kmaj + b * kDS16 + kk * 2, q_mn + so + kk * kRows16, kIdKV,
                                     (j > 0 || kk > 0) ? 1u : 0u);
-                    ptx::mma_commit(bar(S::kQEmpty + st));  // Q_j and dO_j have all their readers
+                    ptx::mma_commit(bar(S::kQEmpty + st));  // Q_J and dO_J have all their readers
                     ptx::mma_commit(bar(S::kDSFree + b));   // and so has dS^T of buffer b
                 }
                 __syncwarp();
+              }
+              // the unit's last products (and, before them, every S^T and
+              // dP^T) have read K and V: the next unit's may be loaded
+              if (ok && leader) ptx::mma_commit(bar(S::kKVEmpty));
+              __syncwarp();
             }
         }
         // each issuer waits for its own MMAs before the CTA may free TMEM
@@ -977,21 +1086,27 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
         const int wq = warp % 4;       // TMEM lane quarter
         const int h = (warp - 4) / 4;  // query half of every sub-step
         const int r = wq * 32 + lane;  // key row
-        const int key = k0 + r;
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t ds_row = sbase + S::kOffDS + (r >> 3) * 1024 + (r & 7) * 128;
+        int J = 0;  // sub-steps so far
         bool ok = true;
-        for (int j = 0; j < n; ++j) {
-            const int b = j & 1;
+        for (int iu = 0; ok; ++iu) {
+          UnitView uv;
+          if (!(ok = read_unit(iu, uv)) || !uv.live) break;
+          const BwdUnit &u = uv.u;
+          const int k0 = uv.k0, qs0 = uv.qs0, n = uv.n;
+          const int key = k0 + r;
+          for (int j = 0; j < n; ++j, ++J) {
+            const int b = J & 1;
             const int qc = qs0 + j * S::kQ + 32 * h;  // first query of this warp's chunk
             const uint32_t tb = tmem + lane_base + S::kTmemBuf + 128 * b;
             // the sub-step's rows, then S^T and dP^T: one test of both first,
             // the bounded waits only when one is open
-            const bool ready = ptx::bar_try_wait(bar(S::kSFull + b), (j >> 1) & 1) &&
-                               ptx::bar_try_wait(bar(S::kLFull + b), (j >> 1) & 1);
+            const bool ready = ptx::bar_try_wait(bar(S::kSFull + b), (J >> 1) & 1) &&
+                               ptx::bar_try_wait(bar(S::kLFull + b), (J >> 1) & 1);
             if (!__all_sync(0xffffffffu, ready)) {
-                if (!(ok = wait(S::kLFull + b, (j >> 1) & 1))) break;
-                if (!(ok = wait(S::kSFull + b, (j >> 1) & 1))) break;
+                if (!(ok = wait(S::kLFull + b, (J >> 1) & 1))) break;
+                if (!(ok = wait(S::kSFull + b, (J >> 1) & 1))) break;
             }
             ptx::tc_fence_after();
             uint32_t sv[32], dpv[32];
@@ -1023,8 +1138,11 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             }
             // P^T over the first 16 of this half's own S^T columns
             ptx::tmem_st16(tb + 32 * h, pp);
-            // dS^T buffer b is free once sub-step j-2's dQ_t^T and dK have read it
-            if (j >= 2 && !(ok = wait(S::kDSFree + b, ((j - 2) >> 1) & 1))) break;
+            // dS^T buffer b is free once sub-step J-2's dQ_t^T and dK have read it
+            if (J >= 2 && !(ok = wait(S::kDSFree + b, ((J - 2) >> 1) & 1))) break;
+            // the dS^T buffers hold the key-row warps' staging blocks during a
+            // unit's epilogue: every warp must have written out the previous unit's
+            if (j == 0 && iu > 0 && !(ok = wait(S::kStagingFree, (iu - 1) & 1))) break;
             // dS^T row r, queries [32h, 32h+32): 16-byte chunks 4h..4h+3, 128-byte swizzle
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -1037,10 +1155,13 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             ptx::fence_proxy_async_smem();  // dS^T is read by the tensor core next
             __syncwarp();
             if (lane == 0) ptx::bar_arrive(bar(S::kPFull + b));
-        }
-        // epilogue: head columns [64h, 64h+64) of dV and scale * dK for this key row
-        if (ok && n > 0) {
-            ok = wait(S::kDSFree + ((n - 1) & 1), ((n - 1) >> 1) & 1);  // the last dV and dK are done
+          }
+          if (!ok) break;
+        // epilogue: head columns [64h, 64h+64) of dV and scale * dK for this key
+        // row. The dV/dK accumulators are read out before this warp publishes
+        // the next unit's first P^T, which the next unit's first dV/dK wait for.
+        if (n > 0) {
+            ok = wait(S::kDSFree + ((J - 1) & 1), ((J - 1) >> 1) & 1);  // the last dV and dK are done
             ptx::tc_fence_after();
         }
         // The TMEM loads are warp-collective (.sync.aligned): every lane runs
@@ -1101,16 +1222,23 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
                 }
                 __syncwarp();  // the block is rewritten for the next tensor
             }
+            if (lane == 0) ptx::bar_arrive(bar(S::kStagingFree));
         }
-    } else if (warp >= 12 && n > 0) {
+        }
+    } else if (warp >= 12) {
         // ---- dQ_t^T warps: head column r, all 64 queries of the sub-step ----
         const int wq = warp % 4;
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         // head column r = 32 wq + lane of the staging tile: box wq, 4-byte word lane
         const uint32_t dq_col = sbase + S::kOffQ + wq * S::kDQBoxBytes + (lane & 3) * 4;
-        for (int j = 0; j < n; ++j) {
-            const int b = j & 1, st = j % S::kStages;
-            if (!wait(S::kDQFull + b, (j >> 1) & 1)) break;
+        int J = 0;  // sub-steps so far
+        bool ok = true;
+        for (int iu = 0; ok; ++iu) {
+          UnitView uv;
+          if (!(ok = read_unit(iu, uv)) || !uv.live) break;
+          for (int j = 0; j < uv.n; ++j, ++J) {
+            const int b = J & 1, st = J % S::kStages;
+            if (!(ok = wait(S::kDQFull + b, (J >> 1) & 1))) break;
             ptx::tc_fence_after();
             uint32_t v0[32], v1[32];
             const uint32_t tb = tmem + lane_base + S::kTmemBuf + 128 * b + 64;
@@ -1122,8 +1250,8 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::bar_arrive(bar(S::kBufFree + b));
-            // the sub-step's stage takes the tile once dV and dK are done with Q_j, dO_j
-            if (!wait(S::kQEmpty + st, (j / S::kStages) & 1)) break;
+            // the sub-step's stage takes the tile once dV and dK are done with Q_J, dO_J
+            if (!(ok = wait(S::kQEmpty + st, (J / S::kStages) & 1))) break;
             const uint32_t col = dq_col + st * S::kStageBytes;
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
@@ -1135,15 +1263,22 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             ptx::fence_proxy_async_smem();  // the bulk reduction reads the tile next
             __syncwarp();
             if (lane == 0) ptx::bar_arrive(bar(S::kStageReady + st));
+          }
         }
-    } else if (warp == 2 && n > 0) {
+    } else if (warp == 2) {
         // ---- bulk reductions of the staged dQ_t into the accumulator ----
         const bool leader = ptx::elect_one();
-        for (int j = 0; j < n; ++j) {
-            const int st = j % S::kStages;
-            if (!wait(S::kStageReady + st, (j / S::kStages) & 1)) break;
+        int J = 0;  // sub-steps so far
+        bool ok = true;
+        for (int iu = 0; ok; ++iu) {
+          UnitView uv;
+          if (!(ok = read_unit(iu, uv)) || !uv.live) break;
+          const BwdUnit &u = uv.u;
+          for (int j = 0; j < uv.n; ++j, ++J) {
+            const int st = J % S::kStages;
+            if (!(ok = wait(S::kStageReady + st, (J / S::kStages) & 1))) break;
             if (leader) {
-                const int q0 = qs0 + j * S::kQ;
+                const int q0 = uv.qs0 + j * S::kQ;
                 const uint32_t tile = sbase + S::kOffQ + st * S::kStageBytes;
                 int y, z;
                 unit_coords<VARLEN>(u, false, q0, y, z);
@@ -1154,6 +1289,7 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
                 ptx::bar_arrive(bar(S::kStageFree + st));
             }
             __syncwarp();
+          }
         }
         if (leader) ptx::bulk_wait_all();  // the reductions themselves are complete
         __syncwarp();
@@ -1182,8 +1318,11 @@ cudaError_t launch_t(const CUtensorMap *maps, const void *o, const void *dout, c
     constexpr int kSmem = D == 64 ? Shape<64>::kSmemBytes : ShapeQ64::kSmemBytes;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(p.BH * p.n_ktiles), D == 64 ? kThreads : kThreadsQ64, kSmem, st>>>(
-        maps[0], maps[1], maps[2], maps[3], maps[4], p);
+    // D = 64: one CTA per work unit; D = 128: persistent CTAs take units from a counter
+    const long long units = static_cast<long long>(p.BH) * p.n_ktiles;
+    const long long grid = D == 64 ? units : (units < p.grid ? units : p.grid);
+    kern<<<static_cast<unsigned>(grid), D == 64 ? kThreads : kThreadsQ64, kSmem, st>>>(maps[0], maps[1], maps[2],
+                                                                                        maps[3], maps[4], p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long n8 = (VARLEN ? static_cast<long long>(p.total_q) * p.H : static_cast<long long>(p.BH) * p.Sq) * D / 8;

@@ -101,6 +101,9 @@ struct BwdParams {
     int *err;              // device error word
     unsigned long long timeout_ns;
     int withhold;          // test support, 0 = off: CTA 0 never issues its Q/dO load number withhold - 1
+    int *work_counter;     // D = 128: next work unit to hand out (in the workspace, zeroed by the prep kernel)
+    int total_units;       // D = 128: work units of the launch (BH * n_ktiles)
+    int grid;              // D = 128: persistent CTAs (at most one per SM)
 };
 
 // Test support: a launch that withholds one load (see FwdParams::withhold)

@@ -246,8 +246,10 @@ FA_API fa_status_t fa_decode_paged_splitkv_fused(const void *q, const void *k_ca
                                                  float scale, fa_dtype_t dtype, void *stream);
 
 /*
- * fa_bwd_workspace_bytes - bytes of fp32 workspace fa_bwd needs:
- * 4 * (B*H*Sq*D + 2*B*H*ceil(Sq/128)*128); 0 for an invalid shape.
+ * fa_bwd_workspace_bytes - bytes of workspace fa_bwd needs:
+ * 4 * (B*H*Sq*D + 2*B*H*ceil(Sq/128)*128) + 16 (an fp32 dQ accumulator, the
+ * per-row statistics and the work counter of the D = 128 kernel); 0 for an
+ * invalid shape.
  */
 FA_API size_t fa_bwd_workspace_bytes(int B, int H, int Sq, int D);
 
@@ -266,9 +268,9 @@ FA_API size_t fa_bwd_workspace_bytes(int B, int H, int Sq, int D);
  *   dq [B,H,Sq,D], dk and dv [B,H,Sk,D]: outputs in the input dtype
  *   workspace   caller-owned device memory of at least
  *               fa_bwd_workspace_bytes(B, H, Sq, D) bytes, 16-byte aligned
- *               (fp32 dQ accumulator and per-row statistics); its contents on
- *               entry do not matter. Calls sharing a workspace must not
- *               overlap on the GPU.
+ *               (fp32 dQ accumulator, per-row statistics, work counter); its
+ *               contents on entry do not matter. Calls sharing a workspace
+ *               must not overlap on the GPU.
  *   D           64 or 128.
  * Three launches on `stream`. dQ sums contributions of all key tiles with
  * fp32 atomic additions, so its rounding can differ between runs; dK and dV
@@ -282,8 +284,8 @@ FA_API fa_status_t fa_bwd(const void *q, const void *k, const void *v, const voi
                           float scale, fa_dtype_t dtype, void *stream);
 
 /*
- * fa_bwd_varlen_workspace_bytes - bytes of fp32 workspace fa_bwd_varlen needs:
- * 4 * (total_q*H*D + 2*H*total_q); 0 for an invalid shape.
+ * fa_bwd_varlen_workspace_bytes - bytes of workspace fa_bwd_varlen needs:
+ * 4 * (total_q*H*D + 2*H*total_q) + 16; 0 for an invalid shape.
  */
 FA_API size_t fa_bwd_varlen_workspace_bytes(int total_q, int H, int D);
 

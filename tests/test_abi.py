@@ -188,7 +188,7 @@ def test_bwd_validation(lib):
     assert _bwd(lib, dq=MIS) == ALIGN
     assert _bwd(lib, ws=MIS) == ALIGN
     need = lib.fa_bwd_workspace_bytes(1, 2, 200, 128)
-    assert need == 4 * (2 * 200 * 128 + 2 * 2 * 256)
+    assert need == 4 * (2 * 200 * 128 + 2 * 2 * 256) + 16
     assert _bwd(lib, wsb=need - 4) == -12
     assert lib.fa_bwd_workspace_bytes(1, 2, 200, 96) == 0
 
@@ -212,7 +212,7 @@ def test_bwd_varlen_validation(lib):
         assert _bwd_varlen(lib, **{kw: MIS}) == ALIGN, kw
     assert _bwd_varlen(lib, cq=A + 2) == ALIGN
     need = lib.fa_bwd_varlen_workspace_bytes(500, 2, 128)
-    assert need == 4 * (500 * 2 * 128 + 2 * 2 * 500)
+    assert need == 4 * (500 * 2 * 128 + 2 * 2 * 500) + 16
     assert _bwd_varlen(lib, wsb=need - 4) == -12
     assert lib.fa_bwd_varlen_workspace_bytes(500, 2, 80) == 0
 

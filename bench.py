@@ -653,12 +653,72 @@ def run_wide_head(args, fa, torch, dev, stream, flush, world, key):
               f"fa_fwd_kernel<{w.D},fp16,non-causal,dense>")
     rec = {"workload": w.name, "value": tf, "unit": "TFLOPS", "ms_per_launch": ms, "steps": n,
            "kernel": kernel, "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "per_launch_flops": flops}
+    if key == "small":
+        rec.update(short_launch_context(args, fa, torch, dev, stream, flush, world, w, n))
     if w.D < 256:
         return rec
     if slices > 1:
         rec.update(output_slices=slices, executed_tflops=world * executed / (ms * 1e-3) / 1e12)
     rec["traffic"] = committed_traffic().get("fa_fwd_d256_kernel" + (f"_d{w.D}" if slices > 1 else ""))
     return rec
+
+
+def short_launch_context(args, fa, torch, dev, stream, flush, world, w, n):
+    """Context for a launch this short (a few microseconds of work per CTA):
+    - launch_floor_us: an empty kernel with the forward's launch shape (128
+      CTAs of 384 threads, 166,656 bytes of dynamic shared memory), timed
+      the same way (L2 flushed, events around the one launch): the fixed
+      cost of any launch of that shape;
+    - back_to_back: the forward launched 400 times in a row over 40 input
+      sets used in turn (336 MB, more than L2, so no flush between them),
+      one event pair around all of them: the rate of a stream of such
+      calls, where one launch's set-up overlaps the previous one's drain."""
+    import ctypes
+    from exact_attention_54_gb300 import build as fabuild
+    from exact_attention_54_gb300.metrics import attention_flops
+    st = ctypes.CDLL(fabuild.SELFTEST_LIB)
+    st.fa_selftest_empty_launch.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    sp = stream.cuda_stream
+
+    def empty():
+        if st.fa_selftest_empty_launch(128, 384, 166656, sp) != 0:
+            raise RuntimeError("fa_selftest_empty_launch failed")
+
+    for _ in range(3):
+        flush.fill_(float(1.0))
+        empty()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        flush.fill_(float(1.0))
+        evs[i][0].record(stream)
+        empty()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    floor_ms = aggregate_max([sum(e[0].elapsed_time(e[1]) for e in evs) / n], world)[0]
+
+    from exact_attention_54_gb300 import inputs
+    sets = []
+    for i in range(40):
+        q, k, v = (t.to(dev) for t in inputs.make_workload(w))
+        sets.append((q, k, v, torch.empty_like(q), torch.empty(w.B, w.H, w.Sq, dtype=torch.float32, device=dev)))
+    launches = 400
+    for i in range(40):
+        fa.fa_fwd(*sets[i][:4], sets[i][4], w.causal, w.scale, stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush.fill_(float(1.0))
+    e0.record(stream)
+    for i in range(launches):
+        q, k, v, o, lse = sets[i % 40]
+        fa.fa_fwd(q, k, v, o, lse, w.causal, w.scale, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    b2b_ms = aggregate_max([e0.elapsed_time(e1) / launches], world)[0]
+    flops = attention_flops(w.B, w.H, w.Sq, w.Sk, w.D, w.causal)
+    del sets
+    return {"launch_floor_us": floor_ms * 1e3,
+            "back_to_back": {"us_per_launch": b2b_ms * 1e3, "tflops": world * flops / (b2b_ms * 1e-3) / 1e12,
+                             "launches": launches, "input_sets": 40}}
 
 
 def run_shapes(args, fa, torch, dev, stream, flush, world):

@@ -240,5 +240,6 @@ def test_binding_fails_loudly_without_library(tmp_path):
 
 def test_selftest_library_exports(lib):
     st = ctypes.CDLL(fabuild.SELFTEST_LIB)
-    for n in ("fa_selftest_qk", "fa_selftest_pv", "fa_selftest_tn", "fa_selftest_ldmax", "fa_selftest_watchdog"):
+    for n in ("fa_selftest_qk", "fa_selftest_pv", "fa_selftest_tn", "fa_selftest_ldmax", "fa_selftest_watchdog",
+              "fa_selftest_empty_launch"):
         assert hasattr(st, n)

@@ -108,6 +108,30 @@ def test_dk_dv_aligned_to_16_bytes_only(D):
     assert_grad_close(dv.cpu(), rv, "dv at a 16-byte offset")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+def test_every_dq_row_written_from_a_nan_workspace(D, causal):
+    """dQ and the workspace start out as NaN: the call must clear what it
+    accumulates in the workspace and write every dQ row, with a ragged last
+    query tile and Sq != Sk."""
+    B, H, Sq, Sk = 2, 3, 333, 270
+    q, k, v = inputs.make_dense(B, H, Sq, Sk, D, torch.bfloat16, seed=71 + D)
+    do = inputs.make_dense(B, H, Sq, Sq, D, torch.bfloat16, seed=72 + D)[0]
+    qd, kd, vd, dod = dev(q, k, v, do)
+    o, lse = fa.flash_attention(qd, kd, vd, causal=causal, scale=0.1)
+    dq = torch.full_like(qd, float("nan"))
+    dk, dv = torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.full((fa.fa_bwd_workspace_bytes(B, H, Sq, D) // 4,), float("nan"), dtype=torch.float32,
+                    device="cuda")
+    fa.fa_bwd(qd, kd, vd, o, dod, lse, dq, dk, dv, ws, causal, 0.1)
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    assert not torch.isnan(dq).any()
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, causal, 0.1)
+    assert_grad_close(dq.cpu(), rq, f"dq D={D} causal={causal}")
+    assert_grad_close(dk.cpu(), rk, f"dk D={D} causal={causal}")
+
+
 def test_bwd_llama_prefill_full_size_two_heads():
     """The LLaMA-7B prefill shape (1,32,4096,4096,128, causal, bf16) through
     the full kernel; two heads compared against the oracle (about a minute of

@@ -68,6 +68,41 @@ def test_varlen_bwd_query_and_key_lengths_differ(D):
         assert torch.all(dk[a:b] == 0) and torch.all(dv[a:b] == 0)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+def test_varlen_bwd_queries_without_keys_get_zero_dq(D, causal):
+    """A sequence with queries but no keys: dS is empty there, so its dQ rows
+    are exactly zero. dQ and the workspace start out as NaN, so every dQ row
+    has to be written by the call; the other sequences match the oracle. The
+    keyless sequence's O and LSE are set to the empty-set values (0, -inf)."""
+    Lq, Lk = [40, 70, 0, 100], [60, 0, 30, 129]
+    H = 2
+    cq, ck = _cu(Lq), _cu(Lk)
+    g = torch.Generator().manual_seed(81)
+    q = inputs.randn((int(cq[-1]), H, D), torch.bfloat16, g)
+    do = inputs.randn((int(cq[-1]), H, D), torch.bfloat16, g)
+    k = inputs.randn((int(ck[-1]), H, D), torch.bfloat16, g)
+    v = inputs.randn((int(ck[-1]), H, D), torch.bfloat16, g)
+    qd, kd, vd, dod, cqd, ckd = dev(q, k, v, do, cq, ck)
+    o, lse = fa.flash_attention_varlen(qd, kd, vd, cqd, ckd, max(Lq), causal=causal, scale=0.1)
+    a, b = int(cq[1]), int(cq[2])
+    o[a:b] = 0
+    lse[:, a:b] = float("-inf")
+    dq = torch.full_like(qd, float("nan"))
+    dk, dv = torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.full((fa.fa_bwd_varlen_workspace_bytes(qd.shape[0], H, D) // 4,), float("nan"),
+                    dtype=torch.float32, device="cuda")
+    fa.fa_bwd_varlen(qd, kd, vd, o, dod, lse, dq, dk, dv, ws, cqd, ckd, max(Lq), max(Lk), causal, 0.1)
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    dq = dq.cpu()
+    assert torch.all(dq[a:b] == 0)
+    rq, rk, rv = oracle.attention_bwd_varlen(q, k, v, do, cq, ck, causal, 0.1)
+    assert_grad_close(dq, rq, f"dq D={D} causal={causal}")
+    assert_grad_close(dk.cpu(), rk, f"dk D={D} causal={causal}")
+    assert_grad_close(dv.cpu(), rv, f"dv D={D} causal={causal}")
+
+
 def test_varlen_bwd_dk_dv_equal_dense_per_sequence_bitwise():
     lengths = [200, 1, 384, 129, 77]
     H, D = 2, 128

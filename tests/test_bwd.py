@@ -132,6 +132,29 @@ def test_every_dq_row_written_from_a_nan_workspace(D, causal):
     assert_grad_close(dk.cpu(), rk, f"dk D={D} causal={causal}")
 
 
+@pytest.mark.parametrize("causal,Sq,Sk", [(True, 300, 700), (False, 333, 260)])
+def test_many_units_per_cta_equal_single_head_calls(causal, Sq, Sk):
+    """B*H = 160 heads of 3-6 key tiles: the persistent CTAs (one per SM) each
+    take several (key tile, head) units in turn, and causal with Sq < Sk
+    interleaves units whose keys no query sees. dK and dV of sampled heads
+    equal, bit for bit, those of a call on that head alone; dQ, dK and dV
+    match the oracle."""
+    B, H, D = 4, 40, 128
+    q, k, v = inputs.make_dense(B, H, Sq, Sk, D, torch.bfloat16, seed=91)
+    do = inputs.make_dense(B, H, Sq, Sq, D, torch.bfloat16, seed=92)[0]
+    dq, dk, dv = grads(q, k, v, do, causal, 0.1)
+    for b, h in [(0, 0), (1, 17), (3, 39)]:
+        one = [x[b:b + 1, h:h + 1].contiguous() for x in (q, k, v, do)]
+        _, dk1, dv1 = grads(*one, causal, 0.1)
+        assert torch.equal(dk[b:b + 1, h:h + 1].view(torch.int16), dk1.view(torch.int16)), (b, h)
+        assert torch.equal(dv[b:b + 1, h:h + 1].view(torch.int16), dv1.view(torch.int16)), (b, h)
+        rq, rk, rv = oracle.attention_bwd(*one, causal, 0.1)
+        what = f"head ({b}, {h}) causal={causal}"
+        assert_grad_close(dq[b:b + 1, h:h + 1], rq, "dq " + what)
+        assert_grad_close(dk[b:b + 1, h:h + 1], rk, "dk " + what)
+        assert_grad_close(dv[b:b + 1, h:h + 1], rv, "dv " + what)
+
+
 def test_bwd_llama_prefill_full_size_two_heads():
     """The LLaMA-7B prefill shape (1,32,4096,4096,128, causal, bf16) through
     the full kernel; two heads compared against the oracle (about a minute of

@@ -114,64 +114,73 @@ __device__ __forceinline__ float to_f32(uint16_t x) {
 
 // ------------------------------------------------------------- preprocess --
 
-// One warp per (head, padded row): D_i = sum_d dO_id O_id, LSE in base 2, and
-// the zeroed dQ accumulator row. Rows past Sq get D = 0 and LSE = +inf.
-// Packed sequences: one warp per (head, token) row of the [H][total_q] row
-// arrays, with O, dO and the accumulator laid out [total_q][H][D]; no padding
-// (the main kernel fills rows past a sequence itself).
+// Per query row of every head: D_i = sum_d dO_id O_id, the LSE in base 2 and
+// a zeroed dQ accumulator row. Grid: x = chunks of kPrepRows rows, y and z =
+// the head (dense: B*H index over [B*H][Sq_pad] row arrays; packed: head h
+// over [H][total_q] row arrays, with O, dO and the accumulator laid out
+// [total_q][H][D]). Dense rows past Sq get D = 0 and LSE = +inf. Each warp
+// takes kPrepPasses groups of rows, all of its 16-byte loads in flight
+// before the first sum; the D/8 lanes of a row reduce among themselves.
+constexpr int kPrepPasses = 4;
+template <int D>
+constexpr int kPrepRows = 8 * (32 / (D / 8)) * kPrepPasses;  // rows per 256-thread block
+
 template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(256)
     fa_bwd_prep_kernel(const uint16_t *__restrict__ o, const uint16_t *__restrict__ dout,
                        const float *__restrict__ lse, const BwdParams p) {
-    constexpr int E = D / 32;  // elements per lane
+    constexpr int kLanesPerRow = D / 8;              // 16-byte pieces of a 16-bit row
+    constexpr int kRowsPerPass = 32 / kLanesPerRow;  // rows one warp instruction covers
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     // the main kernel's work counter starts every call at zero
-    if (blockIdx.x == 0 && threadIdx.x == 0 && p.work_counter != nullptr) *p.work_counter = 0;
-    const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;
-    size_t srow, off, lrow;
-    if constexpr (VARLEN) {
-        if (row >= static_cast<long long>(p.H) * p.total_q) return;
-        const int h = static_cast<int>(row / p.total_q);
-        const int t = static_cast<int>(row % p.total_q);
-        srow = lrow = static_cast<size_t>(row);
-        off = (static_cast<size_t>(t) * p.H + h) * D + lane * E;
-    } else {
-        if (row >= static_cast<long long>(p.BH) * p.Sq_pad) return;
-        const int bh = static_cast<int>(row / p.Sq_pad);
-        const int r = static_cast<int>(row % p.Sq_pad);
-        srow = static_cast<size_t>(bh) * p.Sq_pad + r;
-        if (r >= p.Sq) {
-            if (lane == 0) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0 && p.work_counter != nullptr)
+        *p.work_counter = 0;
+    const int z = static_cast<int>(blockIdx.z * gridDim.y + blockIdx.y);
+    if (z >= (VARLEN ? p.H : p.BH)) return;
+    const int rows = VARLEN ? p.total_q : p.Sq_pad;   // rows of one head's row arrays
+    const int valid = VARLEN ? p.total_q : p.Sq;       // rows with O and dO
+    const int sub = lane % kLanesPerRow, grp = lane / kLanesPerRow;
+    const int r0 = static_cast<int>(blockIdx.x) * kPrepRows<D> + warp * kRowsPerPass * kPrepPasses + grp;
+    uint4 ov[kPrepPasses], gv[kPrepPasses];
+    size_t off[kPrepPasses];
+#pragma unroll
+    for (int i = 0; i < kPrepPasses; ++i) {
+        const int r = r0 + i * kRowsPerPass;
+        off[i] = (VARLEN ? static_cast<size_t>(r) * p.H + z : static_cast<size_t>(z) * p.Sq + r) * D + sub * 8;
+        if (r < valid) {
+            ov[i] = __ldcs(reinterpret_cast<const uint4 *>(o + off[i]));
+            gv[i] = __ldcs(reinterpret_cast<const uint4 *>(dout + off[i]));
+        } else {
+            ov[i] = gv[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kPrepPasses; ++i) {
+        const int r = r0 + i * kRowsPerPass;
+        const uint32_t a[4] = {ov[i].x, ov[i].y, ov[i].z, ov[i].w}, c[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc = fmaf(to_f32<BF16>(static_cast<uint16_t>(a[e] & 0xffffu)), to_f32<BF16>(static_cast<uint16_t>(c[e] & 0xffffu)), acc);
+            acc = fmaf(to_f32<BF16>(static_cast<uint16_t>(a[e] >> 16)), to_f32<BF16>(static_cast<uint16_t>(c[e] >> 16)), acc);
+        }
+#pragma unroll
+        for (int s = kLanesPerRow / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+        if (r < valid) {
+            float4 *acc_row = reinterpret_cast<float4 *>(p.dq_acc + off[i]);
+            acc_row[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            acc_row[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (sub == 0 && r < rows) {
+            const size_t srow = static_cast<size_t>(z) * rows + r;
+            if (r < valid) {
+                p.delta[srow] = acc;
+                p.lse2[srow] = lse[VARLEN ? srow : static_cast<size_t>(z) * p.Sq + r] * 1.4426950408889634f;
+            } else {
                 p.delta[srow] = 0.f;
                 p.lse2[srow] = CUDART_INF_F;
             }
-            return;
         }
-        lrow = static_cast<size_t>(bh) * p.Sq + r;
-        off = lrow * D + lane * E;
-    }
-    // E = 2 or 4 consecutive 16-bit values per lane: one 4- or 8-byte load
-    // each from O and dO, one 8- or 16-byte store of zeros
-    uint16_t ov[E], gv[E];
-    if constexpr (E == 4) {
-        const uint2 a = *reinterpret_cast<const uint2 *>(o + off), c = *reinterpret_cast<const uint2 *>(dout + off);
-        ov[0] = a.x & 0xffffu, ov[1] = a.x >> 16, ov[2] = a.y & 0xffffu, ov[3] = a.y >> 16;
-        gv[0] = c.x & 0xffffu, gv[1] = c.x >> 16, gv[2] = c.y & 0xffffu, gv[3] = c.y >> 16;
-        *reinterpret_cast<float4 *>(p.dq_acc + off) = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else {
-        const uint32_t a = *reinterpret_cast<const uint32_t *>(o + off), c = *reinterpret_cast<const uint32_t *>(dout + off);
-        ov[0] = a & 0xffffu, ov[1] = a >> 16;
-        gv[0] = c & 0xffffu, gv[1] = c >> 16;
-        *reinterpret_cast<float2 *>(p.dq_acc + off) = make_float2(0.f, 0.f);
-    }
-    float acc = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc = fmaf(to_f32<BF16>(ov[e]), to_f32<BF16>(gv[e]), acc);
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (lane == 0) {
-        p.delta[srow] = acc;
-        p.lse2[srow] = lse[lrow] * 1.4426950408889634f;
     }
 }
 
@@ -1308,9 +1317,14 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
 template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 cudaError_t launch_t(const CUtensorMap *maps, const void *o, const void *dout, const float *lse, void *dq,
                      const BwdParams &p, cudaStream_t st) {
-    const long long rows = VARLEN ? static_cast<long long>(p.H) * p.total_q : static_cast<long long>(p.BH) * p.Sq_pad;
-    fa_bwd_prep_kernel<D, BF16, VARLEN><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
-        static_cast<const uint16_t *>(o), static_cast<const uint16_t *>(dout), lse, p);
+    // prep grid: row chunks x heads (heads split over y and z: at most 65535 each)
+    const int heads = VARLEN ? p.H : p.BH;
+    const int head_rows = VARLEN ? p.total_q : p.Sq_pad;
+    const unsigned hy = static_cast<unsigned>(heads < 65535 ? heads : 65535);
+    const dim3 prep_grid(static_cast<unsigned>((head_rows + kPrepRows<D> - 1) / kPrepRows<D>), hy,
+                         static_cast<unsigned>((heads + hy - 1) / hy));
+    fa_bwd_prep_kernel<D, BF16, VARLEN><<<prep_grid, 256, 0, st>>>(static_cast<const uint16_t *>(o),
+                                                                   static_cast<const uint16_t *>(dout), lse, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // D = 64: 128-query steps; D = 128: 64-query sub-steps, double-buffered in TMEM

@@ -132,6 +132,9 @@ __global__ void __launch_bounds__(256)
     constexpr int kLanesPerRow = D / 8;              // 16-byte pieces of a 16-bit row
     constexpr int kRowsPerPass = 32 / kLanesPerRow;  // rows one warp instruction covers
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    // the main kernel may be launched now: it sets up its barriers and TMEM
+    // and then waits for this grid to complete
+    ptx::grid_launch_dependents();
     // the main kernel's work counter starts every call at zero
     if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0 && p.work_counter != nullptr)
         *p.work_counter = 0;
@@ -189,6 +192,8 @@ __global__ void __launch_bounds__(256)
 template <bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float *__restrict__ acc, uint16_t *__restrict__ dq,
                                                         long long n8, float scale) {
+    // launched as a dependent of the main kernel: its reductions must be complete
+    ptx::grid_dependency_wait();
     const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= n8) return;
     const float4 a = reinterpret_cast<const float4 *>(acc)[2 * i];
@@ -839,6 +844,11 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched as a dependent of the prep kernel: everything above overlaps
+    // its tail; the work counter, row values and zeroed accumulator it writes
+    // are read only after this wait. The dQ conversion launch may start.
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
 
     // A published unit as every role sees it; n: its 64-query sub-steps from
     // the first query that sees any of its keys.
@@ -1335,14 +1345,29 @@ cudaError_t launch_t(const CUtensorMap *maps, const void *o, const void *dout, c
     // D = 64: one CTA per work unit; D = 128: persistent CTAs take units from a counter
     const long long units = static_cast<long long>(p.BH) * p.n_ktiles;
     const long long grid = D == 64 ? units : (units < p.grid ? units : p.grid);
-    kern<<<static_cast<unsigned>(grid), D == 64 ? kThreads : kThreadsQ64, kSmem, st>>>(maps[0], maps[1], maps[2],
-                                                                                        maps[3], maps[4], p);
-    e = cudaGetLastError();
+    // D = 128: the main and the conversion kernels are launched as programmatic
+    // dependents (each waits for its predecessor in the kernel itself)
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(D == 64 ? kThreads : kThreadsQ64);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = D == 64 ? 0 : 1;
+    e = cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], p);
     if (e != cudaSuccess) return e;
     const long long n8 = (VARLEN ? static_cast<long long>(p.total_q) * p.H : static_cast<long long>(p.BH) * p.Sq) * D / 8;
-    fa_bwd_dq_kernel<BF16><<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, st>>>(
-        p.dq_acc, static_cast<uint16_t *>(dq), n8, p.scale);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg2 = {};
+    cfg2.gridDim = dim3(static_cast<unsigned>((n8 + 255) / 256));
+    cfg2.blockDim = dim3(256);
+    cfg2.stream = st;
+    cfg2.attrs = pdl;
+    cfg2.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg2, fa_bwd_dq_kernel<BF16>, static_cast<const float *>(p.dq_acc),
+                              static_cast<uint16_t *>(dq), n8, p.scale);
 }
 
 }  // namespace bwd

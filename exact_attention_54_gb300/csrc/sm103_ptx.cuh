@@ -195,6 +195,16 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// Programmatic dependent launch. launch_dependents: the next kernel on the
+// stream, if launched with programmatic serialization, may start once every
+// block of this grid has issued it (or exited). wait: block until the grid
+// this one depends on has completed and its memory is visible (returns at
+// once when the launch had no such dependency).
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA / tensor core) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -19,8 +19,8 @@
 // softmax warps exponentiate tile j, and "S tile j is ready" also means that
 // P V j-2 has finished (so P buffer j mod 2 is free again).
 //
-// Roles (256 threads): warp 0 TMA producer of Q and K (plus an L2 prefetch of
-// the next item's Q), warp 1 MMA issuer and TMEM owner, warp 2 TMA producer of
+// Roles (256 threads): warp 0 TMA producer of Q and K, warp 1 MMA issuer and
+// TMEM owner, warp 2 TMA producer of
 // V, warps 4..7 softmax (one query row per thread). Q K^T is 16 MMAs of
 // 128x64x16 per K tile; P V is 4 MMAs of 128x256x16 per V tile with P read
 // from TMEM.
@@ -217,19 +217,6 @@ __device__ void producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, const 
             ptx::bar_arrive_expect_tx(bar(S::kQFull), S::kQTileBytes);
             load_rows<S::kColBlocks, VARLEN>(tq, sbase + S::kOffQ, S::kQBoxBytes, bar(S::kQFull), wk, wk.seq_q0,
                                              wk.q_start, p.H, 0);
-            const int wn = work_index(r + 1);
-            if (wn < num_items<DQK, VARLEN>(p, sbase)) {
-                const Work nx = get_work<DQK, CAUSAL, VARLEN>(p, wn);
-                if (nx.n_kv > 0) {
-#pragma unroll
-                    for (int c = 0; c < S::kColBlocks; ++c) {
-                        if constexpr (VARLEN)
-                            ptx::tma_prefetch_3d(tq, c * 64, nx.h, nx.seq_q0 + nx.q_start);
-                        else
-                            ptx::tma_prefetch_3d(tq, c * 64, nx.q_start, nx.b * p.H + nx.h);
-                    }
-                }
-            }
         }
         for (int j = 0; j < wk.n_kv && ok; ++j) {
             for (int c = 0; c < S::kChunks; ++c, ++it) {

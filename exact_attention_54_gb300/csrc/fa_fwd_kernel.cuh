@@ -12,9 +12,8 @@
 // that straddle it are masked (k_idx <= q_idx, top-left aligned).
 //
 // GB300 mapping (one CTA per SM, persistent):
-//   warp 0        TMA producer of Q (a tile pair once per work item, plus an L2
-//                 prefetch of the next item's pair) and of the K ring
-//                 (128-byte swizzle, 128 rows x 64 columns per box)
+//   warp 0        TMA producer of Q (a tile pair once per work item) and of
+//                 the K ring (128-byte swizzle, 128 rows x 64 columns per box)
 //   warp 2        TMA producer of the V ring (K and V rings are separate, so K
 //                 tiles, needed first, are released and refilled earlier)
 //   warp 1        MMA issuer (one thread): S_t = Q_t K^T into TMEM, then
@@ -257,8 +256,9 @@ __device__ __forceinline__ void load_kv_tile(const CUtensorMap *tm, uint32_t dst
     }
 }
 
-// Q and K producer (one thread). Also asks L2 for the next work item's Q
-// tiles while the current item runs.
+// Q and K producer (one thread). It issues no L2 prefetches: asking L2 for
+// the next item's Q while the current item ran cost 1.5 % (dense) and 4 %
+// (packed sequences), and K/V tiles prefetched ahead of the ring cost more.
 template <int D, bool CAUSAL, bool VARLEN>
 __device__ void fwd_producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, const FwdParams &p, uint32_t sbase,
                                 volatile int *abort_flag) {
@@ -267,22 +267,6 @@ __device__ void fwd_producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, co
     const uint32_t bars = sbase + S::kOffBar;
     auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
     const bool leader = ptx::elect_one();
-    auto prefetch_q = [&](int r) {
-        if (work_index(r) >= num_items<VARLEN>(p, sched)) return;
-        const Work nx = get_work<CAUSAL, VARLEN>(p, r, sched);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            if (nx.n_kv[t] == 0) continue;
-#pragma unroll
-            for (int c = 0; c < S::kColBlocks; ++c) {
-                if (!leader) continue;
-                if constexpr (VARLEN)
-                    ptx::tma_prefetch_3d(tq, c * 64, nx.h, nx.seq_q0 + nx.q_start[t]);
-                else
-                    ptx::tma_prefetch_3d(tq, c * 64, nx.q_start[t], nx.b * p.H + nx.h);
-            }
-        }
-    };
     const uint64_t stream_pol = ptx::l2_policy_evict_first();
     uint32_t it = 0;  // K tiles issued
     uint32_t wi = 0;  // work items loaded
@@ -312,7 +296,6 @@ __device__ void fwd_producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, co
                                           stream_pol);
             }
         }
-        prefetch_q(r + 1);
         for (int j = 0; j < wk.n_kv_max; ++j, ++it) {
             // All CTAs fill their rings at once when the kernel starts; the
             // first products need only Q and K tile 0, so the rest of the

@@ -270,32 +270,46 @@ __device__ void fwd_producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, co
     const uint64_t stream_pol = ptx::l2_policy_evict_first();
     uint32_t it = 0;  // K tiles issued
     uint32_t wi = 0;  // work items loaded
+    uint32_t nq = 0;  // Q pair loads issued
     bool ok = true;
     for (int r = 0; ok; ++r) {
         const int w = work_index(r);
         if (w >= num_items<VARLEN>(p, sched)) break;
         const Work wk = get_work<CAUSAL, VARLEN>(p, r, sched);
         if (wk.n_kv_max == 0) continue;
-        if (wi > 0 && !(ok = ptx::warp_all(ptx::bar_wait(bar(S::kQEmpty), (wi - 1) & 1, abort_flag, p.timeout_ns))))
-            break;
-        uint32_t qbytes = 0;
+        // The item's Q pair, once the previous item's last Q K^T has read
+        // the buffer.
+        auto load_q = [&]() -> bool {
+            if (nq > 0 &&
+                !ptx::warp_all(ptx::bar_wait(bar(S::kQEmpty), (nq - 1) & 1, abort_flag, p.timeout_ns)))
+                return false;
+            uint32_t qbytes = 0;
 #pragma unroll
-        for (int t = 0; t < 2; ++t) qbytes += wk.n_kv[t] > 0 ? S::kTileBytes : 0;
-        if (leader) ptx::bar_arrive_expect_tx(bar(S::kQFull), qbytes);
+            for (int t = 0; t < 2; ++t) qbytes += wk.n_kv[t] > 0 ? S::kTileBytes : 0;
+            if (leader) ptx::bar_arrive_expect_tx(bar(S::kQFull), qbytes);
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            if (wk.n_kv[t] == 0 || !leader) continue;
+            for (int t = 0; t < 2; ++t) {
+                if (wk.n_kv[t] == 0 || !leader) continue;
 #pragma unroll
-            for (int c = 0; c < S::kColBlocks; ++c) {
-                // Q tiles are read once: evict them first, keep L2 for K and V
-                const uint32_t dst = sbase + S::kOffQ + t * S::kTileBytes + c * S::kBlockBytes;
-                if constexpr (VARLEN)
-                    ptx::tma_load_3d_hint(dst, tq, bar(S::kQFull), c * 64, wk.h, wk.seq_q0 + wk.q_start[t], stream_pol);
-                else
-                    ptx::tma_load_3d_hint(dst, tq, bar(S::kQFull), c * 64, wk.q_start[t], wk.b * p.H + wk.h,
-                                          stream_pol);
+                for (int c = 0; c < S::kColBlocks; ++c) {
+                    // Q tiles are read once: evict them first, keep L2 for K and V
+                    const uint32_t dst = sbase + S::kOffQ + t * S::kTileBytes + c * S::kBlockBytes;
+                    if constexpr (VARLEN)
+                        ptx::tma_load_3d_hint(dst, tq, bar(S::kQFull), c * 64, wk.h, wk.seq_q0 + wk.q_start[t],
+                                              stream_pol);
+                    else
+                        ptx::tma_load_3d_hint(dst, tq, bar(S::kQFull), c * 64, wk.q_start[t], wk.b * p.H + wk.h,
+                                              stream_pol);
+                }
             }
-        }
+            ++nq;
+            return true;
+        };
+        // The first item loads Q before K; a later item loads its first K
+        // tile first: that ring stage frees rounds before the Q buffer does
+        // (at the previous item's last Q K^T), and the K tile would otherwise
+        // wait behind the Q load.
+        if (wi == 0 && !(ok = load_q())) break;
         for (int j = 0; j < wk.n_kv_max; ++j, ++it) {
             // All CTAs fill their rings at once when the kernel starts; the
             // first products need only Q and K tile 0, so the rest of the
@@ -313,7 +327,9 @@ __device__ void fwd_producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, co
                 load_kv_tile<D, VARLEN>(tk, sbase + S::kOffK + stage * S::kTileBytes, bar(S::kKFull + stage), wk, j,
                                         p.H);
             }
+            if (wi > 0 && j == 0 && !(ok = load_q())) break;
         }
+        if (!ok) break;
         ++wi;
     }
     // Never leave with copies in flight: wait (bounded, even after an abort)
@@ -322,7 +338,7 @@ __device__ void fwd_producer_qk(const CUtensorMap *tq, const CUtensorMap *tk, co
         const uint32_t last = (it - 1) - ((it - 1 - s) % S::kKStages);
         ptx::bar_wait(bar(S::kKFull + s), (last / S::kKStages) & 1, nullptr, p.timeout_ns);
     }
-    if (wi > 0) ptx::bar_wait(bar(S::kQFull), (wi - 1) & 1, nullptr, p.timeout_ns);
+    if (nq > 0) ptx::bar_wait(bar(S::kQFull), (nq - 1) & 1, nullptr, p.timeout_ns);
 }
 
 // V producer (one thread): runs ahead of the P V products as far as its ring allows.

@@ -57,8 +57,10 @@ struct FwdShape {
     static constexpr int kColBlocks = D / 64;            // 128-byte column blocks per row
     static constexpr int kBlockBytes = kBlockM * 128;    // one 128-row x 64-column box
     static constexpr int kTileBytes = kBlockM * D * 2;   // one 128-row tile of Q, K or V
-    static constexpr int kKStages = (D == 128) ? 3 : 4;  // K ring depth (K is needed first)
-    static constexpr int kVStages = (D == 128) ? 2 : 4;  // V ring depth
+    // D = 128: a K tile is free once both Q K^T of its round are issued, a V
+    // tile only after both P V, so V gets the deeper ring
+    static constexpr int kKStages = (D == 128) ? 2 : 4;  // K ring depth
+    static constexpr int kVStages = (D == 128) ? 3 : 4;  // V ring depth
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kKStages * kTileBytes;

@@ -772,7 +772,8 @@ struct ShapeQ64 {
     static constexpr int kUnitFree = 37;   // +slot: every role has read it (15 warps)
     // a unit's dK/dV written out of every key-row warp's staging block (8 warps)
     static constexpr int kStagingFree = 41;
-    static constexpr int kNumBars = 42;
+    static constexpr int kPTFull = 42;     // +b: P^T written (8 warps): dV may start before dS^T is
+    static constexpr int kNumBars = 44;
     static constexpr int kOffMisc = kNumBars * 8;
     static constexpr int kOffRows = 384;   // + b * 512: float lse2[64], delta[64]
     // + slot * 32: int {live, kt, z, hh, tq0, tk0, Lq, Lk} of a published unit
@@ -824,6 +825,7 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             if (i == S::kTeardown) count = 2;  // one commit per MMA-issuing warp
             if (i >= S::kUnitFree && i < S::kUnitFree + S::kRing) count = kThreadsQ64 / 32 - 1;  // every warp but 0
             if (i == S::kStagingFree) count = 2 * kBlock / 32;  // the key-row warps
+            if (i >= S::kPTFull && i < S::kPTFull + 2) count = 2 * kBlock / 32;  // the key-row warps
             ptx::bar_init(bar(i), count);
         }
         *abort_flag = 0;
@@ -1062,24 +1064,30 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
               ++wi;
               for (int j = 0; j < uv.n && ok; ++j, ++J) {
                 const int st = J % S::kStages, b = J & 1;
-                if (!(ok = wait(S::kPFull + b, (J >> 1) & 1))) break;
+                const uint64_t so = static_cast<uint64_t>(st) * kStage16;
+                const uint32_t tb = tmem + S::kTmemBuf + 128 * b;
+                // dV += P^T dO over the 64 queries (P^T of queries [32h, 32h+32)
+                // in columns [32h, 32h+16) of the buffer) as soon as P^T is in:
+                // it frees the buffer's S^T columns for sub-step J+2
+                if (!(ok = wait(S::kPTFull + b, (J >> 1) & 1))) break;
                 ptx::tc_fence_after();
                 if (leader) {
-                    const uint64_t so = static_cast<uint64_t>(st) * kStage16;
-                    const uint32_t tb = tmem + S::kTmemBuf + 128 * b;
-                    // dQ_t^T = K^T dS^T over the 128 keys, into the buffer's dP^T
-                    // columns, first: its read-out frees them for sub-step j+2
-#pragma unroll
-                    for (int kk = 0; kk < kBlock / 16; ++kk)
-                        ptx::mma_ss(tb + 64, k_mn + kk * kRows16, ds_mn + b * kDS16 + kk * kRows16, kIdQ, kk > 0);
-                    ptx::mma_commit(bar(S::kDQFull + b));
-                    // dV += P^T dO over the 64 queries (P^T of queries [32h, 32h+32)
-                    // in columns [32h, 32h+16) of the buffer): frees the S^T columns
 #pragma unroll
                     for (int kk = 0; kk < S::kQ / 16; ++kk)
                         ptx::mma_ts(tmem + S::kTmemDV, tb + kk * 8 + (kk >= 2 ? 16 : 0), do_mn + so + kk * kRows16,
                                     kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
                     ptx::mma_commit(bar(S::kPTFree + b));
+                }
+                __syncwarp();
+                if (!(ok = wait(S::kPFull + b, (J >> 1) & 1))) break;
+                ptx::tc_fence_after();
+                if (leader) {
+                    // dQ_t^T = K^T dS^T over the 128 keys, into the buffer's dP^T
+                    // columns: its read-out frees them for sub-step J+2
+#pragma unroll
+                    for (int kk = 0; kk < kBlock / 16; ++kk)
+                        ptx::mma_ss(tb + 64, k_mn + kk * kRows16, ds_mn + b * kDS16 + kk * kRows16, kIdQ, kk > 0);
+                    ptx::mma_commit(bar(S::kDQFull + b));
                     // dK += dS^T Q
 #pragma unroll
                     for (int kk = 0; kk < S::kQ / 16; ++kk)
@@ -1142,9 +1150,8 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             uint32_t pp[16], dd[16];
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
-                const float4 lv = lq[i / 4], dv4 = dq4[i / 4];
+                const float4 lv = lq[i / 4];
                 const float l0 = (i % 4 == 0) ? lv.x : lv.z, l1 = (i % 4 == 0) ? lv.y : lv.w;
-                const float d0 = (i % 4 == 0) ? dv4.x : dv4.z, d1 = (i % 4 == 0) ? dv4.y : dv4.w;
                 float e0 = ptx::ex2(fmaf(__uint_as_float(sv[i]), p.scale_log2, -l0));
                 float e1 = ptx::ex2(fmaf(__uint_as_float(sv[i + 1]), p.scale_log2, -l1));
                 if (need_mask) {
@@ -1152,11 +1159,23 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
                     if (i + 1 < lo) e1 = 0.f;
                 }
                 pp[i / 2] = ptx::pack2<BF16>(e0, e1);
+            }
+            // P^T over the first 16 of this half's own S^T columns, published
+            // at once: dV starts while dS^T is formed
+            ptx::tmem_st16(tb + 32 * h, pp);
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::bar_arrive(bar(S::kPTFull + b));
+            // dS = P (dP - D_i), with P as rounded for dV
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const float4 dv4 = dq4[i / 4];
+                const float d0 = (i % 4 == 0) ? dv4.x : dv4.z, d1 = (i % 4 == 0) ? dv4.y : dv4.w;
+                const float e0 = ptx::unpack_lo<BF16>(pp[i / 2]), e1 = ptx::unpack_hi<BF16>(pp[i / 2]);
                 dd[i / 2] = ptx::pack2<BF16>(e0 * (__uint_as_float(dpv[i]) - d0),
                                              e1 * (__uint_as_float(dpv[i + 1]) - d1));
             }
-            // P^T over the first 16 of this half's own S^T columns
-            ptx::tmem_st16(tb + 32 * h, pp);
             // dS^T buffer b is free once sub-step J-2's dQ_t^T and dK have read it
             if (J >= 2 && !(ok = wait(S::kDSFree + b, ((J - 2) >> 1) & 1))) break;
             // the dS^T buffers hold the key-row warps' staging blocks during a
@@ -1169,8 +1188,7 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
                 st_shared_v4(ds_row + b * S::kDSBytes + chunk * 16, dd[4 * m], dd[4 * m + 1], dd[4 * m + 2],
                              dd[4 * m + 3]);
             }
-            ptx::tmem_st_wait();
-            ptx::tc_fence_before();
+            ptx::tc_fence_before();         // the dP^T loads precede dQ_t^T over those columns
             ptx::fence_proxy_async_smem();  // dS^T is read by the tensor core next
             __syncwarp();
             if (lane == 0) ptx::bar_arrive(bar(S::kPFull + b));

@@ -422,5 +422,17 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
+// The two 16-bit values of a pack2 word, back in fp32 (exact).
+template <bool BF16>
+__device__ __forceinline__ float unpack_lo(uint32_t w) {
+    if constexpr (BF16) return __uint_as_float(w << 16);
+    else return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+}
+template <bool BF16>
+__device__ __forceinline__ float unpack_hi(uint32_t w) {
+    if constexpr (BF16) return __uint_as_float(w & 0xffff0000u);
+    else return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+
 }  // namespace ptx
 }  // namespace fa

@@ -109,7 +109,7 @@ def _roles(units, single_stage_handoff=False, no_slot_release_wait=False):
             wi += 1
         yield _wait(*unit_slot(len(units))[0::2])
 
-    def product_issuer():  # warp 3: dQ^T, dV, dK
+    def product_issuer():  # warp 3: dV once P^T is in, then dQ^T and dK once dS^T is
         J = wi = 0
         for i, n in enumerate(units):
             yield from take(i)
@@ -117,10 +117,12 @@ def _roles(units, single_stage_handoff=False, no_slot_release_wait=False):
                 continue
             for j in range(n):
                 st, b = J % STAGES, J & 1
-                yield _wait(f"PFull{b}", J >> 1)
+                yield _wait(f"PTFull{b}", J >> 1)
                 if j == 0:
                     yield ("products", wi)  # overwrite the accumulators of unit wi
-                for name in (f"DQFull{b}", f"PTFree{b}", f"QEmpty{st}", f"DSFree{b}"):
+                yield _async(f"PTFree{b}")
+                yield _wait(f"PFull{b}", J >> 1)
+                for name in (f"DQFull{b}", f"QEmpty{st}", f"DSFree{b}"):
                     yield _async(name)
                 J += 1
             yield _async("KVEmpty")
@@ -135,6 +137,7 @@ def _roles(units, single_stage_handoff=False, no_slot_release_wait=False):
                 b = J & 1
                 yield _wait(f"LFull{b}", J >> 1)
                 yield _wait(f"SFull{b}", J >> 1)
+                yield _arrive(f"PTFull{b}")  # P^T in TMEM: dV may start
                 if J >= 2:
                     yield _wait(f"DSFree{b}", (J - 2) >> 1)
                 if j == 0 and i > 0:

@@ -753,7 +753,7 @@ struct ShapeQ64 {
     static constexpr int kKVFull = 0;
     static constexpr int kQFull = 1;       // +stage: Q_j and dO_j landed (TMA)
     static constexpr int kQEmpty = 5;      // +stage: dV_j and dK_j done with them (MMA commit)
-    static constexpr int kSFull = 9;       // +b: S^T and dP^T of the buffer written (MMA commit)
+    static constexpr int kSFull = 9;       // +b: S^T of the buffer written (MMA commit)
     static constexpr int kPFull = 11;      // +b: P^T and dS^T written (8 warps)
     static constexpr int kDQFull = 13;     // +b: dQ_t^T written (MMA commit)
     static constexpr int kBufFree = 15;    // +b: dQ_t^T read out, the buffer's dP^T columns free (4 warps)
@@ -773,7 +773,8 @@ struct ShapeQ64 {
     // a unit's dK/dV written out of every key-row warp's staging block (8 warps)
     static constexpr int kStagingFree = 41;
     static constexpr int kPTFull = 42;     // +b: P^T written (8 warps): dV may start before dS^T is
-    static constexpr int kNumBars = 44;
+    static constexpr int kDPFull = 44;     // +b: dP^T of the buffer written (MMA commit)
+    static constexpr int kNumBars = 46;
     static constexpr int kOffMisc = kNumBars * 8;
     static constexpr int kOffRows = 384;   // + b * 512: float lse2[64], delta[64]
     // + slot * 32: int {live, kt, z, hh, tq0, tk0, Lq, Lk} of a published unit
@@ -1033,6 +1034,8 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
                         const uint64_t qa = (kk / 4) * kQBox16 + (kk % 4) * 2;
                         ptx::mma_ss(tb, k_kmaj + ka, q_kmaj + so + qa, kIdS, kk > 0);
                     }
+                    // the key-row warps exponentiate S^T while dP^T is formed
+                    ptx::mma_commit(bar(S::kSFull + b));
                 }
                 // dP^T: the buffer's dQ_t^T of sub-step J-2 read out
                 if (J >= 2 && !(ok = wait(S::kBufFree + b, ((J - 2) >> 1) & 1))) break;
@@ -1044,7 +1047,7 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
                         const uint64_t qa = (kk / 4) * kQBox16 + (kk % 4) * 2;
                         ptx::mma_ss(tb + 64, v_kmaj + ka, do_kmaj + so + qa, kIdS, kk > 0);
                     }
-                    ptx::mma_commit(bar(S::kSFull + b));
+                    ptx::mma_commit(bar(S::kDPFull + b));
                 }
                 __syncwarp();
               }
@@ -1127,8 +1130,8 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             const int b = J & 1;
             const int qc = qs0 + j * S::kQ + 32 * h;  // first query of this warp's chunk
             const uint32_t tb = tmem + lane_base + S::kTmemBuf + 128 * b;
-            // the sub-step's rows, then S^T and dP^T: one test of both first,
-            // the bounded waits only when one is open
+            // the sub-step's rows, then S^T: one test of both first, the
+            // bounded waits only when one is open
             const bool ready = ptx::bar_try_wait(bar(S::kSFull + b), (J >> 1) & 1) &&
                                ptx::bar_try_wait(bar(S::kLFull + b), (J >> 1) & 1);
             if (!__all_sync(0xffffffffu, ready)) {
@@ -1138,10 +1141,8 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             ptx::tc_fence_after();
             uint32_t sv[32], dpv[32];
             ptx::tmem_ld32(tb + 32 * h, sv);
-            ptx::tmem_ld32(tb + 64 + 32 * h, dpv);
             ptx::tmem_ld_wait();
             ptx::reg_fence(sv);
-            ptx::reg_fence(dpv);
             const bool need_mask = (CAUSAL && key > qc) || key >= u.Lk;
             const int lo = key >= u.Lk ? 32 : (CAUSAL ? key - qc : 0);  // queries i < lo do not see the key
             const float *rows = reinterpret_cast<const float *>(smem_raw + S::kOffRows + b * 2 * S::kQ * 4);
@@ -1167,6 +1168,12 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::bar_arrive(bar(S::kPTFull + b));
+            // dP^T, formed on the tensor core meanwhile
+            if (!(ok = wait(S::kDPFull + b, (J >> 1) & 1))) break;
+            ptx::tc_fence_after();
+            ptx::tmem_ld32(tb + 64 + 32 * h, dpv);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence(dpv);
             // dS = P (dP - D_i), with P as rounded for dV
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {

@@ -103,8 +103,10 @@ def _roles(units, single_stage_handoff=False, no_slot_release_wait=False):
                 yield _wait(f"QFull{st}", J // STAGES)
                 if J >= 2:
                     yield _wait(f"PTFree{b}", (J - 2) >> 1)
+                yield _async(f"SFull{b}")  # S^T
+                if J >= 2:
                     yield _wait(f"BufFree{b}", (J - 2) >> 1)
-                yield _async(f"SFull{b}")
+                yield _async(f"DPFull{b}")  # dP^T
                 J += 1
             wi += 1
         yield _wait(*unit_slot(len(units))[0::2])
@@ -138,6 +140,7 @@ def _roles(units, single_stage_handoff=False, no_slot_release_wait=False):
                 yield _wait(f"LFull{b}", J >> 1)
                 yield _wait(f"SFull{b}", J >> 1)
                 yield _arrive(f"PTFull{b}")  # P^T in TMEM: dV may start
+                yield _wait(f"DPFull{b}", J >> 1)
                 if J >= 2:
                     yield _wait(f"DSFree{b}", (J - 2) >> 1)
                 if j == 0 and i > 0:

@@ -754,7 +754,7 @@ struct ShapeQ64 {
     static constexpr int kQFull = 1;       // +stage: Q_j and dO_j landed (TMA)
     static constexpr int kQEmpty = 5;      // +stage: dV_j and dK_j done with them (MMA commit)
     static constexpr int kSFull = 9;       // +b: S^T of the buffer written (MMA commit)
-    static constexpr int kPFull = 11;      // +b: P^T and dS^T written (8 warps)
+    static constexpr int kPFull = 11;      // +b: dS^T written (8 warps; P^T came earlier, on kPTFull)
     static constexpr int kDQFull = 13;     // +b: dQ_t^T written (MMA commit)
     static constexpr int kBufFree = 15;    // +b: dQ_t^T read out, the buffer's dP^T columns free (4 warps)
     static constexpr int kDSFree = 17;     // +b: products of the buffer done: dS^T no longer read (MMA commit)

@@ -751,7 +751,7 @@ struct ShapeQ64 {
     // small region: barriers, TMEM base and abort flag, then for sub-steps
     // j mod 2 the 64 base-2 LSE values and 64 D values
     static constexpr int kKVFull = 0;
-    static constexpr int kQFull = 1;       // +stage: Q_j and dO_j landed (TMA)
+    static constexpr int kQFull = 1;       // +stage: Q_j landed (TMA)
     static constexpr int kQEmpty = 5;      // +stage: dV_j and dK_j done with them (MMA commit)
     static constexpr int kSFull = 9;       // +b: S^T of the buffer written (MMA commit)
     static constexpr int kPFull = 11;      // +b: dS^T written (8 warps; P^T came earlier, on kPTFull)
@@ -762,7 +762,9 @@ struct ShapeQ64 {
     // the hand-off between them is per stage (a single barrier waited by
     // parity would alias phases two or more apart).
     static constexpr int kStageReady = 19; // +stage: dQ_t staged in its sub-step's stage (4 warps)
-    static constexpr int kStageFree = 23;  // +stage: the bulk reductions have read the stage (1 thread)
+    // The fp32 dQ_t tile's boxes 0, 1 lie over Q_j and boxes 2, 3 over dO_j;
+    // each half of the stage is refilled once the boxes over it are read.
+    static constexpr int kStageFree = 23;  // +stage: the boxes over dO_j read (1 thread)
     static constexpr int kTeardown = 27;
     static constexpr int kPTFree = 28;     // +b: dV of the buffer done, its S^T columns free (MMA commit)
     static constexpr int kLFull = 30;      // +b: the sub-step's LSE and D values landed (bulk copy)
@@ -774,9 +776,11 @@ struct ShapeQ64 {
     static constexpr int kStagingFree = 41;
     static constexpr int kPTFull = 42;     // +b: P^T written (8 warps): dV may start before dS^T is
     static constexpr int kDPFull = 44;     // +b: dP^T of the buffer written (MMA commit)
-    static constexpr int kNumBars = 46;
+    static constexpr int kDOFull = 46;     // +stage: dO_j landed (TMA)
+    static constexpr int kStageFreeQ = 50; // +stage: the boxes over Q_j read (1 thread)
+    static constexpr int kNumBars = 54;
     static constexpr int kOffMisc = kNumBars * 8;
-    static constexpr int kOffRows = 384;   // + b * 512: float lse2[64], delta[64]
+    static constexpr int kOffRows = 448;   // + b * 512: float lse2[64], delta[64]
     // + slot * 32: int {live, kt, z, hh, tq0, tk0, Lq, Lk} of a published unit
     static constexpr int kOffUnits = kOffRows + 2 * 2 * kQ * 4;
     static constexpr int kSmallBytes = kOffUnits + kRing * 32;
@@ -949,19 +953,24 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
             ++wi;
             for (int j = 0; j < n; ++j, ++J) {
                 const int st = J % S::kStages, b = J & 1;
-                // the stage held sub-step J-4's staged dQ_t until its reductions read it
-                if (J >= S::kStages && !(ok = wait(S::kStageFree + st, ((J / S::kStages) - 1) & 1))) break;
+                // each half of the stage held part of sub-step J-4's staged dQ_t
+                // until its reductions read it: Q_J first (S^T needs it), then dO_J
                 const int q0 = qs0 + j * S::kQ;
+                const uint32_t qb = sbase + S::kOffQ + st * S::kStageBytes;
+                int qy, qz;
+                unit_coords<VARLEN>(u, false, q0, qy, qz);
+                if (J >= S::kStages && !(ok = wait(S::kStageFreeQ + st, ((J / S::kStages) - 1) & 1))) break;
                 if (leader && !withheld(p.withhold, static_cast<uint32_t>(J))) {
-                    const uint32_t qb = sbase + S::kOffQ + st * S::kStageBytes;
-                    ptx::bar_arrive_expect_tx(bar(S::kQFull + st), S::kStageBytes);
-                    int qy, qz;
-                    unit_coords<VARLEN>(u, false, q0, qy, qz);
-                    for (int c = 0; c < 2; ++c) {
+                    ptx::bar_arrive_expect_tx(bar(S::kQFull + st), S::kQTileBytes);
+                    for (int c = 0; c < 2; ++c)
                         ptx::tma_load_3d(qb + c * S::kQBoxBytes, &tm_q, bar(S::kQFull + st), c * 64, qy, qz);
-                        ptx::tma_load_3d(qb + S::kQTileBytes + c * S::kQBoxBytes, &tm_do, bar(S::kQFull + st),
+                }
+                if (J >= S::kStages && !(ok = wait(S::kStageFree + st, ((J / S::kStages) - 1) & 1))) break;
+                if (leader) {
+                    ptx::bar_arrive_expect_tx(bar(S::kDOFull + st), S::kQTileBytes);
+                    for (int c = 0; c < 2; ++c)
+                        ptx::tma_load_3d(qb + S::kQTileBytes + c * S::kQBoxBytes, &tm_do, bar(S::kDOFull + st),
                                          c * 64, qy, qz);
-                    }
                 }
                 ++nq;
                 // row buffer b is free once the key-row warps are done with sub-step J-2
@@ -985,6 +994,7 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
         for (int st = 0; st < S::kStages && st < nq; ++st) {
             const int last = (nq - 1) - ((nq - 1 - st) % S::kStages);
             ptx::bar_wait(bar(S::kQFull + st), (last / S::kStages) & 1, nullptr, p.timeout_ns);
+            ptx::bar_wait(bar(S::kDOFull + st), (last / S::kStages) & 1, nullptr, p.timeout_ns);
         }
         for (int b = 0; b < 2 && b < nl; ++b) {
             const int last = (nl - 1) - ((nl - 1 - b) % 2);
@@ -1037,7 +1047,8 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
                     // the key-row warps exponentiate S^T while dP^T is formed
                     ptx::mma_commit(bar(S::kSFull + b));
                 }
-                // dP^T: the buffer's dQ_t^T of sub-step J-2 read out
+                // dP^T: dO_J landed and the buffer's dQ_t^T of sub-step J-2 read out
+                if (!(ok = wait(S::kDOFull + st, (J / S::kStages) & 1))) break;
                 if (J >= 2 && !(ok = wait(S::kBufFree + b, ((J - 2) >> 1) & 1))) break;
                 ptx::tc_fence_after();
                 if (leader) {
@@ -1073,6 +1084,7 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
                 // in columns [32h, 32h+16) of the buffer) as soon as P^T is in:
                 // it frees the buffer's S^T columns for sub-step J+2
                 if (!(ok = wait(S::kPTFull + b, (J >> 1) & 1))) break;
+                if (!(ok = wait(S::kDOFull + st, (J / S::kStages) & 1))) break;  // dV reads dO_J
                 ptx::tc_fence_after();
                 if (leader) {
 #pragma unroll
@@ -1326,10 +1338,14 @@ __global__ void __launch_bounds__(kThreadsQ64, 1)
                 const uint32_t tile = sbase + S::kOffQ + st * S::kStageBytes;
                 int y, z;
                 unit_coords<VARLEN>(u, false, q0, y, z);
-                for (int c = 0; c < D / 32; ++c)
+                // boxes 0, 1 (over Q_J), then 2, 3 (over dO_J), as two groups
+                for (int c = 0; c < D / 32; ++c) {
                     ptx::tma_reduce_add_3d(&tm_dq, tile + c * S::kDQBoxBytes, 32 * c, y, z);
-                ptx::bulk_commit();
-                ptx::bulk_wait_read_all();  // the stage may be refilled now
+                    if (c == 1 || c == D / 32 - 1) ptx::bulk_commit();
+                }
+                ptx::bulk_wait_read_all_but_newest();  // Q's half may be refilled now
+                ptx::bar_arrive(bar(S::kStageFreeQ + st));
+                ptx::bulk_wait_read_all();              // and dO's
                 ptx::bar_arrive(bar(S::kStageFree + st));
             }
             __syncwarp();

@@ -82,9 +82,14 @@ def _roles(units, single_stage_handoff=False, no_slot_release_wait=False):
             yield _async("KVFull")
             for _ in range(n):
                 st, b = J % STAGES, J & 1
+                # Q and dO halves of the stage: each refilled once the dQ
+                # boxes staged over it have been read
+                if J >= STAGES:
+                    yield _wait(f"StageFreeQ{st}", J // STAGES - 1)
+                yield _async(f"QFull{st}")
                 if J >= STAGES:
                     yield _wait(f"StageFree{st}", J // STAGES - 1)
-                yield _async(f"QFull{st}")
+                yield _async(f"DOFull{st}")
                 if J >= 2:
                     yield _wait(f"PFull{b}", (J - 2) >> 1)
                 yield _async(f"LFull{b}")
@@ -104,6 +109,7 @@ def _roles(units, single_stage_handoff=False, no_slot_release_wait=False):
                 if J >= 2:
                     yield _wait(f"PTFree{b}", (J - 2) >> 1)
                 yield _async(f"SFull{b}")  # S^T
+                yield _wait(f"DOFull{st}", J // STAGES)  # dO
                 if J >= 2:
                     yield _wait(f"BufFree{b}", (J - 2) >> 1)
                 yield _async(f"DPFull{b}")  # dP^T
@@ -120,6 +126,7 @@ def _roles(units, single_stage_handoff=False, no_slot_release_wait=False):
             for j in range(n):
                 st, b = J % STAGES, J & 1
                 yield _wait(f"PTFull{b}", J >> 1)
+                yield _wait(f"DOFull{st}", J // STAGES)  # dV reads dO
                 if j == 0:
                     yield ("products", wi)  # overwrite the accumulators of unit wi
                 yield _async(f"PTFree{b}")
@@ -174,7 +181,8 @@ def _roles(units, single_stage_handoff=False, no_slot_release_wait=False):
             for _ in range(n or 0):
                 st = J % STAGES
                 yield _wait(*ready(st, J))
-                yield _async(f"StageFree{st}")
+                yield _async(f"StageFreeQ{st}")  # the boxes over Q read
+                yield _async(f"StageFree{st}")   # the boxes over dO read
                 J += 1
         yield _wait(*unit_slot(len(units))[0::2])
 

@@ -73,7 +73,7 @@ def parse_args(argv=None):
                     help="kernel seconds of the back-to-back prefill leg (0 skips it)")
     ap.add_argument("--parts", default="prefill,decode",
                     help="comma list of the path parts to run (profiling runs may isolate one: prefill, decode, "
-                         "backward, d256, splitd, varlen, varlen_backward, shapes, decode_two)")
+                         "backward, d256, splitd, varlen, varlen_backward, shapes, decode_two, paged)")
     return ap.parse_args(argv)
 
 
@@ -359,7 +359,8 @@ def run_gpu(args, rank, world, local):
     pf_flops = attention_flops(wp.B, wp.H, wp.Sq, wp.Sk, wp.D, wp.causal)
     dc_bytes = decode_bytes(wd.B, wd.H, wd.Sk, wd.D)
 
-    if parts & {"backward", "d256", "splitd", "varlen", "varlen_backward", "shapes", "decode_two"} and not (run_pf or run_dc):
+    if parts & {"backward", "d256", "splitd", "varlen", "varlen_backward", "shapes", "decode_two", "paged"} and \
+            not (run_pf or run_dc):
         # profiling run of the backward pass or of the large-head forwards alone
         rec = {"part": args.parts, "steps": args.steps}
         if "backward" in parts:
@@ -374,6 +375,8 @@ def run_gpu(args, rank, world, local):
             rec["small_prefill"] = run_wide_head(args, fa, torch, dev, stream, flush, world, "small")
         if "varlen_backward" in parts:
             rec["varlen_backward"] = run_varlen_bwd(args, fa, torch, dev, stream, flush, world)
+        if "paged" in parts:
+            rec["paged_decode"] = run_paged(args, fa, torch, stream, dev, flush, world)
         if "shapes" in parts:
             rec["shapes"] = run_shapes(args, fa, torch, dev, stream, flush, world)
         if "decode_two" in parts:

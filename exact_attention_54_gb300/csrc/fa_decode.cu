@@ -32,6 +32,10 @@ namespace fa {
 
 constexpr int kDecodeThreads = 128;
 constexpr int kDecodeUnroll = 8;  // keys in flight per lane group
+// Four CTAs per SM: up to 128 registers a thread, no spills, and 4,096
+// partitions fill 6.7 waves (five CTAs at 96 registers spilled and left the
+// last of 5.4 waves 39 % full; three or two CTAs keep too few bytes in flight).
+constexpr int kDecodeCtasPerSm = 4;
 
 template <bool BF16>
 __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
@@ -149,7 +153,7 @@ __device__ __forceinline__ void merge_head(const float *o_part, const float *m_p
 // outside [0, num_blocks) is never dereferenced: its keys are skipped and the
 // device error word records kDeviceErrBadIndex.
 template <int D, bool BF16, bool PAGED, bool FUSED>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     fa_decode_split_kernel(const DecodeParams p) {
     constexpr int kLanesPerKey = D / 8;                  // 16-byte pieces per key row
     constexpr int kKeysPerWarp = 32 / kLanesPerKey;      // key rows one warp load covers
